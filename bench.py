@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse-attention decode hot path on GB300.
+
+Default workload (the decode indexer + top-k configuration): batch 64, next_n 1,
+64 indexer heads, head_dim 128, page 64, context lengths U[4096, 32768] in a 2x
+oversized shuffled FP8 pool, top-k 2048.  One step = device schedule build +
+paged MQA logits + top-k (3 libdsa launches).  Reported:
+
+* value        K-tokens scored/s (sum of visible lengths / step time / 1e3),
+               inputs resident in HBM, L2 flushed between steps, CUDA events;
+* e2e          the same metric through the public step API with the step's
+               query-side inputs (q, weights, context lengths, block table)
+               copied from pinned host memory and the top-k indices copied back
+               inside the timed region (the K cache is device-resident state);
+* roofline     the logits kernel: algorithmic bytes per launch / its event time
+               vs the measured HBM copy bandwidth;
+* full_step    the whole graph-captured step of the full decode workload
+               (indexer + top-k + sparse MLA, 128 heads 576/512) in us/step;
+* cpu_baseline the fp64 oracle on the host cores over a bounded sample.
+
+``--impl reference`` times the oracle itself (the only reference available
+for this path) on the same workload and metric.
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "indexer K-tokens scored/s & HBM GB/s (%roofline); sparse-attn decode µs/step"
+UNIT = "K-tokens/s"
+WORKLOAD = ("decode indexer + top-k: batch 64, next_n 1, 64 heads, head_dim 128, page 64, "
+            "FP8 e4m3 K cache with fp32 token scale, lens U[4096,32768], 2x shuffled pool, top-k 2048")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def wait_first(self, timeout=3.0):
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.01)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_begin, t_end):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, line in self.lines:
+            if t < t_begin - 0.15 or t > t_end + 0.15:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def scored_pairs(case):
+    L = case.context_lens.cpu().tolist()
+    n = case.next_n
+    from deepseek_sparse_attention_mqa_gb300 import inputs as _  # noqa: F401
+    tot = 0
+    for b, l in enumerate(L):
+        for i in range(n):
+            v = l - n + i + 1
+            tot += max(0, min(v, l))
+    return tot
+
+
+def logits_algorithmic_bytes(case):
+    """Bytes the logits kernel must move: each sequence's visible K rows (values
+    + fp32 scale) once, q and weights once, the visible logits written once."""
+    D, H, n = case.head_dim, case.num_heads, case.next_n
+    L = case.context_lens.cpu().tolist()
+    kv = sum(l * (D + 4) for l in L)
+    q = case.rows * H * D
+    w = case.rows * H * 4
+    out = scored_pairs(case) * 4
+    bt = sum(-(-l // case.page_kv) for l in L) * 4 + len(L) * 4
+    return kv + q + w + out + bt
+
+
+def run_ours(args, rank, world, local):
+    from deepseek_sparse_attention_mqa_gb300 import _abi, build, inputs
+    from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(_abi.LIB_PATH):
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    _abi.lib()
+
+    case = inputs.make_case(args.workload, device=dev)
+    st = SparseAttentionStep(case, with_mla=False)
+    pairs = scored_pairs(case)
+    flush = torch.empty(int(256 * 2 ** 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    status = st.device_status()
+    if status != 0:
+        raise RuntimeError("device status %#x after warm-up" % status)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    for s in range(args.steps):
+        flush.fill_(float(s))                    # evict L2 between steps (256 MiB > 129 MB L2)
+        e = ev[s]
+        c = st.case
+        e[0].record(stream)
+        _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, 0, c.rows, st.sched,
+                            st.status)
+        e[1].record(stream)
+        _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
+                        c.batch, c.next_n, 0, c.rows, st.sched, st.logits, st.width, st.status)
+        e[2].record(stream)
+        st.topk_chunk(0, c.rows)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    logits_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    topk_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    sched_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = pairs * world / (ms_per_step * 1e-3) / 1e3
+
+    clocks = sampler.summary(t_begin, t_end) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # ---- end to end through the public step API, host buffers
+    e2e = None
+    if rank == 0:
+        e2e = measure_e2e(st, case, args, pairs, dev)
+
+    result = None
+    if rank == 0:
+        hbm, bf16, bf16s, src = measured_peaks()
+        lg_bytes = logits_algorithmic_bytes(case)
+        lg_ms = statistics.mean(logits_ms)
+        achieved = lg_bytes / (lg_ms * 1e-3) / 1e9
+        traffic = load_traffic("logits_fp8", args.workload)
+        full = None if args.skip_full_step else measure_full_step(dev, args)
+        result = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": case.batch, "next_n": case.next_n,
+                       "heads": case.num_heads, "head_dim": case.head_dim, "page_kv": case.page_kv,
+                       "topk": case.topk, "scored_pairs_per_step": pairs, "seed": case.meta["seed"],
+                       "l2": "flushed between steps (256 MiB write)", "parallelism": "replicas"},
+            "kernel_ms": {"schedule": round(statistics.mean(sched_ms), 5),
+                          "logits": round(lg_ms, 5), "topk": round(statistics.mean(topk_ms), 5)},
+            "roofline": {"kernel": "logits_fp8 (indexer_mqa_logits_paged)", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "peak_source": src,
+                         "algorithmic_bytes": lg_bytes, "traffic": traffic},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+            "e2e": e2e,
+            "full_step": full,
+        }
+        if not args.skip_cpu:
+            result["cpu_baseline"] = cpu_baseline(case, pairs)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def load_traffic(kernel, workload):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    return d.get("%s/%s" % (kernel, workload))
+
+
+def measure_e2e(st, case, args, pairs, dev):
+    from deepseek_sparse_attention_mqa_gb300 import _abi
+    c = case
+    host = {k: getattr(c, k).cpu().pin_memory() for k in ("q", "weights", "context_lens", "block_table")}
+    idx_host = torch.empty(st.idx.shape, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = idx_host.numel() * 4
+    stream = torch.cuda.current_stream()
+    steps = max(10, args.steps // 4)
+    for _ in range(3):
+        for k, t in host.items():
+            getattr(c, k).copy_(t, non_blocking=True)
+        st.run()
+        idx_host.copy_(st.idx, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(int(256 * 2 ** 20) // 4, dtype=torch.float32, device=dev)
+    tot = 0.0
+    for s in range(steps):
+        flush.fill_(float(s))
+        e0.record(stream)
+        for k, t in host.items():
+            getattr(c, k).copy_(t, non_blocking=True)
+        st.run()
+        idx_host.copy_(st.idx, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    ms = tot / steps
+    return {"value": round(pairs / (ms * 1e-3) / 1e3, 1), "unit": UNIT, "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def measure_full_step(dev, args):
+    """Full decode step of the full-step workload (indexer 4 heads x 32, page 64,
+    lens U[8192,131072], top-k 2048, sparse MLA 128 heads 576/512 on an FP8
+    latent) captured in one CUDA graph; us/step over replays, L2 flushed."""
+    from deepseek_sparse_attention_mqa_gb300 import inputs
+    from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
+    case = inputs.make_case("full_step", device=dev)
+    st = SparseAttentionStep(case, with_mla=True)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            st.run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.run()
+    flush = torch.empty(int(256 * 2 ** 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    n = max(20, min(200, args.steps // 10))
+    for i in range(n + 3):
+        flush.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) * 1e3)
+    status = st.device_status()
+    return {"workload": "full sparse-attention decode step: batch 64, indexer 4 heads x 32 FP8 page 64, "
+                        "lens U[8192,131072], top-k 2048, sparse MLA 128 heads q/k 576 v 512 FP8 latent",
+            "us_per_step_median": round(statistics.median(times), 2),
+            "us_per_step_mean": round(statistics.mean(times), 2), "replays": n,
+            "launches_per_step": st.launches_per_step(), "device_status": status}
+
+
+def cpu_baseline(case, pairs):
+    """fp64 oracle (logits + full-sort top-k) on the host cores, all rows of one step."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import parity
+    cache, _ = parity.oracle_cache(case.kcache, case.block_table)
+    q = case.q.cpu()
+    w = case.weights.cpu()
+    ctx = case.context_lens.cpu()
+    t0 = time.time()
+    lg = oracle.logits_fp8(q, w, cache, ctx, case.next_n, width=case.width)
+    oracle.topk(lg, ctx, case.next_n, case.topk)
+    dt = time.time() - t0
+    return {"value": round(pairs / dt / 1e3, 2), "unit": UNIT, "cores": oracle.threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "one full step of the same workload (all %d rows, %d scored pairs): "
+                      "fp64 logits + full-sort top-k" % (case.rows, pairs)}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed as the reference arm, on the same workload and metric.
+    Each step scores one row of the workload over at most its first 4096 visible
+    tokens (rows taken in turn), so that K steps stay within minutes."""
+    if rank != 0:
+        return None
+    import oracle
+    from deepseek_sparse_attention_mqa_gb300 import inputs
+    oracle.build()
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import parity
+    case = inputs.make_case(args.workload, device="cpu")
+    cache, _ = parity.oracle_cache(case.kcache, case.block_table)
+    q, w = case.q, case.weights
+    n = case.next_n
+    cap = 4096
+    times, pairs_tot = [], 0
+    for s in range(args.warmup + args.steps):
+        r = s % case.rows
+        b = r // n
+        L = min(int(case.context_lens[b]), cap)
+        ctx = torch.tensor([L], dtype=torch.int32)
+        bt_cache = oracle.PagedBytes(cache.values, cache.vps, cache.vts, cache.scales, cache.sps,
+                                     cache.sts, cache.block_table[b:b + 1], cache.page_kv,
+                                     cache.num_pages)
+        t0 = time.time()
+        lg = oracle.logits_fp8(q[b * n:(b + 1) * n], w[b * n:(b + 1) * n], bt_cache, ctx, n,
+                               width=L)
+        oracle.topk(lg, ctx, n, case.topk)
+        dt = time.time() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            pairs_tot += sum(oracle.visible(L, n, i) for i in range(n))
+    tot = sum(times)
+    v = pairs_tot / tot / 1e3
+    ms = tot / len(times) * 1e3
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD,
+                       "sample": "per step one sequence's rows over its first <= %d tokens" % cap},
+            "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "per step one sequence (rows in turn) over its first <= %d "
+                                       "visible tokens: fp64 logits + full-sort top-k" % cap},
+            "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-full-step", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

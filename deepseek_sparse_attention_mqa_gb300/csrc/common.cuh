@@ -1,0 +1,87 @@
+// common.cuh -- definitions shared by the libdsa kernels and their host launchers.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Tokens scored per indexer tile: one tcgen05 M=128 accumulator (one TMEM lane
+// per token).
+constexpr int kTileTokens = 128;
+// Largest MMA N (rows x heads per work unit).
+constexpr int kMaxUnitCols = 256;
+
+// Visible length of draft row i of a sequence of context length L with next_n
+// new tokens: clamp(L - next_n + i + 1, 0, L) ("SM120 FP8 paged MQA page 32",
+// Summary: next_n 1/2/3 + varlen; the context length counts the new tokens).
+__host__ __device__ __forceinline__ int visible_len(int L, int next_n, int i)
+{
+    long long v = static_cast<long long>(L) - next_n + i + 1;
+    v = v < 0 ? 0 : v;
+    return static_cast<int>(v > L ? L : v);
+}
+
+// Rows per work unit for a head count: as many draft rows of one sequence as
+// fit in one MMA N dimension.
+__host__ __device__ __forceinline__ int unit_rows(int next_n, int num_heads)
+{
+    int g = kMaxUnitCols / num_heads;
+    g = g < 1 ? 1 : g;
+    return g < next_n ? g : next_n;
+}
+
+// --------------------------------------------------------------- schedule
+//
+// Layout of the caller-owned schedule buffer (int32 words):
+//   header[0..7]: magic, num_units, rows_per_unit, row_begin, row_end, next_n,
+//                 total_tiles, batch
+//   units[num_units] (16-byte records): first_row (absolute), nrows, seq,
+//                 tile_begin (prefix of 128-token tiles over the units)
+constexpr int32_t kSchedMagic = 0x44534131;  // "DSA1"
+constexpr int kSchedHeaderWords = 8;
+
+struct SchedUnit {
+    int32_t first_row;
+    int32_t nrows;
+    int32_t seq;
+    int32_t tile_begin;
+};
+
+__host__ __device__ __forceinline__ int64_t sched_bytes_for_units(int64_t num_units)
+{
+    return static_cast<int64_t>(kSchedHeaderWords) * 4 + num_units * 16;
+}
+
+// Number of units covering rows [row_begin, row_end): per sequence, the rows it
+// owns in the range, in groups of rows_per_unit.
+__host__ __device__ __forceinline__ int64_t count_units(int batch, int next_n, int rows_per_unit,
+                                                         int row_begin, int row_end)
+{
+    if (row_end <= row_begin)
+        return 0;
+    const int b0 = row_begin / next_n, b1 = (row_end - 1) / next_n;
+    int64_t total = 0;
+    // sequences strictly inside the range own next_n rows each
+    for (int b = b0; b <= b1 && b < batch; ++b) {
+        const int lo = b * next_n > row_begin ? b * next_n : row_begin;
+        const int hi = (b + 1) * next_n < row_end ? (b + 1) * next_n : row_end;
+        total += (hi - lo + rows_per_unit - 1) / rows_per_unit;
+        if (b == b0 && b1 - b0 > 2) {
+            // middle sequences are identical: skip ahead in O(1)
+            const int full = b1 - b0 - 1;
+            total += static_cast<int64_t>(full) * ((next_n + rows_per_unit - 1) / rows_per_unit);
+            b = b1 - 1;
+        }
+    }
+    return total;
+}
+
+// Order-preserving map of an fp32 bit pattern to uint32 (larger float -> larger key).
+__host__ __device__ __forceinline__ uint32_t float_key(uint32_t bits)
+{
+    return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+
+}  // namespace dsa

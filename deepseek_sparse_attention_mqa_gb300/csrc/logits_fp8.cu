@@ -1,0 +1,555 @@
+// logits_fp8.cu -- paged lightning-indexer MQA logits over an FP8 (e4m3) K cache.
+//
+//   logits[r][s] = k_scale[s] * sum_h w[r][h] * relu(q[r][h] . k[s])
+//
+// Prior art on the pages ("SM120 FP8 paged MQA page 32", vllm-project/DeepGEMM #14,
+// Summary and review): one TMA copy per physical page, never a tile that
+// straddles two non-contiguous pages (BLOCK_KV = min(PAGE_KV, 64)), several
+// TMA warps each owning a KV group, 2-3 stages to fit SM120's 99 KiB.
+//
+// GB300 design (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer: per 128-token tile, one 3-D box per physical page
+//               (2 boxes at page 64, 4 at page 32) into a 128B/64B/32B-swizzled
+//               K-major stage, plus one box of per-token fp32 scales per page;
+//               the unit's q rows ([rows x heads, D], K-major) once per unit.
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer, kind::f8f6f4:
+//               D[128 tokens x N] += K_tile[128 x D] * Q[N x D]^T, N = rows x heads.
+//               Each TMEM lane is one token and each column one (row, head).
+//   warps 2-5   epilogue: tcgen05.ld of the thread's own lane, then the whole
+//               relu / head-weighting / k_scale reduction is thread-local (no
+//               shuffles), and each warp stores 32 consecutive logits per row.
+//   Two TMEM accumulators let the epilogue of tile i overlap the MMA of tile i+1;
+//   the stage ring keeps enough K bytes in flight to cover HBM latency.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "host.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kMaxStages = 16;
+constexpr int kThreads = 192;  // 6 warps
+
+struct LogitsParams {
+    const int32_t* sched;
+    const int32_t* context_lens;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int max_pages;
+    int num_pages;
+    int page_kv;
+    int next_n;
+    int row_begin;
+    int row_end;
+    int num_units;
+    int rows_per_unit;
+    const float* weights;
+    float* logits;
+    int64_t logits_stride;
+    int logits_width;
+    int32_t* status;
+    int stages;
+    int n_cols;         // MMA N (multiple of 16)
+    uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= 32, >= n_cols)
+    uint32_t q_buf_bytes;
+};
+
+struct UnitInfo {
+    int seq, first_row, nrows, tile_begin, tile_end, vis_max;
+};
+
+__device__ __forceinline__ UnitInfo load_unit(const LogitsParams& p, const SchedUnit* units,
+                                              int total_tiles, int u)
+{
+    UnitInfo ui;
+    const SchedUnit su = units[u];
+    ui.seq = su.seq;
+    ui.first_row = su.first_row;
+    ui.nrows = su.nrows;
+    ui.tile_begin = su.tile_begin;
+    ui.tile_end = (u + 1 < p.num_units) ? units[u + 1].tile_begin : total_tiles;
+    const int L = max(0, p.context_lens[su.seq]);
+    ui.vis_max = visible_len(L, p.next_n, su.first_row + su.nrows - 1 - su.seq * p.next_n);
+    return ui;
+}
+
+// Last unit whose tile_begin <= t (units with no tiles are skipped naturally).
+__device__ __forceinline__ int find_unit(const SchedUnit* units, int num_units, int t)
+{
+    int lo = 0, hi = num_units - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (units[mid].tile_begin <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Walks this CTA's tiles [t0, t1) unit by unit; identical in every role.
+struct TileWalk {
+    const LogitsParams* p;
+    const SchedUnit* units;
+    int total_tiles;
+    int u;
+    UnitInfo ui;
+    __device__ __forceinline__ void start(const LogitsParams& pp, const SchedUnit* us, int total, int t0)
+    {
+        p = &pp;
+        units = us;
+        total_tiles = total;
+        u = find_unit(us, pp.num_units, t0);
+        ui = load_unit(pp, us, total, u);
+        while (t0 >= ui.tile_end && u + 1 < pp.num_units) {
+            ++u;
+            ui = load_unit(pp, us, total, u);
+        }
+    }
+    // Advance to the unit that owns tile t; returns true if the unit changed.
+    __device__ __forceinline__ bool seek(int t)
+    {
+        bool changed = false;
+        while (t >= ui.tile_end && u + 1 < p->num_units) {
+            ++u;
+            ui = load_unit(*p, units, total_tiles, u);
+            changed = true;
+        }
+        return changed;
+    }
+};
+
+template <int D>
+struct Fp8Tile {
+    static constexpr uint32_t kTileBytes = kTileTokens * D;   // K bytes per stage
+    static constexpr uint32_t kLayout = D == 128 ? kLayoutSw128 : (D == 64 ? kLayoutSw64 : kLayoutSw32);
+    static constexpr uint32_t kSbo = 8 * D;                    // 8 rows per swizzle atom
+    static constexpr int kKSteps = D / 32;                      // K = 32 bytes per MMA
+};
+
+// Shared memory map (offsets from a 1024-aligned base).
+struct SmemMap {
+    uint32_t k_off, q_off, sc_off, w_off, bar_off, misc_off, total;
+};
+
+__host__ __device__ __forceinline__ SmemMap smem_map(int D, int stages, uint32_t q_buf_bytes)
+{
+    SmemMap m;
+    m.k_off = 0;
+    m.q_off = m.k_off + stages * kTileTokens * D;
+    m.sc_off = m.q_off + 2 * q_buf_bytes;
+    m.w_off = m.sc_off + stages * kTileTokens * 4;
+    m.bar_off = m.w_off + 4 * kMaxUnitCols * 4;              // one weight copy per epilogue warp
+    m.misc_off = m.bar_off + (2 * kMaxStages + 8 + 1) * 8;
+    m.total = m.misc_off + 16;
+    return m;
+}
+
+template <int D, int H>
+__global__ void __launch_bounds__(kThreads, 1)
+logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_s,
+                  const __grid_constant__ CUtensorMap tm_q, const LogitsParams p)
+{
+    using T = Fp8Tile<D>;
+    constexpr int kMaxRows = (kMaxUnitCols / H) > 0 ? (kMaxUnitCols / H) : 1;
+    constexpr int kMaxChunks = kMaxUnitCols / 32;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SmemMap mp = smem_map(D, p.stages, p.q_buf_bytes);
+    uint8_t* sK = smem + mp.k_off;
+    uint8_t* sQ = smem + mp.q_off;
+    float* sS = reinterpret_cast<float*>(smem + mp.sc_off);
+    float* sW = reinterpret_cast<float*>(smem + mp.w_off);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + mp.bar_off);
+    uint64_t* full_bar = bars;                       // [stages]
+    uint64_t* empty_bar = bars + kMaxStages;         // [stages]
+    uint64_t* accf_bar = bars + 2 * kMaxStages;      // [2]
+    uint64_t* acce_bar = accf_bar + 2;               // [2]
+    uint64_t* qf_bar = acce_bar + 2;                 // [2]
+    uint64_t* qe_bar = qf_bar + 2;                   // [2]
+    uint64_t* done_bar = qe_bar + 2;                 // [1]
+    volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc_off);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc_off + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- schedule header (uniform over the CTA, checked before any allocation)
+    const int32_t* hdr = p.sched;
+    const SchedUnit* units = reinterpret_cast<const SchedUnit*>(p.sched + kSchedHeaderWords);
+    if (hdr[0] != kSchedMagic || hdr[1] != p.num_units || hdr[2] != p.rows_per_unit ||
+        hdr[3] != p.row_begin || hdr[4] != p.row_end || hdr[5] != p.next_n) {
+        if (threadIdx.x == 0 && p.status)
+            atomicOr(p.status, DSA_DEV_SCHEDULE);
+        return;
+    }
+    const int total_tiles = hdr[6];
+    const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total_tiles) / gridDim.x);
+    const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total_tiles) / gridDim.x);
+    if (t0 >= t1 || p.num_units == 0)
+        return;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1 + 4);   // MMA commit + 4 epilogue warps
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&accf_bar[a]), 1);
+            mbar_init(smem_u32(&acce_bar[a]), 4);
+            mbar_init(smem_u32(&qf_bar[a]), 1);
+            mbar_init(smem_u32(&qe_bar[a]), 1);
+        }
+        mbar_init(smem_u32(done_bar), 1);
+        *s_abort = 0;
+        fence_barrier_init();
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_s);
+        tma_prefetch_map(&tm_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), 2 * p.acc_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *s_tmem;
+    const int P = p.page_kv;
+    const int pages_per_tile = kTileTokens / P;
+
+    if (warp == 0) {
+        // =========================== TMA producer ===========================
+        if (lane == 0) {
+            TileWalk w;
+            w.start(p, units, total_tiles, t0);
+            int stage = 0;
+            uint32_t phase = 0;
+            int ucount = 0;
+            long long issued = 0;
+            for (int t = t0; t < t1 && !*s_abort; ++t) {
+                const bool first = (t == t0);
+                const bool changed = w.seek(t) || first;
+                if (changed) {
+                    const int qb = ucount & 1;
+                    if (!mbar_wait(smem_u32(&qe_bar[qb]), ((ucount >> 1) & 1) ^ 1)) {
+                        *s_abort = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(smem_u32(&qf_bar[qb]), static_cast<uint32_t>(p.n_cols) * D);
+                    tma_load_2d(smem_u32(sQ + qb * p.q_buf_bytes), &tm_q, smem_u32(&qf_bar[qb]), 0,
+                                w.ui.first_row * H);
+                    ++ucount;
+                }
+                if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1)) {
+                    *s_abort = 1;
+                    break;
+                }
+                const int tt = t - w.ui.tile_begin;              // tile index inside the unit
+                int phys[kTileTokens / 32];
+                uint32_t bytes = 0;
+                for (int j = 0; j < pages_per_tile; ++j) {
+                    const int lp = tt * pages_per_tile + j;
+                    phys[j] = -1;
+                    if (lp * P < w.ui.vis_max) {
+                        int pg = -1;
+                        if (lp < p.max_pages)
+                            pg = p.block_table[static_cast<int64_t>(w.ui.seq) * p.bt_stride + lp];
+                        if (pg >= 0 && pg < p.num_pages) {
+                            phys[j] = pg;
+                            bytes += static_cast<uint32_t>(P) * (D + 4);
+                        } else if (p.status) {
+                            atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                        }
+                    }
+                }
+                const uint32_t fb = smem_u32(&full_bar[stage]);
+                mbar_arrive_expect_tx(fb, bytes);
+                for (int j = 0; j < pages_per_tile; ++j) {
+                    if (phys[j] < 0)
+                        continue;
+                    tma_load_3d(smem_u32(sK + stage * T::kTileBytes + j * P * D), &tm_k, fb, 0, 0, phys[j]);
+                    tma_load_2d(smem_u32(sS + stage * kTileTokens + j * P), &tm_s, fb, 0, phys[j]);
+                }
+                ++issued;
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            // drain: every copy this thread issued has landed before the CTA exits
+            const long long lo = issued > p.stages ? issued - p.stages : 0;
+            for (long long j = lo; j < issued; ++j)
+                mbar_wait(smem_u32(&full_bar[j % p.stages]), static_cast<uint32_t>((j / p.stages) & 1));
+            for (int j = ucount > 2 ? ucount - 2 : 0; j < ucount; ++j)
+                mbar_wait(smem_u32(&qf_bar[j & 1]), static_cast<uint32_t>((j >> 1) & 1));
+        }
+    } else if (warp == 1) {
+        // =========================== MMA issuer =============================
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc(0, 0, 0, 128, static_cast<uint32_t>(p.n_cols));
+            TileWalk w;
+            w.start(p, units, total_tiles, t0);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            int ucount = 0, qb = 0;
+            for (int t = t0; t < t1 && !*s_abort; ++t) {
+                const bool changed = w.seek(t) || (t == t0);
+                if (changed) {
+                    qb = ucount & 1;
+                    if (!mbar_wait(smem_u32(&qf_bar[qb]), (ucount >> 1) & 1)) {
+                        *s_abort = 1;
+                        break;
+                    }
+                    ++ucount;
+                }
+                if (!mbar_wait(smem_u32(&acce_bar[acc]), acc_phase ^ 1) ||
+                    !mbar_wait(smem_u32(&full_bar[stage]), phase)) {
+                    *s_abort = 1;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols;
+                const uint32_t a_base = smem_u32(sK + stage * T::kTileBytes);
+                const uint32_t b_base = smem_u32(sQ + qb * p.q_buf_bytes);
+#pragma unroll
+                for (int k = 0; k < T::kKSteps; ++k) {
+                    const uint64_t ad = make_smem_desc(a_base + k * 32, 16, T::kSbo, T::kLayout);
+                    const uint64_t bd = make_smem_desc(b_base + k * 32, 16, T::kSbo, T::kLayout);
+                    umma_f8f6f4(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+                }
+                umma_commit(smem_u32(&empty_bar[stage]));
+                umma_commit(smem_u32(&accf_bar[acc]));
+                const bool unit_ends = (t + 1 == t1) || (t + 1 >= w.ui.tile_end);
+                if (unit_ends)
+                    umma_commit(smem_u32(&qe_bar[qb]));
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            // every MMA issued by this thread has completed before TMEM is released
+            umma_commit(smem_u32(done_bar));
+            mbar_wait(smem_u32(done_bar), 0);
+        }
+    } else {
+        // =========================== epilogue ===============================
+        const int quarter = warp & 3;                 // TMEM lanes this warp may access
+        const int tok = quarter * 32 + lane;          // token of this thread within the tile
+        float* wS = sW + (warp - 2) * kMaxUnitCols;   // this warp's copy of the unit weights
+        TileWalk w;
+        w.start(p, units, total_tiles, t0);
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        int vis[kMaxRows];
+        int ncols_valid = 0;
+        for (int t = t0; t < t1 && !*s_abort; ++t) {
+            const bool changed = w.seek(t) || (t == t0);
+            if (changed) {
+                __syncwarp();
+                ncols_valid = w.ui.nrows * H;
+                const float* wsrc = p.weights + static_cast<int64_t>(w.ui.first_row) * H;
+                for (int c = lane; c < kMaxUnitCols; c += 32)
+                    wS[c] = c < ncols_valid ? wsrc[c] : 0.f;
+                __syncwarp();
+                const int L = max(0, p.context_lens[w.ui.seq]);
+                const int i0 = w.ui.first_row - w.ui.seq * p.next_n;
+#pragma unroll
+                for (int i = 0; i < kMaxRows; ++i) {
+                    int v = i < w.ui.nrows ? visible_len(L, p.next_n, i0 + i) : 0;
+                    if (v > p.logits_width) {
+                        if (p.status)
+                            atomicOr(p.status, DSA_DEV_WIDTH);
+                        v = p.logits_width;
+                    }
+                    vis[i] = v;
+                }
+            }
+            if (!mbar_wait(smem_u32(&full_bar[stage]), phase) ||
+                !mbar_wait(smem_u32(&accf_bar[acc]), acc_phase)) {
+                *s_abort = 1;
+                break;
+            }
+            tc_fence_after_sync();
+            const float kscale = sS[stage * kTileTokens + tok];
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&empty_bar[stage]));
+
+            float sums[kMaxRows];
+#pragma unroll
+            for (int i = 0; i < kMaxRows; ++i)
+                sums[i] = 0.f;
+            const uint32_t t_acc = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols +
+                                   (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll
+            for (int c = 0; c < kMaxChunks; ++c) {
+                if (c * 32 < ncols_valid) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_acc + c * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = c * 32 + j;
+                        if (col < ncols_valid)
+                            sums[col / H] = fmaf(wS[col], fmaxf(__uint_as_float(r[j]), 0.f), sums[col / H]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&acce_bar[acc]));
+
+            const int s = (t - w.ui.tile_begin) * kTileTokens + tok;
+#pragma unroll
+            for (int i = 0; i < kMaxRows; ++i) {
+                if (i < w.ui.nrows && s < vis[i]) {
+                    const int64_t row = w.ui.first_row + i - p.row_begin;
+                    p.logits[row * p.logits_stride + s] = kscale * sums[i];
+                }
+            }
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1;
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    __syncwarp();
+    if (threadIdx.x == 0 && *s_abort && p.status)
+        atomicOr(p.status, DSA_DEV_TIMEOUT);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1)
+        tmem_dealloc(tmem_base, 2 * p.acc_cols);
+}
+
+template <int D, int H>
+dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    const dsa_paged_cache* k = a.k;
+    const int P = k->page_kv;
+    const int G = a.rows_per_unit;
+    const int n_cols = ((G * H + 15) / 16) * 16;
+    uint32_t acc_cols = 32;
+    while (acc_cols < static_cast<uint32_t>(n_cols))
+        acc_cols <<= 1;
+    const uint32_t q_buf_bytes = ((static_cast<uint32_t>(n_cols) * D + 1023u) / 1024u) * 1024u;
+
+    // tensor maps: K values [num_pages][P][D] bytes, scales [num_pages][P] fp32,
+    // q [rows_total*H][D] bytes
+    CUtensorMap tm_k, tm_s, tm_q;
+    const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                           : (D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(P),
+                                  static_cast<uint64_t>(k->num_pages)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(k->val_token_stride),
+                                     static_cast<uint64_t>(k->val_page_stride)};
+        const uint32_t box[3] = {static_cast<uint32_t>(D), static_cast<uint32_t>(P), 1};
+        dsa_status st = encode_tiled(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k->values, dims, strides, box, sw);
+        if (st != DSA_OK)
+            return st;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(P), static_cast<uint64_t>(k->num_pages)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(k->sc_page_stride)};
+        const uint32_t box[2] = {static_cast<uint32_t>(P), 1};
+        dsa_status st = encode_tiled(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, k->scales, dims, strides, box,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != DSA_OK)
+            return st;
+    }
+    {
+        const uint64_t rows_total = static_cast<uint64_t>(a.batch) * a.next_n * H;
+        const uint64_t dims[2] = {static_cast<uint64_t>(D), rows_total};
+        const uint64_t strides[1] = {static_cast<uint64_t>(D)};
+        const uint32_t box[2] = {static_cast<uint32_t>(D), static_cast<uint32_t>(n_cols)};
+        dsa_status st = encode_tiled(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q, dims, strides, box, sw);
+        if (st != DSA_OK)
+            return st;
+    }
+
+    // as many stages as fit next to the q buffers
+    const int budget = std::min(dev.max_smem_optin, 227 * 1024) - 1024;
+    int stages = kMaxStages;
+    while (stages > 2 && static_cast<int>(smem_map(D, stages, q_buf_bytes).total) > budget)
+        --stages;
+    const SmemMap mp = smem_map(D, stages, q_buf_bytes);
+    if (static_cast<int>(mp.total) > budget)
+        return DSA_ERR_UNSUPPORTED;
+    const int smem_bytes = static_cast<int>(mp.total) + 1024;
+
+    LogitsParams p;
+    p.sched = a.sched;
+    p.context_lens = a.context_lens;
+    p.block_table = k->block_table;
+    p.bt_stride = k->bt_row_stride;
+    p.max_pages = k->max_pages_per_seq;
+    p.num_pages = k->num_pages;
+    p.page_kv = P;
+    p.next_n = a.next_n;
+    p.row_begin = a.row_begin;
+    p.row_end = a.row_end;
+    p.num_units = a.num_units;
+    p.rows_per_unit = G;
+    p.weights = a.weights;
+    p.logits = a.logits;
+    p.logits_stride = a.logits_row_stride;
+    p.logits_width = a.logits_width;
+    p.status = a.status;
+    p.stages = stages;
+    p.n_cols = n_cols;
+    p.acc_cols = acc_cols;
+    p.q_buf_bytes = q_buf_bytes;
+
+    auto kern = logits_fp8_kernel<D, H>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    kern<<<dev.sm_count, kThreads, smem_bytes, stream>>>(tm_k, tm_s, tm_q, p);
+    return check_launch();
+}
+
+template <int D>
+dsa_status launch_fp8_d(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    switch (a.num_heads) {
+    case 4: return launch_fp8_dh<D, 4>(a, dev, stream);
+    case 8: return launch_fp8_dh<D, 8>(a, dev, stream);
+    case 16: return launch_fp8_dh<D, 16>(a, dev, stream);
+    case 32: return launch_fp8_dh<D, 32>(a, dev, stream);
+    case 64: return launch_fp8_dh<D, 64>(a, dev, stream);
+    case 128: return launch_fp8_dh<D, 128>(a, dev, stream);
+    default: return DSA_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+dsa_status launch_logits_fp8(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    switch (a.k->head_dim) {
+    case 32: return launch_fp8_d<32>(a, dev, stream);
+    case 64: return launch_fp8_d<64>(a, dev, stream);
+    case 128: return launch_fp8_d<128>(a, dev, stream);
+    default: return DSA_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace dsa

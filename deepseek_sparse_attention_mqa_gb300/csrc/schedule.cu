@@ -1,0 +1,138 @@
+// schedule.cu -- device-side indexer schedule builder.
+//
+// "feat(deepseek_v4): Add fp4 indexer for dsv4" (ROCm/ATOM #1709), commit notes:
+// the decode indexer schedule is produced by a single kernel directly into a
+// fixed-address CUDA-graph buffer (instead of ~50 small launches plus a copy),
+// and the scoring kernel consumes it instead of building its own; it records
+// absolute row ids, so every prefill chunk has its own schedule.
+//
+// Here one CTA turns the device-resident context lengths into the unit list
+// (rows of one sequence that share an MMA N dimension) and the prefix of
+// 128-token tiles over the units.  Everything that depends only on host-known
+// values (unit boundaries) is recomputed on the device too, so the buffer is
+// self-contained and valid for every graph replay.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "host.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kSchedThreads = 1024;
+
+// Unit u -> (sequence, first absolute row, rows) for rows [row_begin, row_end).
+__device__ __forceinline__ void unit_rows_of(int u, int next_n, int G, int row_begin, int row_end,
+                                             int* seq, int* first_row, int* nrows)
+{
+    const int b0 = row_begin / next_n;
+    const int lo0 = row_begin;
+    const int hi0 = min((b0 + 1) * next_n, row_end);
+    const int u_first = (hi0 - lo0 + G - 1) / G;
+    const int U = (next_n + G - 1) / G;  // units of a sequence fully inside the range
+    int b, lo, hi, j;
+    if (u < u_first) {
+        b = b0;
+        lo = lo0;
+        hi = hi0;
+        j = u;
+    } else {
+        b = b0 + 1 + (u - u_first) / U;
+        j = (u - u_first) % U;
+        lo = b * next_n;
+        hi = min((b + 1) * next_n, row_end);
+    }
+    *seq = b;
+    *first_row = lo + j * G;
+    *nrows = min(G, hi - *first_row);
+}
+
+__global__ void __launch_bounds__(kSchedThreads)
+build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int next_n, int G,
+                      int row_begin, int row_end, int num_units, int32_t* __restrict__ sched,
+                      int32_t* __restrict__ status)
+{
+    __shared__ int32_t warp_tot[kSchedThreads / 32];
+    __shared__ int32_t carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    SchedUnit* units = reinterpret_cast<SchedUnit*>(sched + kSchedHeaderWords);
+    if (tid == 0)
+        carry_s = 0;
+    __syncthreads();
+
+    for (int base = 0; base < num_units; base += kSchedThreads) {
+        const int u = base + tid;
+        int seq = 0, first_row = 0, nrows = 0, tiles = 0;
+        if (u < num_units) {
+            unit_rows_of(u, next_n, G, row_begin, row_end, &seq, &first_row, &nrows);
+            if (seq < batch && nrows > 0) {
+                const int L = context_lens[seq];
+                const int last_i = first_row + nrows - 1 - seq * next_n;
+                const int vis = visible_len(L < 0 ? 0 : L, next_n, last_i);
+                tiles = (vis + kTileTokens - 1) / kTileTokens;
+            } else if (status) {
+                atomicOr(status, DSA_DEV_SCHEDULE);
+            }
+        }
+        // block-wide exclusive scan of tiles
+        int incl = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        if (lane == 31)
+            warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int t = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o)
+                    t += v;
+            }
+            warp_tot[lane] = t;   // inclusive over warps
+        }
+        __syncthreads();
+        const int carry = carry_s;
+        const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - tiles;
+        if (u < num_units) {
+            SchedUnit su;
+            su.first_row = first_row;
+            su.nrows = nrows;
+            su.seq = seq;
+            su.tile_begin = excl;
+            units[u] = su;
+        }
+        __syncthreads();
+        if (tid == 0)
+            carry_s = carry + warp_tot[31];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        sched[0] = kSchedMagic;
+        sched[1] = num_units;
+        sched[2] = G;
+        sched[3] = row_begin;
+        sched[4] = row_end;
+        sched[5] = next_n;
+        sched[6] = carry_s;
+        sched[7] = batch;
+    }
+}
+
+}  // namespace
+
+dsa_status launch_build_schedule(const int32_t* context_lens, int batch, int next_n,
+                                 int rows_per_unit, int row_begin, int row_end, int num_units,
+                                 int32_t* sched, int32_t* status, cudaStream_t stream)
+{
+    build_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(context_lens, batch, next_n,
+                                                           rows_per_unit, row_begin, row_end,
+                                                           num_units, sched, status);
+    return check_launch();
+}
+
+}  // namespace dsa

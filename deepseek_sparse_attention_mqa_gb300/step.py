@@ -1,0 +1,94 @@
+"""One sparse-attention step over caller-owned device buffers.
+
+A step is: build the indexer schedule on the device, score the paged
+lightning-indexer logits, select the per-row top-k, and (when the workload has
+an MLA stage) run sparse MLA decode over the selected latent tokens.  Prefill
+rows are processed in chunks so that the fp32 logits buffer stays within a
+byte budget ("feat(deepseek_v4): Add fp4 indexer for dsv4", prefill notes:
+logits width = the actual longest visible length, Q-row budget chunking, one
+schedule per chunk).  Every step of the computation runs in libdsa; this
+module only allocates buffers once and issues the C-ABI calls in order, so the
+whole step can be captured in one CUDA graph.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+from .inputs import Case
+
+LOGITS_BUDGET_BYTES = 512 * 1024 * 1024   # 512 MiB
+
+
+class SparseAttentionStep:
+    def __init__(self, case: Case, with_mla: bool = True, budget_bytes: int = LOGITS_BUDGET_BYTES,
+                 rows_per_chunk: int | None = None):
+        dev = case.q.device
+        assert dev.type == "cuda", "SparseAttentionStep needs the case on a CUDA device"
+        self.case = case
+        c = case
+        self.rows = c.rows
+        self.width = int(c.width)
+        if rows_per_chunk is None:
+            rows_per_chunk = max(1, min(self.rows, budget_bytes // (4 * max(1, self.width))))
+        self.rows_per_chunk = int(rows_per_chunk)
+        self.chunks = [(rb, min(self.rows, rb + self.rows_per_chunk))
+                       for rb in range(0, self.rows, self.rows_per_chunk)] or [(0, 0)]
+        kc = c.kcache
+        self.kcache = _abi.make_cache(kc.fmt, kc.head_dim, kc.page_kv, kc.num_pages, kc.values,
+                                      kc.val_page_stride, kc.val_token_stride, kc.scales,
+                                      kc.sc_page_stride, kc.sc_token_stride, c.block_table)
+        sb = max(_abi.schedule_bytes(c.batch, c.next_n, c.num_heads, rb, re) for rb, re in self.chunks)
+        self.sched = torch.empty((sb + 15) // 16 * 4, dtype=torch.int32, device=dev)
+        self.logits = torch.empty((self.rows_per_chunk, max(1, self.width)), dtype=torch.float32,
+                                  device=dev)
+        self.idx = torch.empty((self.rows, c.topk), dtype=torch.int32, device=dev)
+        self.count = torch.empty((self.rows,), dtype=torch.int32, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        tw = _abi.topk_workspace_bytes(self.rows_per_chunk, self.width, c.topk)
+        self.topk_ws = torch.empty((max(tw, 16),), dtype=torch.uint8, device=dev)
+        self.with_mla = bool(with_mla and c.latent is not None)
+        if self.with_mla:
+            lat = c.latent
+            self.latent = _abi.make_cache(lat.fmt, lat.head_dim, lat.page_kv, lat.num_pages,
+                                          lat.values, lat.val_page_stride, lat.val_token_stride,
+                                          lat.scales, lat.sc_page_stride, lat.sc_token_stride,
+                                          c.block_table)
+            self.out = torch.empty((self.rows, c.mla_heads, c.d_v), dtype=torch.bfloat16, device=dev)
+            self.lse = torch.empty((self.rows, c.mla_heads), dtype=torch.float32, device=dev)
+            mw = _abi.mla_workspace_bytes(self.rows, c.mla_heads, c.d_qk, c.d_v, c.topk)
+            self.mla_ws = torch.empty((max(mw, 16),), dtype=torch.uint8, device=dev)
+
+    # ------------------------------------------------------------------ stages
+    def indexer_chunk(self, rb: int, re: int, stream=None):
+        c = self.case
+        _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, self.sched,
+                            self.status, stream)
+        _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, self.kcache,
+                        c.context_lens, c.batch, c.next_n, rb, re, self.sched, self.logits,
+                        self.width, self.status, stream)
+
+    def topk_chunk(self, rb: int, re: int, stream=None):
+        c = self.case
+        _abi.topk(self.logits, self.width, c.context_lens, c.batch, c.next_n, rb, re, c.topk,
+                  self.idx[rb:re], self.count[rb:re], self.topk_ws, self.status, stream)
+
+    def mla(self, stream=None):
+        c = self.case
+        _abi.sparse_mla(c.q_mla, c.softmax_scale, self.latent, self.idx, c.topk, self.out,
+                        self.lse, c.d_v, None, c.next_n, self.mla_ws, self.status, stream)
+
+    def run(self, stream=None):
+        for rb, re in self.chunks:
+            if re > rb:
+                self.indexer_chunk(rb, re, stream)
+                self.topk_chunk(rb, re, stream)
+        if self.with_mla:
+            self.mla(stream)
+
+    def launches_per_step(self) -> int:
+        n = sum(3 for rb, re in self.chunks if re > rb)
+        return n + (1 if self.with_mla else 0)
+
+    def device_status(self) -> int:
+        return _abi.device_status(self.status)

@@ -1,0 +1,233 @@
+/*
+ * dsa.h -- C ABI of libdsa, the GB300 (sm_103a) DeepSeek sparse-attention
+ * decode path: paged lightning-indexer MQA logits, per-row top-k, sparse MLA
+ * decode, and a device-side schedule builder for CUDA-graph capture.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or retains them past the call.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *    void*, NULL = legacy default stream).  No entry point synchronises or reads
+ *    device memory from the host, except dsa_get_device_status().  Every
+ *    compute entry point may therefore be captured into a CUDA graph.
+ *  - Strides are in BYTES unless stated otherwise.
+ *  - Arguments are validated on the host before anything is enqueued; an
+ *    invalid call returns an error code and enqueues nothing.  Conditions that
+ *    only the device can see (a block-table entry out of range, a visible
+ *    length above the logits width, an index outside the block table) make the
+ *    kernel skip the offending access and OR a bit into the caller's int32
+ *    status word `status_dev` (nullable = not reported).
+ *  - The library is stateless apart from a per-thread record of the last CUDA
+ *    error (dsa_last_cuda_error) and is safe to call from several threads.
+ *
+ * Sources: "SM120 FP8 paged MQA page 32" (vllm-project/DeepGEMM #14), Summary:
+ * FP8 paged MQA logits with block_kv 32/64, next_n >= 1, varlen; "feat(deepseek_v4):
+ * Add fp4 indexer for dsv4" (ROCm/ATOM #1709), commit notes: FP4 indexer,
+ * indexer_score_topk, schedule built into a fixed-address CUDA-graph buffer,
+ * prefill logits width and Q-row budget chunking; "Add DeepSeek V4 sparse MLA
+ * TRTLLM-GEN kernels" (flashinfer #3269): sparse MLA decode over top-k indices.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride / alignment */
+    DSA_ERR_UNSUPPORTED = 2, /* shape or format this build has no kernel for; wrong GPU arch */
+    DSA_ERR_CAPACITY = 3,    /* a caller buffer (schedule, workspace) is too small */
+    DSA_ERR_CUDA = 4         /* a CUDA call failed; see dsa_last_cuda_error() */
+} dsa_status;
+
+/* Storage formats of a paged cache. */
+typedef enum {
+    DSA_KV_FP8_E4M3 = 0, /* e4m3 values + one fp32 scale per token */
+    DSA_KV_MXFP4 = 1,    /* packed e2m1 values (even element in the low nibble) +
+                            one ue8m0 scale per 32 elements */
+    DSA_KV_BF16 = 2      /* bf16 values, no scale */
+} dsa_format;
+
+/* Bits OR-ed into the caller's device status word. */
+#define DSA_DEV_BAD_PAGE 0x1  /* block_table entry outside [0, num_pages): access skipped */
+#define DSA_DEV_WIDTH 0x2     /* visible length > logits_width: clipped to the width */
+#define DSA_DEV_TIMEOUT 0x4   /* a bounded on-chip wait gave up; outputs are invalid */
+#define DSA_DEV_BAD_INDEX 0x8 /* top-k index beyond the block table: token skipped */
+#define DSA_DEV_SCHEDULE 0x10 /* schedule buffer does not describe this call */
+
+/*
+ * One paged cache.  Token t (0 <= t < page_kv) of physical page p has its
+ * values at  values + p*val_page_stride + t*val_token_stride  and its scales at
+ * scales + p*sc_page_stride + t*sc_token_stride.  Logical token s of sequence b
+ * lives in physical page block_table[b*bt_row_stride + s/page_kv], row s%page_kv
+ * (the paged layout of "SM120 FP8 paged MQA page 32", Summary: shuffled physical
+ * pages, padded page strides).  Values and scales may share one allocation
+ * (the "fused" cache: scales after the page's values).
+ *
+ * Alignment required by the tensor-memory-access (TMA) paths: values, scales
+ * and the page strides 16-byte aligned; val_token_stride == the dense row size
+ * (head_dim bytes for FP8, head_dim/2 for MXFP4, 2*head_dim for BF16);
+ * sc_token_stride == 4 (FP8) or head_dim/32 (MXFP4).
+ */
+typedef struct {
+    int32_t fmt;               /* dsa_format */
+    int32_t head_dim;          /* elements per token */
+    int32_t page_kv;           /* tokens per page: 32 or 64 */
+    int32_t num_pages;         /* pages in the pool */
+    const void* values;        /* device */
+    int64_t val_page_stride;   /* bytes */
+    int64_t val_token_stride;  /* bytes */
+    const void* scales;        /* device; NULL for BF16 */
+    int64_t sc_page_stride;    /* bytes */
+    int64_t sc_token_stride;   /* bytes */
+    const int32_t* block_table; /* device, [batch, bt_row_stride] int32 */
+    int64_t bt_row_stride;     /* ELEMENTS between sequences' rows */
+    int32_t max_pages_per_seq; /* valid columns of each block-table row */
+} dsa_paged_cache;
+
+/* Human-readable name of a status code (static string, never NULL). */
+DSA_API const char* dsa_status_string(dsa_status status);
+
+/* cudaError_t of the last failed CUDA call made by this thread (0 = none). */
+DSA_API int dsa_last_cuda_error(void);
+
+/* Library ABI version (major*100 + minor). */
+DSA_API int dsa_version(void);
+
+/*
+ * Indexer schedule ("feat(deepseek_v4): Add fp4 indexer for dsv4", commit notes:
+ * the decode schedule is built by one kernel straight into a fixed-address
+ * CUDA-graph buffer and the logits kernel then skips its own build; cta_info
+ * holds absolute row ids, so each prefill chunk needs its own schedule).
+ *
+ * The rows [row_begin, row_end) of a batch (row r = sequence r/next_n, draft
+ * position r%next_n) are grouped into work units of at most
+ * max(1, min(next_n, 256/num_heads)) consecutive rows of one sequence; each unit
+ * is split into 128-token tiles up to the largest visible length of its rows.
+ * dsa_indexer_schedule_bytes() gives the buffer size for a call shape (it
+ * depends only on host-known values); dsa_indexer_build_schedule() fills it on
+ * the device from the device-resident context_lens, so the buffer can be built
+ * inside a captured graph at every replay.
+ *
+ * context_lens: device int32 [batch], lengths INCLUDING the next_n new tokens.
+ * sched: device buffer of at least dsa_indexer_schedule_bytes(...) bytes,
+ *        16-byte aligned, caller-owned; its contents are opaque.
+ * Errors: DSA_ERR_INVALID_ARG (sizes, row range, null pointers),
+ *         DSA_ERR_CAPACITY (sched_bytes too small).
+ */
+DSA_API size_t dsa_indexer_schedule_bytes(int batch, int next_n, int num_heads, int row_begin,
+                                  int row_end);
+DSA_API dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int batch, int next_n,
+                                      int num_heads, int row_begin, int row_end, void* sched,
+                                      size_t sched_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * Paged lightning-indexer MQA logits (DeepSeek sparse attention):
+ *   logits[r - row_begin][s] = k_scale[s] * sum_h w[r][h] * relu(sum_d q[r][h][d] * k[s][d])
+ * for row_begin <= r < row_end and 0 <= s < vis(r), where for sequence
+ * b = r/next_n, draft position i = r%next_n and L = context_lens[b]:
+ *   vis(r) = clamp(L - next_n + i + 1, 0, L)
+ * (next_n = 1: all L tokens; a causal prefill is batch 1, next_n = L).
+ * Entries at s >= vis(r) are left untouched.
+ *
+ * q:        FP8:   [rows_total, num_heads, head_dim] e4m3 bytes (absolute rows).
+ *           MXFP4: [rows_total, num_heads, head_dim/2] packed e2m1, with
+ * q_scales: [rows_total, num_heads, head_dim/32] ue8m0 (MXFP4 only, else NULL).
+ * q_fmt:    must equal k->fmt (DSA_KV_FP8_E4M3 or DSA_KV_MXFP4).
+ * weights:  fp32 [rows_total, num_heads].
+ * k:        the paged indexer K cache; FP8 caches carry k_scale per token,
+ *           MXFP4 caches carry block scales only (k_scale = 1).
+ * sched:    built by dsa_indexer_build_schedule() with the same batch, next_n,
+ *           num_heads, row_begin, row_end (and current context_lens).
+ * logits:   fp32, row (r - row_begin) at logits + (r-row_begin)*logits_row_stride
+ *           (ELEMENTS); logits_width = columns available per row.  A decode
+ *           step under graph capture keeps a fixed width; a prefill sizes it to
+ *           the actual longest visible length ("Add fp4 indexer for dsv4",
+ *           prefill logits width note).
+ * Supported: head_dim in {32, 64, 128}; num_heads in {4, 8, 16, 32, 64, 128};
+ *           page_kv in {32, 64}; FP8 and MXFP4 (MXFP4 needs head_dim % 32 == 0).
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (sched_bytes), CUDA.
+ */
+DSA_API dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_fmt,
+                                    const float* weights, int num_heads,
+                                    const dsa_paged_cache* k, const int32_t* context_lens,
+                                    int batch, int next_n, int row_begin, int row_end,
+                                    const void* sched, size_t sched_bytes, float* logits,
+                                    int64_t logits_row_stride, int logits_width,
+                                    int32_t* status_dev, void* stream);
+
+/*
+ * Per-row top-k of the indexer logits ("feat(deepseek_v4): Add fp4 indexer for
+ * dsv4": indexer_score_topk; "Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels":
+ * dynamic per-row top-k lengths).  For each row, the k largest of
+ * logits[row][0 : vis(row)) (vis as above, clipped to logits_width) are
+ * selected; idx[row][0 : min(k, vis)) receives their token positions (the
+ * order within a row is unspecified; this implementation writes ascending
+ * positions) and idx[row][min(k, vis) : k) receives -1.  Among exactly equal
+ * logits the lower position wins.  count (nullable) receives min(k, vis).
+ *
+ * logits:   as produced by indexer_mqa_logits_paged (row stride in ELEMENTS).
+ * idx:      int32 [rows, idx_row_stride >= k] (stride in ELEMENTS).
+ * workspace: device scratch of dsa_topk_workspace_bytes(...) bytes (may be 0,
+ *           then workspace may be NULL).
+ * Supported: 1 <= k <= 16384.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (workspace), CUDA.
+ */
+DSA_API size_t dsa_topk_workspace_bytes(int rows, int logits_width, int k);
+DSA_API dsa_status indexer_topk(const float* logits, int64_t logits_row_stride, int logits_width,
+                        const int32_t* context_lens, int batch, int next_n, int row_begin,
+                        int row_end, int k, int32_t* idx, int64_t idx_row_stride,
+                        int32_t* count, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                        void* stream);
+
+/*
+ * Sparse MLA decode ("Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels":
+ * trtllm_batch_decode_sparse_mla over top-k selected latent tokens, bf16 output
+ * + LSE).  For row r (sequence b = seq_of_row ? seq_of_row[r] : r/next_n) and
+ * head h, over the valid entries j (idx[r][j] >= 0) with latent rows
+ * c_j = decode(latent[b][idx[r][j]]) * token_scale:
+ *   s_j = softmax_scale * sum_{d < d_qk} q[r][h][d] * c_j[d]
+ *   lse[r][h] = ln sum_j exp(s_j)                 (natural log)
+ *   out[r][h][e] = sum_j exp(s_j - lse) * c_j[e]  for e < d_v
+ * A row with no valid index gets out = 0 and lse = -inf.
+ *
+ * q_bf16:   bf16 [rows, num_heads, d_qk].
+ * kv:       the paged latent cache (FP8 + fp32 token scale, or BF16) with
+ *           head_dim == d_qk; the value vector is its first d_v elements.
+ * idx:      int32 [rows, idx_row_stride >= k] (ELEMENTS), logical positions.
+ * out_bf16: bf16 [rows, num_heads, d_v]; lse: fp32 [rows, num_heads].
+ * workspace: device scratch of dsa_sparse_mla_workspace_bytes(...) bytes.
+ * Supported: d_v <= d_qk <= 1024, d_qk % 16 == 0, d_v % 16 == 0.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (workspace), CUDA.
+ */
+DSA_API size_t dsa_sparse_mla_workspace_bytes(int rows, int num_heads, int d_qk, int d_v, int k);
+DSA_API dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads, int d_qk, int d_v,
+                             float softmax_scale, const dsa_paged_cache* kv,
+                             const int32_t* seq_of_row, int next_n, const int32_t* idx,
+                             int64_t idx_row_stride, int k, void* out_bf16, float* lse,
+                             void* workspace, size_t ws_bytes, int32_t* status_dev,
+                             void* stream);
+
+/*
+ * Opt-in, SYNCHRONISING read of a device status word: waits for `stream`,
+ * copies *status_dev into *host_out.  Never called by the other entry points.
+ */
+DSA_API dsa_status dsa_get_device_status(const int32_t* status_dev, int32_t* host_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,162 @@
+"""GPU parity of the indexer schedule + paged MQA logits (libdsa, tcgen05/TMA)
+against the fp64 oracle, element by element, plus device-status behaviour.
+
+Case matrix after "SM120 FP8 paged MQA page 32" (Validation): page 32/64 x
+heads 16/32/64 x next_n 1/2/3 x head_dim 32/64/128, shuffled physical pages,
+padded strides, empty history, partial pages; plus heads 4/8/128, a chunked
+causal prefill, and the full-size decode workload checked on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from deepseek_sparse_attention_mqa_gb300 import _abi, build, inputs
+from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    _abi.lib()
+    oracle.build()
+
+
+def gpu_logits(case, rows_per_chunk=None, width=None):
+    """Run schedule + logits for every chunk; returns (rows list, step)."""
+    st = SparseAttentionStep(case, with_mla=False, rows_per_chunk=rows_per_chunk)
+    if width is not None:
+        st.width = width
+    rows = []
+    for rb, re in st.chunks:
+        if re == rb:
+            continue
+        st.logits.fill_(float("nan"))
+        st.indexer_chunk(rb, re)
+        torch.cuda.synchronize()
+        rows.extend(list(st.logits[:re - rb].cpu().numpy()))
+    return rows, st
+
+
+def oracle_logits(case, rows=None):
+    cache, _ = parity.oracle_cache(case.kcache, case.block_table)
+    ctx = case.context_lens.cpu()
+    if case.fmt == inputs.FMT_FP8:
+        fn = lambda rb, re: oracle.logits_fp8(case.q.cpu(), case.weights.cpu(), cache, ctx,
+                                              case.next_n, rb, re, width=case.width)
+    else:
+        fn = lambda rb, re: oracle.logits_mxfp4(case.q.cpu(), case.q_scales.cpu(),
+                                                case.weights.cpu(), cache, ctx, case.next_n, rb,
+                                                re, width=case.width)
+    if rows is None:
+        return list(fn(0, case.rows))
+    return [fn(r, r + 1)[0] for r in rows]
+
+
+def compare_all(case, rows_per_chunk=None):
+    g, st = gpu_logits(case, rows_per_chunk)
+    o = oracle_logits(case)
+    vis = [parity.visible(case, r) for r in range(case.rows)]
+    worst, tol = parity.check_logits(g, o, vis)
+    for r, v in enumerate(vis):                       # nothing written past the window
+        assert np.all(np.isnan(g[r][v:])), "row %d written past its visible length" % r
+    assert st.device_status() == 0
+    return worst, tol
+
+
+def test_tiny_workload():
+    case = inputs.make_case("tiny", device="cuda", with_mla=False)
+    compare_all(case)
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("next_n", [1, 2, 3])
+@pytest.mark.parametrize("H", [16, 32, 64])
+@pytest.mark.parametrize("P", [32, 64])
+def test_matrix(P, H, next_n, D):
+    lens = [0, 1, 63, 64, 65, 200, 511]
+    case = inputs.make_case("decode", device="cuda", lens=lens, next_n=next_n, page_kv=P,
+                            num_heads=H, head_dim=D, width=600, pool_factor=2,
+                            seed=1000 + P + H + next_n + D)
+    compare_all(case)
+
+
+@pytest.mark.parametrize("H,next_n", [(4, 1), (4, 3), (8, 2), (128, 1), (128, 3)])
+def test_other_head_counts(H, next_n):
+    case = inputs.make_case("decode", device="cuda", lens=[5, 130, 257, 1000], next_n=next_n,
+                            num_heads=H, head_dim=32 if H <= 8 else 128, width=1024, seed=77 + H)
+    compare_all(case)
+
+
+def test_padded_strides():
+    case = inputs.make_case("decode", device="cuda", lens=[33, 400, 129], num_heads=32,
+                            head_dim=64, page_kv=32, width=512, val_pad=512, sc_pad=64, seed=5)
+    assert case.kcache.val_page_stride == 32 * 64 + 512
+    compare_all(case)
+
+
+def test_prefill_chunked_causal():
+    T = 700
+    case = inputs.make_case("prefill", device="cuda", lens=[T], next_n=T, width=T, seed=3)
+    compare_all(case, rows_per_chunk=256)            # chunks 256 + 256 + 188 rows
+
+
+def test_schedule_buffer_contents():
+    case = inputs.make_case("decode", device="cuda", lens=[0, 129, 5000, 128], next_n=2,
+                            num_heads=64, width=5000, seed=9)
+    st = SparseAttentionStep(case, with_mla=False)
+    st.indexer_chunk(0, case.rows)
+    torch.cuda.synchronize()
+    s = st.sched.cpu().numpy()
+    assert s[0] == 0x44534131 and s[1] == 4 and s[2] == 2 and s[3] == 0 and s[4] == 8
+    units = s[8:8 + 16].reshape(4, 4)
+    tiles = [(parity.visible(case, 2 * b + 1) + 127) // 128 for b in range(4)]
+    assert list(units[:, 0]) == [0, 2, 4, 6] and list(units[:, 1]) == [2] * 4
+    assert list(units[:, 3]) == list(np.concatenate([[0], np.cumsum(tiles)[:-1]]))
+    assert s[6] == sum(tiles)
+
+
+def test_decode_full_size_sampled_rows():
+    case = inputs.make_case("decode", device="cuda")
+    g, st = gpu_logits(case)
+    assert st.device_status() == 0
+    sample = [0, 17, 40, 63]
+    cache, seqs = parity.oracle_cache(case.kcache, case.block_table, seqs=sample)
+    q = case.q.cpu()
+    w = case.weights.cpu()
+    ctx = case.context_lens.cpu()
+    for j, r in enumerate(sample):
+        o = oracle.logits_fp8(q[r:r + 1], w[r:r + 1], cache, ctx[r:r + 1], 1, width=case.width)
+        parity.check_logits([g[r]], [o[0]], [parity.visible(case, r)])
+
+
+def test_bad_block_table_entry_sets_status():
+    case = inputs.make_case("decode", device="cuda", lens=[300, 300], num_heads=16, head_dim=64,
+                            width=300, seed=12)
+    bt = case.block_table.clone()
+    bt[1, 2] = case.kcache.num_pages + 7               # out of the pool
+    case.block_table = bt
+    g, st = gpu_logits(case)
+    assert st.device_status() & _abi.DEV_BAD_PAGE
+    o = oracle_logits(case, rows=[0])
+    parity.check_logits([g[0]], o, [300])              # the other sequence is untouched
+
+
+def test_width_clip_sets_status():
+    case = inputs.make_case("decode", device="cuda", lens=[90, 300], num_heads=16, head_dim=64,
+                            width=300, seed=13)
+    st = SparseAttentionStep(case, with_mla=False)
+    st.logits.fill_(float("nan"))
+    st.width = 128                                     # narrower than the visible length
+    st.indexer_chunk(0, 2)
+    torch.cuda.synchronize()
+    assert st.device_status() & _abi.DEV_WIDTH
+    g = st.logits.cpu().numpy()
+    o = oracle_logits(case)
+    parity.check_logits([g[0], g[1]], o, [90, 128])
+    assert np.all(np.isnan(g[1, 128:]))

@@ -1,0 +1,87 @@
+"""GPU parity of sparse MLA decode against the fp64 oracle (bf16 and FP8
+latent caches, -1 padding, empty selections)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from deepseek_sparse_attention_mqa_gb300 import _abi, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    _abi.lib()
+    oracle.build()
+
+
+def random_indices(case, k, seed, pad_frac=0.0, empty_rows=()):
+    rng = np.random.default_rng(seed)
+    idx = np.full((case.rows, k), -1, np.int32)
+    for r in range(case.rows):
+        if r in empty_rows:
+            continue
+        vis = parity.visible(case, r)
+        n = min(k, vis, int(round(k * (1 - pad_frac))))
+        sel = rng.choice(vis, n, replace=False) if n else []
+        slots = rng.choice(k, n, replace=False)
+        idx[r, slots] = sel
+    return idx
+
+
+def run_mla(case, idx_np):
+    dev = torch.device("cuda")
+    lat = case.latent
+    cache = _abi.make_cache(lat.fmt, lat.head_dim, lat.page_kv, lat.num_pages, lat.values,
+                            lat.val_page_stride, lat.val_token_stride, lat.scales,
+                            lat.sc_page_stride, lat.sc_token_stride, case.block_table)
+    idx = torch.tensor(idx_np, device=dev)
+    out = torch.full((case.rows, case.mla_heads, case.d_v), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((case.rows, case.mla_heads), float("nan"), dtype=torch.float32, device=dev)
+    st = torch.zeros((1,), dtype=torch.int32, device=dev)
+    k = idx_np.shape[1]
+    ws_n = _abi.mla_workspace_bytes(case.rows, case.mla_heads, case.d_qk, case.d_v, k)
+    ws = torch.empty((max(ws_n, 16),), dtype=torch.uint8, device=dev)
+    _abi.sparse_mla(case.q_mla, case.softmax_scale, cache, idx, k, out, lse, case.d_v,
+                    None, case.next_n, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return out, lse
+
+
+def oracle_mla(case, idx_np, rows=None):
+    cache, _ = parity.oracle_cache(case.latent, case.block_table)
+    fmt = oracle.FMT_FP8 if case.latent.fmt == inputs.FMT_FP8 else oracle.FMT_BF16
+    q = case.q_mla.cpu()
+    if rows is None:
+        return oracle.sparse_mla(q, case.softmax_scale, fmt, cache, idx_np, case.d_v,
+                                 next_n=case.next_n)
+    outs, lses = [], []
+    for r in rows:
+        o, l = oracle.sparse_mla(q[r:r + 1], case.softmax_scale, fmt, cache, idx_np[r:r + 1],
+                                 case.d_v, seq_of_row=[r // case.next_n])
+        outs.append(o[0])
+        lses.append(l[0])
+    return np.stack(outs), np.stack(lses)
+
+
+def test_tiny_bf16_latent():
+    case = inputs.make_case("tiny", device="cuda")
+    idx = random_indices(case, case.topk, 1, pad_frac=0.25)
+    out, lse = run_mla(case, idx)
+    ro, rl = oracle_mla(case, idx)
+    parity.check_mla(out, lse, ro, rl)
+
+
+def test_fp8_latent_576_512_with_empty_row():
+    case = inputs.make_case("full_step", device="cuda", lens=[3000, 90, 2500], seed=31)
+    idx = random_indices(case, 2048, 2, pad_frac=0.1, empty_rows=(1,))
+    out, lse = run_mla(case, idx)
+    ro, rl = oracle_mla(case, idx)
+    parity.check_mla(out, lse, ro, rl)
+    assert np.all(out[1].float().cpu().numpy() == 0) and np.all(np.isneginf(lse[1].cpu().numpy()))
