@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "host.h"
+#include "logits_common.cuh"
 #include "ptx.cuh"
 
 namespace dsa {
@@ -57,71 +58,6 @@ struct LogitsParams {
     int n_cols;         // MMA N (multiple of 16)
     uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= 32, >= n_cols)
     uint32_t q_buf_bytes;
-};
-
-struct UnitInfo {
-    int seq, first_row, nrows, tile_begin, tile_end, vis_max;
-};
-
-__device__ __forceinline__ UnitInfo load_unit(const LogitsParams& p, const SchedUnit* units,
-                                              int total_tiles, int u)
-{
-    UnitInfo ui;
-    const SchedUnit su = units[u];
-    ui.seq = su.seq;
-    ui.first_row = su.first_row;
-    ui.nrows = su.nrows;
-    ui.tile_begin = su.tile_begin;
-    ui.tile_end = (u + 1 < p.num_units) ? units[u + 1].tile_begin : total_tiles;
-    const int L = max(0, p.context_lens[su.seq]);
-    ui.vis_max = visible_len(L, p.next_n, su.first_row + su.nrows - 1 - su.seq * p.next_n);
-    return ui;
-}
-
-// Last unit whose tile_begin <= t (units with no tiles are skipped naturally).
-__device__ __forceinline__ int find_unit(const SchedUnit* units, int num_units, int t)
-{
-    int lo = 0, hi = num_units - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (units[mid].tile_begin <= t)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
-// Walks this CTA's tiles [t0, t1) unit by unit; identical in every role.
-struct TileWalk {
-    const LogitsParams* p;
-    const SchedUnit* units;
-    int total_tiles;
-    int u;
-    UnitInfo ui;
-    __device__ __forceinline__ void start(const LogitsParams& pp, const SchedUnit* us, int total, int t0)
-    {
-        p = &pp;
-        units = us;
-        total_tiles = total;
-        u = find_unit(us, pp.num_units, t0);
-        ui = load_unit(pp, us, total, u);
-        while (t0 >= ui.tile_end && u + 1 < pp.num_units) {
-            ++u;
-            ui = load_unit(pp, us, total, u);
-        }
-    }
-    // Advance to the unit that owns tile t; returns true if the unit changed.
-    __device__ __forceinline__ bool seek(int t)
-    {
-        bool changed = false;
-        while (t >= ui.tile_end && u + 1 < p->num_units) {
-            ++u;
-            ui = load_unit(*p, units, total_tiles, u);
-            changed = true;
-        }
-        return changed;
-    }
 };
 
 template <int D>
@@ -220,6 +156,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *s_tmem;
+    const WalkParams wp{p.context_lens, p.next_n, p.num_units};
     const int P = p.page_kv;
     const int pages_per_tile = kTileTokens / P;
 
@@ -227,7 +164,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         // =========================== TMA producer ===========================
         if (lane == 0) {
             TileWalk w;
-            w.start(p, units, total_tiles, t0);
+            w.start(wp, units, total_tiles, t0);
             int stage = 0;
             uint32_t phase = 0;
             int ucount = 0;
@@ -294,7 +231,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (lane == 0) {
             const uint32_t idesc = make_idesc(0, 0, 0, 128, static_cast<uint32_t>(p.n_cols));
             TileWalk w;
-            w.start(p, units, total_tiles, t0);
+            w.start(wp, units, total_tiles, t0);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             int ucount = 0, qb = 0;
@@ -347,7 +284,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int tok = quarter * 32 + lane;          // token of this thread within the tile
         float* wS = sW + (warp - 2) * kMaxUnitCols;   // this warp's copy of the unit weights
         TileWalk w;
-        w.start(p, units, total_tiles, t0);
+        w.start(wp, units, total_tiles, t0);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         int vis[kMaxRows];
