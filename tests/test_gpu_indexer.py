@@ -126,11 +126,11 @@ def test_decode_full_size_sampled_rows():
     g, st = gpu_logits(case)
     assert st.device_status() == 0
     sample = [0, 17, 40, 63]
-    cache, seqs = parity.oracle_cache(case.kcache, case.block_table, seqs=sample)
     q = case.q.cpu()
     w = case.weights.cpu()
     ctx = case.context_lens.cpu()
-    for j, r in enumerate(sample):
+    for r in sample:
+        cache, _ = parity.oracle_cache(case.kcache, case.block_table, seqs=[r])
         o = oracle.logits_fp8(q[r:r + 1], w[r:r + 1], cache, ctx[r:r + 1], 1, width=case.width)
         parity.check_logits([g[r]], [o[0]], [parity.visible(case, r)])
 
