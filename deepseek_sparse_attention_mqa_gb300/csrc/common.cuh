@@ -78,9 +78,11 @@ __host__ __device__ __forceinline__ int64_t count_units(int batch, int next_n, i
     return total;
 }
 
-// Order-preserving map of an fp32 bit pattern to uint32 (larger float -> larger key).
+// Order-preserving map of an fp32 bit pattern to uint32 (larger float -> larger
+// key).  -0 is mapped like +0 so that equal values get equal keys.
 __host__ __device__ __forceinline__ uint32_t float_key(uint32_t bits)
 {
+    bits = (bits == 0x80000000u) ? 0u : bits;
     return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
 }
 

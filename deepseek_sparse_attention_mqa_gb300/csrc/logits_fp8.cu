@@ -35,6 +35,8 @@ namespace {
 
 constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;  // 6 warps
+constexpr int kPageCache = 512; // physical page ids cached by the producer warp
+constexpr int kMaxAcc = 4;      // TMEM accumulators in flight
 
 struct LogitsParams {
     const int32_t* sched;
@@ -57,6 +59,7 @@ struct LogitsParams {
     int stages;
     int n_cols;         // MMA N (multiple of 16)
     uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= 32, >= n_cols)
+    int n_acc;          // accumulators (n_acc * acc_cols <= 512, power of two total)
     uint32_t q_buf_bytes;
 };
 
@@ -70,7 +73,7 @@ struct Fp8Tile {
 
 // Shared memory map (offsets from a 1024-aligned base).
 struct SmemMap {
-    uint32_t k_off, q_off, sc_off, w_off, bar_off, misc_off, total;
+    uint32_t k_off, q_off, sc_off, w_off, pc_off, bar_off, misc_off, total;
 };
 
 __host__ __device__ __forceinline__ SmemMap smem_map(int D, int stages, uint32_t q_buf_bytes)
@@ -80,8 +83,9 @@ __host__ __device__ __forceinline__ SmemMap smem_map(int D, int stages, uint32_t
     m.q_off = m.k_off + stages * kTileTokens * D;
     m.sc_off = m.q_off + 2 * q_buf_bytes;
     m.w_off = m.sc_off + stages * kTileTokens * 4;
-    m.bar_off = m.w_off + 4 * kMaxUnitCols * 4;              // one weight copy per epilogue warp
-    m.misc_off = m.bar_off + (2 * kMaxStages + 8 + 1) * 8;
+    m.pc_off = m.w_off + 4 * kMaxUnitCols * 4;               // one weight copy per epilogue warp
+    m.bar_off = m.pc_off + kPageCache * 4;
+    m.misc_off = m.bar_off + (2 * kMaxStages + 2 * kMaxAcc + 4 + 1) * 8;
     m.total = m.misc_off + 16;
     return m;
 }
@@ -92,8 +96,6 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_q, const LogitsParams p)
 {
     using T = Fp8Tile<D>;
-    constexpr int kMaxRows = (kMaxUnitCols / H) > 0 ? (kMaxUnitCols / H) : 1;
-    constexpr int kMaxChunks = kMaxUnitCols / 32;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -102,12 +104,13 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* sQ = smem + mp.q_off;
     float* sS = reinterpret_cast<float*>(smem + mp.sc_off);
     float* sW = reinterpret_cast<float*>(smem + mp.w_off);
+    int* s_pages = reinterpret_cast<int*>(smem + mp.pc_off);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + mp.bar_off);
     uint64_t* full_bar = bars;                       // [stages]
     uint64_t* empty_bar = bars + kMaxStages;         // [stages]
-    uint64_t* accf_bar = bars + 2 * kMaxStages;      // [2]
-    uint64_t* acce_bar = accf_bar + 2;               // [2]
-    uint64_t* qf_bar = acce_bar + 2;                 // [2]
+    uint64_t* accf_bar = bars + 2 * kMaxStages;      // [kMaxAcc]
+    uint64_t* acce_bar = accf_bar + kMaxAcc;         // [kMaxAcc]
+    uint64_t* qf_bar = acce_bar + kMaxAcc;           // [2]
     uint64_t* qe_bar = qf_bar + 2;                   // [2]
     uint64_t* done_bar = qe_bar + 2;                 // [1]
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc_off);
@@ -135,9 +138,11 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1 + 4);   // MMA commit + 4 epilogue warps
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kMaxAcc; ++a) {
             mbar_init(smem_u32(&accf_bar[a]), 1);
             mbar_init(smem_u32(&acce_bar[a]), 4);
+        }
+        for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&qf_bar[a]), 1);
             mbar_init(smem_u32(&qe_bar[a]), 1);
         }
@@ -149,7 +154,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         tma_prefetch_map(&tm_q);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), 2 * p.acc_cols);
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), p.n_acc * p.acc_cols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -162,64 +167,96 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     if (warp == 0) {
         // =========================== TMA producer ===========================
-        if (lane == 0) {
-            TileWalk w;
-            w.start(wp, units, total_tiles, t0);
-            int stage = 0;
-            uint32_t phase = 0;
-            int ucount = 0;
-            long long issued = 0;
-            for (int t = t0; t < t1 && !*s_abort; ++t) {
-                const bool first = (t == t0);
-                const bool changed = w.seek(t) || first;
-                if (changed) {
+        // The whole warp walks the tiles; lane 0 issues the copies.  Physical
+        // page ids are fetched by all 32 lanes at once into a shared-memory
+        // cache (one global-memory latency per refill instead of one per tile).
+        TileWalk w;
+        w.start(wp, units, total_tiles, t0);
+        int stage = 0;
+        uint32_t phase = 0;
+        int ucount = 0;
+        long long issued = 0;
+        int pc_unit = -1, pc_lp0 = 0, pc_cnt = 0;
+        for (int t = t0; t < t1; ++t) {
+            if (*s_abort)
+                break;
+            const bool changed = w.seek(t) || (t == t0);
+            int ok = 1;
+            if (changed) {
+                if (lane == 0) {
                     const int qb = ucount & 1;
-                    if (!mbar_wait(smem_u32(&qe_bar[qb]), ((ucount >> 1) & 1) ^ 1)) {
-                        *s_abort = 1;
-                        break;
+                    ok = mbar_wait(smem_u32(&qe_bar[qb]), ((ucount >> 1) & 1) ^ 1);
+                    if (ok) {
+                        mbar_arrive_expect_tx(smem_u32(&qf_bar[qb]), static_cast<uint32_t>(p.n_cols) * D);
+                        tma_load_2d(smem_u32(sQ + qb * p.q_buf_bytes), &tm_q, smem_u32(&qf_bar[qb]), 0,
+                                    w.ui.first_row * H);
                     }
-                    mbar_arrive_expect_tx(smem_u32(&qf_bar[qb]), static_cast<uint32_t>(p.n_cols) * D);
-                    tma_load_2d(smem_u32(sQ + qb * p.q_buf_bytes), &tm_q, smem_u32(&qf_bar[qb]), 0,
-                                w.ui.first_row * H);
-                    ++ucount;
                 }
-                if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1)) {
-                    *s_abort = 1;
-                    break;
+                ++ucount;
+            }
+            const int tt = t - w.ui.tile_begin;              // tile index inside the unit
+            const int lp_first = tt * pages_per_tile;
+            if (w.u != pc_unit || lp_first + pages_per_tile > pc_lp0 + pc_cnt) {
+                // refill: this unit's pages from lp_first up to what this CTA will use
+                const int tiles_here = min(t1, w.ui.tile_end) - w.ui.tile_begin;
+                const int lp_vis = (w.ui.vis_max + P - 1) / P;
+                const int lp_end = min(tiles_here * pages_per_tile, lp_vis);
+                const int cnt = min(kPageCache, max(lp_end - lp_first, pages_per_tile));
+                __syncwarp();
+                for (int i = lane; i < cnt; i += 32) {
+                    const int lp = lp_first + i;
+                    int pg = -1;
+                    if (lp < lp_vis && lp < p.max_pages)
+                        pg = p.block_table[static_cast<int64_t>(w.ui.seq) * p.bt_stride + lp];
+                    s_pages[i] = pg;
                 }
-                const int tt = t - w.ui.tile_begin;              // tile index inside the unit
-                int phys[kTileTokens / 32];
-                uint32_t bytes = 0;
-                for (int j = 0; j < pages_per_tile; ++j) {
-                    const int lp = tt * pages_per_tile + j;
-                    phys[j] = -1;
-                    if (lp * P < w.ui.vis_max) {
-                        int pg = -1;
-                        if (lp < p.max_pages)
-                            pg = p.block_table[static_cast<int64_t>(w.ui.seq) * p.bt_stride + lp];
-                        if (pg >= 0 && pg < p.num_pages) {
-                            phys[j] = pg;
-                            bytes += static_cast<uint32_t>(P) * (D + 4);
-                        } else if (p.status) {
-                            atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                __syncwarp();
+                pc_unit = w.u;
+                pc_lp0 = lp_first;
+                pc_cnt = cnt;
+            }
+            if (lane == 0 && ok) {
+                ok = mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1);
+                if (ok) {
+                    int phys[kTileTokens / 32];
+                    uint32_t bytes = 0;
+                    for (int j = 0; j < pages_per_tile; ++j) {
+                        const int lp = lp_first + j;
+                        phys[j] = -1;
+                        if (lp * P < w.ui.vis_max) {
+                            const int pg = s_pages[lp - pc_lp0];
+                            if (pg >= 0 && pg < p.num_pages) {
+                                phys[j] = pg;
+                                bytes += static_cast<uint32_t>(P) * (D + 4);
+                            } else if (p.status) {
+                                atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                            }
                         }
                     }
-                }
-                const uint32_t fb = smem_u32(&full_bar[stage]);
-                mbar_arrive_expect_tx(fb, bytes);
-                for (int j = 0; j < pages_per_tile; ++j) {
-                    if (phys[j] < 0)
-                        continue;
-                    tma_load_3d(smem_u32(sK + stage * T::kTileBytes + j * P * D), &tm_k, fb, 0, 0, phys[j]);
-                    tma_load_2d(smem_u32(sS + stage * kTileTokens + j * P), &tm_s, fb, 0, phys[j]);
-                }
-                ++issued;
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1;
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    for (int j = 0; j < pages_per_tile; ++j) {
+                        if (phys[j] < 0)
+                            continue;
+                        tma_load_3d(smem_u32(sK + stage * T::kTileBytes + j * P * D), &tm_k, fb, 0, 0, phys[j]);
+                        tma_load_2d(smem_u32(sS + stage * kTileTokens + j * P), &tm_s, fb, 0, phys[j]);
+                    }
                 }
             }
-            // drain: every copy this thread issued has landed before the CTA exits
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0)
+                    *s_abort = 1;
+                break;
+            }
+            ++issued;
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        // drain: every copy this warp issued has landed before the CTA exits
+        if (lane == 0) {
             const long long lo = issued > p.stages ? issued - p.stages : 0;
             for (long long j = lo; j < issued; ++j)
                 mbar_wait(smem_u32(&full_bar[j % p.stages]), static_cast<uint32_t>((j / p.stages) & 1));
@@ -269,7 +306,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     stage = 0;
                     phase ^= 1;
                 }
-                if (++acc == 2) {
+                if (++acc == p.n_acc) {
                     acc = 0;
                     acc_phase ^= 1;
                 }
@@ -287,29 +324,21 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         w.start(wp, units, total_tiles, t0);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
-        int vis[kMaxRows];
-        int ncols_valid = 0;
+        int nchunks = 0, L = 0, i0 = 0;
         for (int t = t0; t < t1 && !*s_abort; ++t) {
             const bool changed = w.seek(t) || (t == t0);
             if (changed) {
                 __syncwarp();
-                ncols_valid = w.ui.nrows * H;
+                const int ncols_valid = w.ui.nrows * H;
+                nchunks = (ncols_valid + 31) / 32;
                 const float* wsrc = p.weights + static_cast<int64_t>(w.ui.first_row) * H;
                 for (int c = lane; c < kMaxUnitCols; c += 32)
                     wS[c] = c < ncols_valid ? wsrc[c] : 0.f;
                 __syncwarp();
-                const int L = max(0, p.context_lens[w.ui.seq]);
-                const int i0 = w.ui.first_row - w.ui.seq * p.next_n;
-#pragma unroll
-                for (int i = 0; i < kMaxRows; ++i) {
-                    int v = i < w.ui.nrows ? visible_len(L, p.next_n, i0 + i) : 0;
-                    if (v > p.logits_width) {
-                        if (p.status)
-                            atomicOr(p.status, DSA_DEV_WIDTH);
-                        v = p.logits_width;
-                    }
-                    vis[i] = v;
-                }
+                L = max(0, p.context_lens[w.ui.seq]);
+                i0 = w.ui.first_row - w.ui.seq * p.next_n;
+                if (lane == 0 && p.status && visible_len(L, p.next_n, i0 + w.ui.nrows - 1) > p.logits_width)
+                    atomicOr(p.status, DSA_DEV_WIDTH);
             }
             if (!mbar_wait(smem_u32(&full_bar[stage]), phase) ||
                 !mbar_wait(smem_u32(&accf_bar[acc]), acc_phase)) {
@@ -322,44 +351,88 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             if (lane == 0)
                 mbar_arrive(smem_u32(&empty_bar[stage]));
 
-            float sums[kMaxRows];
-#pragma unroll
-            for (int i = 0; i < kMaxRows; ++i)
-                sums[i] = 0.f;
+            const int s = (t - w.ui.tile_begin) * kTileTokens + tok;
             const uint32_t t_acc = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols +
                                    (static_cast<uint32_t>(quarter * 32) << 16);
+            // store one finished logit of unit row i
+            auto emit = [&](int i, float v) {
+                if (i < w.ui.nrows) {
+                    const int vis = min(visible_len(L, p.next_n, i0 + i), p.logits_width);
+                    if (s < vis)
+                        p.logits[static_cast<int64_t>(w.ui.first_row + i - p.row_begin) * p.logits_stride + s] =
+                            kscale * v;
+                }
+            };
+            float cur = 0.f;                           // running row sum (H >= 32)
+            auto process = [&](const uint32_t (&r)[32], int c) {
+                const float4* w4 = reinterpret_cast<const float4*>(wS + c * 32);
+                if constexpr (H >= 32) {
+                    // one row per chunk: 8 independent partial sums
+                    float part[8];
 #pragma unroll
-            for (int c = 0; c < kMaxChunks; ++c) {
-                if (c * 32 < ncols_valid) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_acc + c * 32, r);
-                    tmem_ld_wait();
+                    for (int j = 0; j < 8; ++j)
+                        part[j] = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = c * 32 + j;
-                        if (col < ncols_valid)
-                            sums[col / H] = fmaf(wS[col], fmaxf(__uint_as_float(r[j]), 0.f), sums[col / H]);
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 wv = w4[q4];
+                        part[(4 * q4 + 0) & 7] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), part[(4 * q4 + 0) & 7]);
+                        part[(4 * q4 + 1) & 7] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), part[(4 * q4 + 1) & 7]);
+                        part[(4 * q4 + 2) & 7] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), part[(4 * q4 + 2) & 7]);
+                        part[(4 * q4 + 3) & 7] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), part[(4 * q4 + 3) & 7]);
                     }
-                }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&acce_bar[acc]));
-
-            const int s = (t - w.ui.tile_begin) * kTileTokens + tok;
+                    cur += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                    if (((c + 1) * 32) % H == 0) {
+                        emit((c * 32) / H, cur);
+                        cur = 0.f;
+                    }
+                } else {
+                    // 32 / H rows per chunk, each summed over its H columns
+                    constexpr int kRowsPerChunk = 32 / H;
+                    float rs[kRowsPerChunk];
 #pragma unroll
-            for (int i = 0; i < kMaxRows; ++i) {
-                if (i < w.ui.nrows && s < vis[i]) {
-                    const int64_t row = w.ui.first_row + i - p.row_begin;
-                    p.logits[row * p.logits_stride + s] = kscale * sums[i];
+                    for (int i = 0; i < kRowsPerChunk; ++i)
+                        rs[i] = 0.f;
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 wv = w4[q4];
+                        rs[(4 * q4 + 0) / H] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), rs[(4 * q4 + 0) / H]);
+                        rs[(4 * q4 + 1) / H] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), rs[(4 * q4 + 1) / H]);
+                        rs[(4 * q4 + 2) / H] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), rs[(4 * q4 + 2) / H]);
+                        rs[(4 * q4 + 3) / H] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), rs[(4 * q4 + 3) / H]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kRowsPerChunk; ++i)
+                        emit(c * kRowsPerChunk + i, rs[i]);
                 }
+            };
+            for (int c = 0; c < nchunks; c += 2) {
+                uint32_t ra[32], rb[32];
+                tmem_ld_32x32b_x32(t_acc + c * 32, ra);
+                if (c + 1 < nchunks)
+                    tmem_ld_32x32b_x32(t_acc + (c + 1) * 32, rb);
+                tmem_ld_wait();
+                if (c + 2 >= nchunks) {
+                    // last TMEM reads of this accumulator are in registers: release it early
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&acce_bar[acc]));
+                }
+                process(ra, c);
+                if (c + 1 < nchunks)
+                    process(rb, c + 1);
+            }
+            if (nchunks == 0) {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&acce_bar[acc]));
             }
             if (++stage == p.stages) {
                 stage = 0;
                 phase ^= 1;
             }
-            if (++acc == 2) {
+            if (++acc == p.n_acc) {
                 acc = 0;
                 acc_phase ^= 1;
             }
@@ -373,7 +446,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     if (warp == 1)
-        tmem_dealloc(tmem_base, 2 * p.acc_cols);
+        tmem_dealloc(tmem_base, p.n_acc * p.acc_cols);
 }
 
 template <int D, int H>
@@ -453,6 +526,7 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     p.stages = stages;
     p.n_cols = n_cols;
     p.acc_cols = acc_cols;
+    p.n_acc = static_cast<int>(std::min<uint32_t>(kMaxAcc, 512u / acc_cols));
     p.q_buf_bytes = q_buf_bytes;
 
     auto kern = logits_fp8_kernel<D, H>;

@@ -1,19 +1,19 @@
-// topk.cu -- per-row top-k of the indexer logits by radix selection.
+// topk.cu -- per-row top-k of the indexer logits.
 //
 // "feat(deepseek_v4): Add fp4 indexer for dsv4" (ROCm/ATOM #1709): the indexer
 // returns the top-k token positions per query row (indexer_score_topk), and
 // the work is bounded by each row's ACTUAL visible length, not by the
 // max-model-length width of the logits buffer.
 //
-// One CTA per row.  Logits are mapped to order-preserving uint32 keys; the k-th
-// largest key is found with three histogram passes (11 + 11 + 10 bits) over the
-// row, each pass only counting keys that match the digits already fixed; then
-// one ordered pass writes every position with a larger key plus the first
-// needed positions with an equal key (lowest positions win ties), ascending.
-// The row is cached in shared memory when it fits (rows <= kSmemRowCap keys),
-// otherwise every pass streams it from global memory (L2 after the first).
-// Histogram updates are aggregated per warp (match.any) so that skewed digit
-// distributions do not serialise on one shared-memory address.
+// One CTA per row.  Logits are mapped to order-preserving uint32 keys.  The
+// row's key range [kmin, kmax] is split into 2048 bins by a right shift, which
+// bins in bit-pattern space: uniform in log scale, so outliers and wide value
+// ranges cost nothing.  One histogram pass finds the bin holding the k-th
+// largest key (refined with narrower bins while that bin is crowded), then one
+// output pass writes every position above that bin and collects the bin's few
+// elements as candidates, which are resolved exactly by the 64-bit order
+// (key, then lower position first) -- the same order as a full sort with ties
+// broken by position.  The row is kept in shared memory when it fits.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -24,15 +24,23 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kBins = 2048;
+constexpr int kBinBits = 11;
+constexpr int kCandCap = 4096;          // threshold-bin candidates kept in shared memory
+constexpr int kRankCap = 1024;          // candidates resolved by direct ranking
 constexpr int kSmemRowCap = 40 * 1024;  // keys cached in shared memory (160 KB)
 
-__device__ __forceinline__ uint32_t load_key(const float* row, int s)
+__device__ __forceinline__ uint64_t order64(uint32_t key, int pos)
 {
-    return float_key(__float_as_uint(__ldg(row + s)));
+    // larger key first, then lower position first
+    return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(pos));
 }
 
-// Block-wide inclusive scan of one int per thread; returns inclusive value and
-// the block total.  Uses ws[32] shared scratch.
+__device__ __forceinline__ int log2_ceil_u64(uint64_t v)
+{
+    return v <= 1 ? 0 : 64 - __clzll(v - 1);
+}
+
+// Block-wide inclusive scan of one int per thread (uses ws[32]).
 __device__ __forceinline__ int block_incl_scan(int v, int* ws, int* total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -62,6 +70,20 @@ __device__ __forceinline__ int block_incl_scan(int v, int* ws, int* total)
     return x + (warp > 0 ? ws[warp - 1] : 0);
 }
 
+// Warp-aggregated append: returns the slot of this lane's element (or -1).
+__device__ __forceinline__ int warp_append(bool take, int* counter)
+{
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (!m)
+        return -1;
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    if (lane == __ffs(m) - 1)
+        base = atomicAdd(counter, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+    return take ? base + __popc(m & ((1u << lane) - 1u)) : -1;
+}
+
 template <bool kCached>
 __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
@@ -71,128 +93,229 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
 {
     extern __shared__ uint32_t s_keys[];                 // [width] when kCached
     __shared__ int s_hist[kBins];
+    __shared__ uint32_t s_ck[kCandCap];
+    __shared__ int s_cp[kCandCap];
     __shared__ int s_ws[32];
-    __shared__ uint32_t s_prefix;
-    __shared__ int s_need;
+    __shared__ int s_bin, s_above_bin;
+    __shared__ int s_nout, s_ncand;
+    __shared__ unsigned s_kmin, s_kmax;
 
+    const int tid = threadIdx.x, lane = tid & 31;
     const int r = row_begin + blockIdx.x;
     const int b = r / next_n, i = r % next_n;
     int vis = visible_len(max(0, context_lens[b]), next_n, i);
     if (vis > width) {
-        if (threadIdx.x == 0 && status)
+        if (tid == 0 && status)
             atomicOr(status, DSA_DEV_WIDTH);
         vis = width;
     }
     const float* row = logits + static_cast<int64_t>(blockIdx.x) * stride;
     int32_t* out = idx + static_cast<int64_t>(blockIdx.x) * idx_stride;
     const int take = vis < k ? vis : k;
-    if (threadIdx.x == 0 && count)
+    if (tid == 0 && count)
         count[blockIdx.x] = take;
-
     if (vis <= k) {
-        for (int s = threadIdx.x; s < k; s += kTopkThreads)
+        for (int s = tid; s < k; s += kTopkThreads)
             out[s] = s < vis ? s : -1;
         return;
     }
 
-    if (kCached) {
-        // vectorised fill when the row start is 16-byte aligned
+    // ---- keys (cached) and key range
+    if (tid == 0) {
+        s_kmin = 0xFFFFFFFFu;
+        s_kmax = 0u;
+        s_nout = 0;
+        s_ncand = 0;
+    }
+    __syncthreads();
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    {
         const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
         int s0 = 0;
         if (vec) {
             const int nv = vis >> 2;
             const float4* row4 = reinterpret_cast<const float4*>(row);
-            for (int v = threadIdx.x; v < nv; v += kTopkThreads) {
+            for (int v = tid; v < nv; v += kTopkThreads) {
                 const float4 x = __ldg(row4 + v);
-                s_keys[4 * v + 0] = float_key(__float_as_uint(x.x));
-                s_keys[4 * v + 1] = float_key(__float_as_uint(x.y));
-                s_keys[4 * v + 2] = float_key(__float_as_uint(x.z));
-                s_keys[4 * v + 3] = float_key(__float_as_uint(x.w));
+                const uint32_t a = float_key(__float_as_uint(x.x)), bb = float_key(__float_as_uint(x.y));
+                const uint32_t c = float_key(__float_as_uint(x.z)), d = float_key(__float_as_uint(x.w));
+                if (kCached) {
+                    s_keys[4 * v + 0] = a;
+                    s_keys[4 * v + 1] = bb;
+                    s_keys[4 * v + 2] = c;
+                    s_keys[4 * v + 3] = d;
+                }
+                kmin = min(kmin, min(min(a, bb), min(c, d)));
+                kmax = max(kmax, max(max(a, bb), max(c, d)));
             }
             s0 = nv << 2;
         }
-        for (int s = s0 + threadIdx.x; s < vis; s += kTopkThreads)
-            s_keys[s] = load_key(row, s);
+        for (int s = s0 + tid; s < vis; s += kTopkThreads) {
+            const uint32_t a = float_key(__float_as_uint(__ldg(row + s)));
+            if (kCached)
+                s_keys[s] = a;
+            kmin = min(kmin, a);
+            kmax = max(kmax, a);
+        }
     }
-
-    auto key_at = [&](int s) -> uint32_t { return kCached ? s_keys[s] : load_key(row, s); };
-
-    if (threadIdx.x == 0) {
-        s_prefix = 0;
-        s_need = k;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     }
-    const int lane = threadIdx.x & 31;
-    const int vis_warp = (vis + 31) & ~31;            // warp-uniform trip count
-    // digits: bits [21,32), [10,21), [0,10)
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-        for (int j = threadIdx.x; j < kBins; j += kTopkThreads)
+    if (lane == 0) {
+        atomicMin(&s_kmin, kmin);
+        atomicMax(&s_kmax, kmax);
+    }
+    __syncthreads();
+    auto key_at = [&](int s) -> uint32_t {
+        return kCached ? s_keys[s] : float_key(__float_as_uint(__ldg(row + s)));
+    };
+
+    // ---- histogram passes: find the bin of the k-th largest key
+    uint32_t lo = s_kmin, hi = s_kmax;
+    int need = k;                 // still to take from keys in [lo, hi]
+    int shift = 0;
+    while (true) {
+        const uint64_t span = static_cast<uint64_t>(hi) - lo + 1;
+        shift = max(0, log2_ceil_u64(span) - kBinBits);
+        for (int j = tid; j < kBins; j += kTopkThreads)
             s_hist[j] = 0;
         __syncthreads();
-        const uint32_t prefix = s_prefix;
-        const int sh = shifts[pass];
-        const int hi = sh + widths[pass];             // bits above the digit are fixed
-        const uint32_t dmask = (1u << widths[pass]) - 1u;
-        for (int s = threadIdx.x; s < vis_warp; s += kTopkThreads) {
-            int bin = -1;
-            if (s < vis) {
-                const uint32_t key = key_at(s);
-                const bool match = (hi >= 32) ? true : ((key >> hi) == prefix);
-                if (match)
-                    bin = static_cast<int>((key >> sh) & dmask);
-            }
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (bin >= 0 && lane == __ffs(peers) - 1)
-                atomicAdd(&s_hist[bin], __popc(peers));
+        for (int s = tid; s < vis; s += kTopkThreads) {
+            const uint32_t key = key_at(s);
+            if (key >= lo && key <= hi)
+                atomicAdd(&s_hist[(key - lo) >> shift], 1);
         }
         __syncthreads();
-        // find the bin holding the need-th largest key: suffix counts from the top
-        const int need = s_need;
-        const int per = kBins / kTopkThreads;          // 2 bins per thread, top bins first
-        int local = 0;
-        for (int q = 0; q < per; ++q)
-            local += s_hist[kBins - 1 - (threadIdx.x * per + q)];
+        // suffix counts from the top bin down: thread t owns bins 2047-2t, 2046-2t
+        const int b0 = kBins - 1 - 2 * tid, b1 = b0 - 1;
+        const int c0 = s_hist[b0], c1 = s_hist[b1];
         int total;
-        const int incl = block_incl_scan(local, s_ws, &total);
-        int before = incl - local;                     // keys in bins above this thread's
+        const int incl = block_incl_scan(c0 + c1, s_ws, &total);
+        const int before = incl - c0 - c1;
         if (before < need && need <= incl) {
-            for (int q = 0; q < per; ++q) {
-                const int bin = kBins - 1 - (threadIdx.x * per + q);
-                const int c = s_hist[bin];
-                if (before + c >= need) {
-                    s_prefix = (prefix << widths[pass]) | static_cast<uint32_t>(bin);
-                    s_need = need - before;
-                    break;
-                }
-                before += c;
+            if (before + c0 >= need) {
+                s_bin = b0;
+                s_above_bin = before;
+            } else {
+                s_bin = b1;
+                s_above_bin = before + c0;
             }
         }
         __syncthreads();
+        const int bin = s_bin;
+        need -= s_above_bin;
+        const uint32_t blo = lo + (static_cast<uint32_t>(bin) << shift);
+        const uint32_t bhi = static_cast<uint32_t>(
+            min(static_cast<uint64_t>(hi), static_cast<uint64_t>(blo) + ((uint64_t(1) << shift) - 1)));
+        const int in_bin = s_hist[bin];
+        __syncthreads();
+        if (in_bin <= kCandCap || shift == 0) {
+            lo = blo;
+            hi = bhi;
+            break;
+        }
+        lo = blo;                 // crowded bin: refine inside it
+        hi = bhi;
     }
-    const uint32_t thr = s_prefix;
-    const int need_eq = s_need;                        // equal keys still to take
+    // keys > hi are taken outright (k - need of them); keys in [lo, hi] are candidates
+    const int n_direct = k - need;
 
-    // ordered output: keys > thr, plus the first need_eq keys == thr by position
-    int written = 0, eq_seen = 0;
-    for (int base = 0; base < vis; base += kTopkThreads) {
-        const int s = base + threadIdx.x;
-        uint32_t key = 0;
-        if (s < vis)
-            key = key_at(s);
-        const int is_eq = (s < vis && key == thr) ? 1 : 0;
-        int eq_tot;
-        const int eq_incl = block_incl_scan(is_eq, s_ws, &eq_tot);
-        const int sel = (s < vis) && (key > thr || (is_eq && eq_seen + eq_incl - 1 < need_eq)) ? 1 : 0;
-        int sel_tot;
-        const int sel_incl = block_incl_scan(sel, s_ws, &sel_tot);
-        if (sel)
-            out[written + sel_incl - 1] = s;
-        written += sel_tot;
-        eq_seen += eq_tot;
+    // ---- output pass
+    int cand_total;
+    {
+        for (int base = 0; base < vis; base += kTopkThreads) {
+            const int s = base + tid;
+            uint32_t key = 0;
+            if (s < vis)
+                key = key_at(s);
+            const bool above = s < vis && key > hi;
+            const bool cand = s < vis && key >= lo && key <= hi;
+            const int slot = warp_append(above, &s_nout);
+            if (slot >= 0)
+                out[slot] = s;
+            const int cs = warp_append(cand, &s_ncand);
+            if (cs >= 0 && cs < kCandCap) {
+                s_ck[cs] = key;
+                s_cp[cs] = s;
+            }
+        }
+        __syncthreads();
+        cand_total = s_ncand;
     }
-    for (int s = written + threadIdx.x; s < k; s += kTopkThreads)
-        out[s] = -1;
+
+    // ---- resolve the candidates: the `need` best by (key desc, position asc)
+    if (cand_total <= kCandCap) {
+        if (cand_total <= kRankCap) {
+            if (tid < cand_total) {
+                const uint64_t me = order64(s_ck[tid], s_cp[tid]);
+                int rank = 0;
+                for (int j = 0; j < cand_total; ++j)
+                    rank += order64(s_ck[j], s_cp[j]) > me ? 1 : 0;
+                if (rank < need)
+                    out[n_direct + rank] = s_cp[tid];
+            }
+        } else {
+            // radix selection on the 64-bit order, 8 bits at a time (high to low)
+            uint64_t prefix = 0;
+            int rem = need;
+            for (int pass = 7; pass >= 0; --pass) {
+                const int sh = 8 * pass;
+                for (int j = tid; j < 256; j += kTopkThreads)
+                    s_hist[j] = 0;
+                __syncthreads();
+                for (int j = tid; j < cand_total; j += kTopkThreads) {
+                    const uint64_t o = order64(s_ck[j], s_cp[j]);
+                    const bool match = (pass == 7) || ((o >> (sh + 8)) == (prefix >> (sh + 8)));
+                    if (match)
+                        atomicAdd(&s_hist[(o >> sh) & 255], 1);
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    int acc = 0;
+                    for (int d = 255; d >= 0; --d) {
+                        if (acc + s_hist[d] >= rem) {
+                            s_bin = d;
+                            s_above_bin = acc;
+                            break;
+                        }
+                        acc += s_hist[d];
+                    }
+                }
+                __syncthreads();
+                prefix |= static_cast<uint64_t>(s_bin) << sh;
+                rem -= s_above_bin;
+                __syncthreads();
+            }
+            // order values are unique: take every candidate >= prefix
+            if (tid == 0)
+                s_nout = n_direct;
+            __syncthreads();
+            for (int base = 0; base < cand_total; base += kTopkThreads) {
+                const int j = base + tid;
+                const bool t = j < cand_total && order64(s_ck[j], s_cp[j]) >= prefix;
+                const int slot = warp_append(t, &s_nout);
+                if (slot >= 0)
+                    out[slot] = s_cp[j];
+            }
+        }
+    } else {
+        // only when every candidate has one key value (shift == 0): take the
+        // `need` lowest positions holding it, in position order
+        const uint32_t key_eq = lo;
+        int seen = 0;
+        for (int base = 0; base < vis && seen < need; base += kTopkThreads) {
+            const int s = base + tid;
+            const int is_eq = (s < vis && key_at(s) == key_eq) ? 1 : 0;
+            int tot;
+            const int incl = block_incl_scan(is_eq, s_ws, &tot);
+            const int rank = seen + incl - 1;
+            if (is_eq && rank < need)
+                out[n_direct + rank] = s;
+            seen += tot;
+        }
+    }
 }
 
 }  // namespace

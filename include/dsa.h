@@ -173,10 +173,10 @@ DSA_API dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales,
  * dsv4": indexer_score_topk; "Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels":
  * dynamic per-row top-k lengths).  For each row, the k largest of
  * logits[row][0 : vis(row)) (vis as above, clipped to logits_width) are
- * selected; idx[row][0 : min(k, vis)) receives their token positions (the
- * order within a row is unspecified; this implementation writes ascending
- * positions) and idx[row][min(k, vis) : k) receives -1.  Among exactly equal
- * logits the lower position wins.  count (nullable) receives min(k, vis).
+ * selected; idx[row][0 : min(k, vis)) receives their token positions (in no
+ * particular order) and idx[row][min(k, vis) : k) receives -1.  Among exactly
+ * equal logits (-0 equals +0) the lower position wins.  count (nullable)
+ * receives min(k, vis).
  *
  * logits:   as produced by indexer_mqa_logits_paged (row stride in ELEMENTS).
  * idx:      int32 [rows, idx_row_stride >= k] (stride in ELEMENTS).

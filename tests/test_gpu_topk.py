@@ -44,6 +44,8 @@ def test_same_logits_exact(width, k):
     rows = torch.randn((len(lens), width), generator=g)
     rows[3, :] = torch.round(rows[3, :] * 2)          # many exact ties
     rows[5, : width // 3] = 1.5                         # all equal
+    rows[6, ::2] = -0.0                                  # signed zeros tie with +0
+    rows[6, 1::2] = 0.0
     idx, cnt, st = run_topk(rows, lens, 1, k, width)
     assert st == 0
     ref_idx, ref_cnt = oracle.topk(rows.double().numpy(), lens, 1, k)
@@ -53,7 +55,7 @@ def test_same_logits_exact(width, k):
     assert sorted(idx[5].tolist()) == list(range(k))
 
 
-def test_next_n_windows_and_ascending_order():
+def test_next_n_windows():
     g = torch.Generator().manual_seed(2)
     lens = [10, 3000]
     rows = torch.randn((6, 3000), generator=g)
@@ -61,9 +63,6 @@ def test_next_n_windows_and_ascending_order():
     vis = [oracle.visible(L, 3, i) for L in lens for i in range(3)]
     ref_idx, _ = oracle.topk(rows.double().numpy(), lens, 3, 64)
     parity.check_topk_same_input(idx, ref_idx, vis, 64)
-    for r, v in enumerate(vis):
-        t = min(64, v)
-        assert list(idx[r, :t]) == sorted(idx[r, :t].tolist())
 
 
 def test_end_to_end_on_indexer_logits():
