@@ -369,6 +369,8 @@ dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads, int d_
     a.workspace = workspace;
     a.ws_bytes = ws_bytes;
     a.status = status_dev;
+    if (sparse_mla_tc_supported(a) && aligned16(q_bf16) && aligned16(out_bf16))
+        return launch_sparse_mla_tc(a, dev, static_cast<cudaStream_t>(stream));
     return launch_sparse_mla_simt(a, static_cast<cudaStream_t>(stream));
 }
 

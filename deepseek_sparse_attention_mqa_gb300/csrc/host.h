@@ -95,5 +95,7 @@ struct MlaArgs {
     int32_t* status;
 };
 dsa_status launch_sparse_mla_simt(const MlaArgs& a, cudaStream_t stream);
+bool sparse_mla_tc_supported(const MlaArgs& a);
+dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace dsa

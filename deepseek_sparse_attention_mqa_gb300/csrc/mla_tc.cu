@@ -1,0 +1,521 @@
+// mla_tc.cu -- sparse MLA decode on the tcgen05 tensor cores (DeepSeek latent
+// attention shapes: up to 128 query heads, q/k dim 512 or 576, v dim 512, FP8
+// e4m3 latent cache with one fp32 scale per token).
+//
+// "Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels" (flashinfer #3269): decode
+// attention of each query row over the latent tokens its top-k selected, with
+// bf16 output and an LSE output; the pages give precompiled kernels and a
+// multi-CTA reduction for it, neither of which is used here.
+//
+// GB300 design: one CLUSTER of two CTAs per query row.  The output O
+// (128 heads x 512 fp32) fills a whole TMEM, so it is split by value dims:
+// CTA 0 owns latent dims [0, 256) and CTA 1 owns [256, d_qk); each keeps its
+// part of Q (bf16, swizzled K-major) resident, gathers and widens its part of
+// the selected latent rows (FP8 -> bf16, exact) and computes a PARTIAL score
+// S_c = Q_c K_c^T on the tensor cores.  The two partials are exchanged through
+// distributed shared memory, so both CTAs hold the same S = S_0 + S_1 (identical
+// arithmetic, hence identical softmax decisions) and each accumulates its half
+// of O = P V in TMEM, where V is the first 256 dims of its own latent slice.
+//
+//   warps 0-3  softmax: thread = head = TMEM lane.  Exchange partial scores,
+//              scale by token scale * softmax scale, online max / sum in base 2
+//              with a lazily refreshed running max (O in TMEM is rescaled only
+//              when the max grows by more than 2^8), write P (bf16, with the
+//              token scale folded in for V) to shared memory, finally normalise
+//              O and store bf16 out / fp32 lse.
+//   warps 4-7  gather: per 64-token block, look up each selected token through
+//              the block table, load its FP8 slice, widen to bf16 into a 128B-
+//              swizzled K-major tile (zeros for unused slots).
+//   warp 8     TMEM allocator + MMA issuer: S = Q K^T (M=128, N=64) and
+//              O += P V (M=128, N=256, V read MN-major from the same tile).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "host.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kNT = 64;                 // selected tokens per block
+constexpr int kMaxChunks = 5;           // 64-dim chunks per CTA (576 = 4 + 5 chunks)
+constexpr int kVChunks = 4;             // 256 value dims per CTA
+constexpr int kQChunkBytes = 128 * 128; // 128 heads x 64 bf16
+constexpr int kLChunkBytes = kNT * 128; // 64 tokens x 64 bf16
+constexpr int kThreads = 288;           // 9 warps
+constexpr int kConvWarp0 = 4;
+constexpr int kMmaWarp = 8;
+constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, O at 256
+constexpr float kRescaleLog2 = 8.f;     // refresh the running max only past 2^8
+
+struct MlaParams {
+    const __nv_bfloat16* q;
+    int num_heads;
+    int d_qk;
+    float scale_log2;                   // softmax_scale * log2(e)
+    const uint8_t* vals;
+    int64_t vps, vts;
+    const uint8_t* scs;
+    int64_t sps, sts;
+    const int32_t* bt;
+    int64_t bt_stride;
+    int max_pages;
+    int page_kv;
+    int num_pages;
+    const int32_t* seq_of_row;
+    int next_n;
+    const int32_t* idx;
+    int64_t idx_stride;
+    int k;
+    __nv_bfloat16* out;
+    float* lse;
+    int32_t* status;
+};
+
+struct MlaSmem {
+    uint32_t q, lat, p, x, scale, valid, bar, misc, total;
+};
+
+__host__ __device__ constexpr MlaSmem mla_smem()
+{
+    MlaSmem m{};
+    m.q = 0;
+    m.lat = m.q + kMaxChunks * kQChunkBytes;
+    m.p = m.lat + 2 * kMaxChunks * kLChunkBytes;
+    m.x = m.p + 128 * 128;
+    m.scale = m.x + 128 * kNT * 4;
+    m.valid = m.scale + 2 * kNT * 4;
+    m.bar = m.valid + 2 * kNT * 4;
+    m.misc = m.bar + 16 * 8;
+    m.total = m.misc + 16;
+    return m;
+}
+
+// 16 e4m3 bytes -> 16 bf16 (exact: every e4m3 value is a bf16 value).
+__device__ __forceinline__ void e4m3x16_to_bf16x16(const uint4 v, uint4& lo, uint4& hi)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hh)) & 0xFFFFu);
+            const __half2_raw h2r = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 f = __half22float2(__half2(h2r));
+            const __nv_bfloat162 b = __float22bfloat162_rn(f);
+            o[2 * i + hh] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+sparse_mla_tc_kernel(const MlaParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr MlaSmem mp = mla_smem();
+    uint8_t* sQ = smem + mp.q;
+    uint8_t* sLat = smem + mp.lat;
+    uint8_t* sP = smem + mp.p;
+    uint8_t* sX = smem + mp.x;
+    float* sScale = reinterpret_cast<float*>(smem + mp.scale);
+    int* sValid = reinterpret_cast<int*>(smem + mp.valid);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + mp.bar);
+    uint64_t* q_full = bars + 0;
+    uint64_t* lat_full = bars + 1;   // [2]
+    uint64_t* lat_empty = bars + 3;  // [2]
+    uint64_t* s_full = bars + 5;     // [2]
+    uint64_t* s_empty = bars + 7;    // [2]
+    uint64_t* x_full = bars + 9;     // peer's partial scores arrived in sX
+    uint64_t* x_free = bars + 10;    // peer consumed what this CTA wrote
+    uint64_t* p_full = bars + 11;
+    uint64_t* p_empty = bars + 12;
+    uint64_t* o_done = bars + 13;
+    volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t peer = crank ^ 1u;
+    const int row = blockIdx.y;
+    const int seq = p.seq_of_row ? p.seq_of_row[row] : row / p.next_n;
+    // latent dims of this CTA: chunks [c_lo, c_lo + nchunk) of 64
+    const int c_lo = crank == 0 ? 0 : kVChunks;
+    const int nchunk = crank == 0 ? kVChunks : (p.d_qk / 64 - kVChunks);
+    const int nblk = (p.k + kNT - 1) / kNT;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(q_full), 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&lat_full[i]), 4);
+            mbar_init(smem_u32(&lat_empty[i]), 1);
+            mbar_init(smem_u32(&s_full[i]), 1);
+            mbar_init(smem_u32(&s_empty[i]), 4);
+        }
+        mbar_init(smem_u32(x_full), 4);
+        mbar_init(smem_u32(x_free), 4);
+        mbar_init(smem_u32(p_full), 4);
+        mbar_init(smem_u32(p_empty), 1);
+        mbar_init(smem_u32(o_done), 1);
+        *s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();              // the peer's barriers are initialised before any remote arrive
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *s_tmem;
+
+    if (warp >= kConvWarp0 && warp < kMmaWarp) {
+        // ================================ gather ================================
+        const int ct = threadIdx.x - kConvWarp0 * 32;   // 0..127
+        // Q slice -> swizzled K-major tile: row = head, 8 units of 16 B per chunk
+        const int qunits = 128 * nchunk * 8;
+        for (int u = ct; u < qunits; u += 128) {
+            const int h = u / (nchunk * 8), rem = u % (nchunk * 8);
+            const int ch = rem >> 3, un = rem & 7;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (h < p.num_heads)
+                v = *reinterpret_cast<const uint4*>(
+                    p.q + (static_cast<int64_t>(row) * p.num_heads + h) * p.d_qk + (c_lo + ch) * 64 + un * 8);
+            *reinterpret_cast<uint4*>(sQ + ch * kQChunkBytes + swizzled_offset(h, un, 128)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(q_full));
+
+        const int32_t* irow = p.idx + static_cast<int64_t>(row) * p.idx_stride;
+        const int nseg = nchunk * 4;                    // 16-byte FP8 segments per token
+        for (int j = 0; j < nblk && !*s_abort; ++j) {
+            const int st = j & 1;
+            if (!mbar_wait(smem_u32(&lat_empty[st]), ((j >> 1) & 1) ^ 1)) {
+                *s_abort = 1;
+                break;
+            }
+            uint8_t* tile = sLat + st * (kMaxChunks * kLChunkBytes);
+            for (int w = ct; w < kNT * nseg; w += 128) {
+                const int t = w / nseg, seg = w % nseg;
+                const int jj = j * kNT + t;
+                int s = jj < p.k ? irow[jj] : -1;
+                int page = -1;
+                if (s >= 0) {
+                    const int lp = s / p.page_kv;
+                    if (lp < p.max_pages)
+                        page = p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp];
+                    if (page < 0 || page >= p.num_pages) {
+                        if (seg == 0 && p.status)
+                            atomicOr(p.status, DSA_DEV_BAD_INDEX);
+                        s = -1;
+                    }
+                }
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                if (s >= 0) {
+                    const uint8_t* src = p.vals + page * p.vps + (s % p.page_kv) * p.vts + (c_lo * 64 + seg * 16);
+                    e4m3x16_to_bf16x16(*reinterpret_cast<const uint4*>(src), lo, hi);
+                }
+                uint8_t* chunk = tile + (seg >> 2) * kLChunkBytes;
+                const int un = (seg & 3) * 2;
+                *reinterpret_cast<uint4*>(chunk + swizzled_offset(t, un, 128)) = lo;
+                *reinterpret_cast<uint4*>(chunk + swizzled_offset(t, un + 1, 128)) = hi;
+                if (seg == 0) {
+                    float sc = 0.f;
+                    if (s >= 0)
+                        sc = *reinterpret_cast<const float*>(p.scs + page * p.sps + (s % p.page_kv) * p.sts);
+                    sScale[st * kNT + t] = sc;
+                    sValid[st * kNT + t] = s >= 0;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&lat_full[st]));
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================ MMA ===================================
+        if (lane == 0) {
+            const uint32_t idesc_qk = make_idesc(1, 1, 0, 128, kNT);
+            const uint32_t idesc_pv = make_idesc(1, 1, 1, 128, 256);
+            bool ok = mbar_wait(smem_u32(q_full), 0);
+            auto issue_qk = [&](int j) -> bool {
+                const int st = j & 1;
+                if (!mbar_wait(smem_u32(&lat_full[st]), (j >> 1) & 1) ||
+                    !mbar_wait(smem_u32(&s_empty[st]), ((j >> 1) & 1) ^ 1))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(st * kNT);
+                const uint32_t qa = smem_u32(sQ);
+                const uint32_t kb = smem_u32(sLat + st * (kMaxChunks * kLChunkBytes));
+                for (int ch = 0; ch < nchunk; ++ch) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ad = make_smem_desc(qa + ch * kQChunkBytes + ks * 32, 16, 1024, kLayoutSw128);
+                        const uint64_t bd = make_smem_desc(kb + ch * kLChunkBytes + ks * 32, 16, 1024, kLayoutSw128);
+                        umma_f16(d, ad, bd, idesc_qk, (ch | ks) != 0 ? 1u : 0u);
+                    }
+                }
+                umma_commit(smem_u32(&s_full[st]));
+                return true;
+            };
+            if (ok && nblk > 0)
+                ok = issue_qk(0);
+            for (int j = 0; j < nblk && ok && !*s_abort; ++j) {
+                if (j + 1 < nblk && !issue_qk(j + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(smem_u32(p_full), j & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                // O[:, v] += P[:, t] V[t, v]: A = P (K-major over tokens), B = V read
+                // MN-major from the latent tile (64-dim blocks 8 KB apart = LBO,
+                // 8-token groups 1 KB apart = SBO)
+                const uint32_t d = tmem_base + 256;
+                const uint32_t pa = smem_u32(sP);
+                const uint32_t vb = smem_u32(sLat + (j & 1) * (kMaxChunks * kLChunkBytes));
+#pragma unroll
+                for (int ks = 0; ks < kNT / 16; ++ks) {
+                    const uint64_t ad = make_smem_desc(pa + ks * 32, 16, 1024, kLayoutSw128);
+                    const uint64_t bd = make_smem_desc(vb + ks * 2048, kLChunkBytes, 1024, kLayoutSw128);
+                    umma_f16(d, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                umma_commit(smem_u32(p_empty));
+                umma_commit(smem_u32(&lat_empty[j & 1]));
+            }
+            if (!ok)
+                *s_abort = 1;
+            umma_commit(smem_u32(o_done));
+            mbar_wait(smem_u32(o_done), 0);
+        }
+    } else {
+        // ================================ softmax ===============================
+        const int h = threadIdx.x;                        // head = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t x_row = smem_u32(sX + h * (kNT * 4));
+        const uint32_t peer_x_row = mapa_shared(x_row, peer);
+        const uint32_t peer_x_full = mapa_shared(smem_u32(x_full), peer);
+        const uint32_t peer_x_free = mapa_shared(smem_u32(x_free), peer);
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nblk && ok; ++j) {
+            const int sb = j & 1;
+            const uint32_t ph = (j >> 1) & 1;
+            if (!mbar_wait(smem_u32(&s_full[sb]), ph)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t ra[32], rb[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + sb * kNT, ra);
+            tmem_ld_32x32b_x32(tmem_base + lane_base + sb * kNT + 32, rb);
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&s_empty[sb]));
+
+            // ---- exchange partial scores with the peer CTA (16-byte units, XOR-swizzled by row)
+            if (!mbar_wait_cluster(smem_u32(x_free), (j & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const uint32_t* src = u < 8 ? &ra[4 * u] : &rb[4 * (u - 8)];
+                st_cluster_v4(peer_x_row + ((u ^ (h & 7)) << 4), src[0], src[1], src[2], src[3]);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_remote(peer_x_full);
+            if (!mbar_wait_cluster(smem_u32(x_full), j & 1)) {
+                ok = false;
+                break;
+            }
+            float sco[kNT];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float4 x = *reinterpret_cast<const float4*>(sX + h * (kNT * 4) + ((u ^ (h & 7)) << 4));
+                const uint32_t* own = u < 8 ? &ra[4 * u] : &rb[4 * (u - 8)];
+                // both CTAs form partial(CTA 0) + partial(CTA 1) in the same order
+                if (crank == 0) {
+                    sco[4 * u + 0] = __uint_as_float(own[0]) + x.x;
+                    sco[4 * u + 1] = __uint_as_float(own[1]) + x.y;
+                    sco[4 * u + 2] = __uint_as_float(own[2]) + x.z;
+                    sco[4 * u + 3] = __uint_as_float(own[3]) + x.w;
+                } else {
+                    sco[4 * u + 0] = x.x + __uint_as_float(own[0]);
+                    sco[4 * u + 1] = x.y + __uint_as_float(own[1]);
+                    sco[4 * u + 2] = x.z + __uint_as_float(own[2]);
+                    sco[4 * u + 3] = x.w + __uint_as_float(own[3]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_remote(peer_x_free);
+
+            // ---- scores in base 2; masked slots are -inf
+            if (!mbar_wait(smem_u32(&lat_full[sb]), ph)) {
+                ok = false;
+                break;
+            }
+            const float* scl = sScale + sb * kNT;
+            const int* vld = sValid + sb * kNT;
+            float m_blk = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+                sco[t] = vld[t] ? sco[t] * (scl[t] * p.scale_log2) : -INFINITY;
+                m_blk = fmaxf(m_blk, sco[t]);
+            }
+            // P of the previous block has been consumed (and O is stable) before
+            // P is rewritten or O rescaled
+            if (j > 0 && !mbar_wait(smem_u32(p_empty), (j - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const float m_new = fmaxf(m_run, m_blk);
+            if (m_new > m_run + kRescaleLog2) {
+                if (m_run != -INFINITY) {
+                    const float f = exp2f(m_run - m_new);
+                    l_run *= f;
+                    // j > 0 here: O holds blocks < j
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                        tmem_st_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                m_run = m_new;
+            }
+            // P (bf16, token scale folded in for V) -> row h of the swizzled K-major tile
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    const int t = 8 * u + 2 * q2;
+                    const float p0 = (m_run == -INFINITY || sco[t] == -INFINITY) ? 0.f : exp2f(sco[t] - m_run);
+                    const float p1 = (m_run == -INFINITY || sco[t + 1] == -INFINITY) ? 0.f : exp2f(sco[t + 1] - m_run);
+                    l_run += p0 + p1;
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(p0 * scl[t], p1 * scl[t + 1]);
+                    pk[q2] = *reinterpret_cast<const uint32_t*>(&b);
+                }
+                *reinterpret_cast<uint4*>(sP + swizzled_offset(h, u, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(p_full));
+        }
+        if (!ok)
+            *s_abort = 1;
+        // ---- epilogue: O / l -> bf16 out[row][h][crank*256 + v], lse (natural log)
+        const bool have = nblk > 0 && mbar_wait(smem_u32(o_done), 0) && ok && !*s_abort;
+        tc_fence_after_sync();
+        const float inv = (have && l_run > 0.f) ? 1.f / l_run : 0.f;
+        if (h < p.num_heads) {
+            __nv_bfloat16* orow = p.out + (static_cast<int64_t>(row) * p.num_heads + h) * 512 + crank * 256;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t o[32];
+                if (have) {
+                    tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                    tmem_ld_wait();
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const float a = have ? __uint_as_float(o[i + 2 * q2]) * inv : 0.f;
+                        const float b = have ? __uint_as_float(o[i + 2 * q2 + 1]) * inv : 0.f;
+                        const __nv_bfloat162 bb = __floats2bfloat162_rn(a, b);
+                        pk[q2] = *reinterpret_cast<const uint32_t*>(&bb);
+                    }
+                    *reinterpret_cast<uint4*>(orow + c * 32 + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+            if (crank == 0)
+                p.lse[static_cast<int64_t>(row) * p.num_heads + h] =
+                    (have && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+
+    __syncwarp();
+    if (threadIdx.x == 0 && *s_abort && p.status)
+        atomicOr(p.status, DSA_DEV_TIMEOUT);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == kMmaWarp)
+        tmem_dealloc(tmem_base, kTmemCols);
+    cluster_sync();              // no CTA leaves while its peer may still touch its shared memory
+}
+
+}  // namespace
+
+bool sparse_mla_tc_supported(const MlaArgs& a)
+{
+    return a.kv->fmt == DSA_KV_FP8_E4M3 && a.num_heads <= 128 && (a.d_qk == 576 || a.d_qk == 512) &&
+           a.d_v == 512 && a.kv->sc_token_stride >= 4;
+}
+
+dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    const dsa_paged_cache* kv = a.kv;
+    constexpr MlaSmem mp = mla_smem();
+    const int smem_bytes = static_cast<int>(mp.total) + 1024;
+    if (smem_bytes > dev.max_smem_optin)
+        return DSA_ERR_UNSUPPORTED;
+    MlaParams p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.num_heads = a.num_heads;
+    p.d_qk = a.d_qk;
+    p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+    p.vals = static_cast<const uint8_t*>(kv->values);
+    p.vps = kv->val_page_stride;
+    p.vts = kv->val_token_stride;
+    p.scs = static_cast<const uint8_t*>(kv->scales);
+    p.sps = kv->sc_page_stride;
+    p.sts = kv->sc_token_stride;
+    p.bt = kv->block_table;
+    p.bt_stride = kv->bt_row_stride;
+    p.max_pages = kv->max_pages_per_seq;
+    p.page_kv = kv->page_kv;
+    p.num_pages = kv->num_pages;
+    p.seq_of_row = a.seq_of_row;
+    p.next_n = a.next_n;
+    p.idx = a.idx;
+    p.idx_stride = a.idx_row_stride;
+    p.k = a.k;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    p.status = a.status;
+    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    sparse_mla_tc_kernel<<<dim3(2, a.rows), kThreads, smem_bytes, stream>>>(p);
+    return check_launch();
+}
+
+}  // namespace dsa

@@ -160,3 +160,41 @@ def test_width_clip_sets_status():
     o = oracle_logits(case)
     parity.check_logits([g[0], g[1]], o, [90, 128])
     assert np.all(np.isnan(g[1, 128:]))
+
+
+# ------------------------------------------------------------------ MXFP4
+
+def test_mxfp4_edge_lengths_padded_strides():
+    case = inputs.make_case("spec_mxfp4", device="cuda", lens=[0, 1, 2, 31, 32, 33, 64, 200, 1000],
+                            width=1024, seed=51)
+    assert case.kcache.val_page_stride == 32 * 32 + 1024
+    compare_all(case)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("next_n", [1, 2, 3])
+@pytest.mark.parametrize("H", [16, 32, 64])
+@pytest.mark.parametrize("P", [32, 64])
+def test_mxfp4_matrix(P, H, next_n, D):
+    case = inputs.make_case("spec_mxfp4", device="cuda", lens=[0, 1, 63, 64, 65, 200, 511],
+                            next_n=next_n, page_kv=P, num_heads=H, head_dim=D, width=600,
+                            seed=2000 + P + H + next_n + D)
+    compare_all(case)
+
+
+def test_mxfp4_full_size_sampled_rows():
+    case = inputs.make_case("spec_mxfp4", device="cuda")
+    g, st = gpu_logits(case)
+    assert st.device_status() == 0
+    q, qs, w = case.q.cpu(), case.q_scales.cpu(), case.weights.cpu()
+    ctx = case.context_lens.cpu()
+    lens = ctx.tolist()
+    sample_seqs = [0, 3, 7] + sorted(range(len(lens)), key=lambda b: -lens[b])[:2]
+    for b in sample_seqs:
+        cache, _ = parity.oracle_cache(case.kcache, case.block_table, seqs=[b])
+        n = case.next_n
+        o = oracle.logits_mxfp4(q[b * n:(b + 1) * n], qs[b * n:(b + 1) * n], w[b * n:(b + 1) * n], cache,
+                                ctx[b:b + 1], n, width=case.width)
+        for i in range(n):
+            r = b * n + i
+            parity.check_logits([g[r]], [o[i]], [parity.visible(case, r)])

@@ -85,3 +85,24 @@ def test_fp8_latent_576_512_with_empty_row():
     ro, rl = oracle_mla(case, idx)
     parity.check_mla(out, lse, ro, rl)
     assert np.all(out[1].float().cpu().numpy() == 0) and np.all(np.isneginf(lse[1].cpu().numpy()))
+
+
+@pytest.mark.parametrize("heads,d_qk,k,pad", [(128, 576, 2048, 0.0), (128, 576, 100, 0.3),
+                                             (64, 576, 256, 0.0), (128, 512, 192, 0.1),
+                                             (16, 576, 64, 0.5)])
+def test_fp8_latent_shapes(heads, d_qk, k, pad):
+    case = inputs.make_case("full_step", device="cuda", lens=[4000, 300, 64, 2500], seed=33,
+                            mla=dict(heads=heads, d_qk=d_qk, d_v=512, fmt=inputs.FMT_FP8,
+                                     scale=1.0 / np.sqrt(192)))
+    idx = random_indices(case, k, 7, pad_frac=pad)
+    out, lse = run_mla(case, idx)
+    ro, rl = oracle_mla(case, idx)
+    parity.check_mla(out, lse, ro, rl)
+
+
+def test_fp8_latent_repeat_is_deterministic():
+    case = inputs.make_case("full_step", device="cuda", lens=[3000, 2000], seed=34)
+    idx = random_indices(case, 2048, 3)
+    a = run_mla(case, idx)
+    b = run_mla(case, idx)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
