@@ -136,11 +136,16 @@ def scored_pairs(case):
 
 def logits_algorithmic_bytes(case):
     """Bytes the logits kernel must move: each sequence's visible K rows (values
-    + fp32 scale) once, q and weights once, the visible logits written once."""
-    D, H, n = case.head_dim, case.num_heads, case.next_n
+    + scales) once, q (+ q scales) and weights once, the visible logits written once."""
+    from deepseek_sparse_attention_mqa_gb300 import inputs
+    D, H = case.head_dim, case.num_heads
     L = case.context_lens.cpu().tolist()
-    kv = sum(l * (D + 4) for l in L)
-    q = case.rows * H * D
+    if case.fmt == inputs.FMT_FP8:
+        tok, qrow = D + 4, D
+    else:
+        tok, qrow = D // 2 + D // 32, D // 2 + D // 32
+    kv = sum(l * tok for l in L)
+    q = case.rows * H * qrow
     w = case.rows * H * 4
     out = scored_pairs(case) * 4
     bt = sum(-(-l // case.page_kv) for l in L) * 4 + len(L) * 4
@@ -178,7 +183,9 @@ def run_ours(args, rank, world, local):
     if status != 0:
         raise RuntimeError("device status %#x after warm-up" % status)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    chunks = [(rb, re) for rb, re in st.chunks if re > rb]
+    nck = len(chunks)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * nck + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.wait_first()
@@ -186,27 +193,27 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_begin = time.time()
+    c = st.case
     for s in range(args.steps):
         flush.fill_(float(s))                    # evict L2 between steps
         e = ev[s]
-        c = st.case
         e[0].record(stream)
-        _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, 0, c.rows, st.sched,
-                            st.status)
-        e[1].record(stream)
-        _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
-                        c.batch, c.next_n, 0, c.rows, st.sched, st.logits, st.width, st.status)
-        e[2].record(stream)
-        st.topk_chunk(0, c.rows)
-        e[3].record(stream)
+        for ci, (rb, re) in enumerate(chunks):
+            _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status)
+            e[3 * ci + 1].record(stream)
+            _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
+                            c.batch, c.next_n, rb, re, st.sched, st.logits, st.width, st.status)
+            e[3 * ci + 2].record(stream)
+            st.topk_chunk(rb, re)
+            e[3 * ci + 3].record(stream)
     torch.cuda.synchronize()
     t_end = time.time()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    logits_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    topk_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    sched_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
+    sched_ms = [sum((e[3 * ci] if ci else e[0]).elapsed_time(e[3 * ci + 1]) for ci in range(nck)) for e in ev]
+    logits_ms = [sum(e[3 * ci + 1].elapsed_time(e[3 * ci + 2]) for ci in range(nck)) for e in ev]
+    topk_ms = [sum(e[3 * ci + 2].elapsed_time(e[3 * ci + 3]) for ci in range(nck)) for e in ev]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -227,27 +234,40 @@ def run_ours(args, rank, world, local):
     result = None
     if rank == 0:
         hbm, bf16, bf16s, src = measured_peaks()
-        lg_bytes = logits_algorithmic_bytes(case)
-        lg_ms = statistics.mean(logits_ms)
-        achieved = lg_bytes / (lg_ms * 1e-3) / 1e9
-        traffic = load_traffic("logits_fp8", args.workload)
+        lg_ms = statistics.mean(logits_ms) / nck            # per launch
+        if args.workload == "prefill":
+            # FP8 MMA work per launch (one chunk): 2 * pairs * heads * head_dim
+            flops = 2.0 * pairs * case.num_heads * case.head_dim / nck
+            achieved = flops / (lg_ms * 1e-3) / 1e12
+            fp8_peak = 2.0 * bf16                             # nominal fp8 : bf16 = 2 : 1
+            roof = {"kernel": "logits_fp8 (indexer_mqa_logits_paged), per chunk launch", "bound": "tensor",
+                    "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / fp8_peak, 4),
+                    "peak_source": src + " bf16 burst x 2 (nominal fp8/bf16 ratio)",
+                    "algorithmic_flops": flops, "traffic": load_traffic("logits_fp8", args.workload)}
+        else:
+            lg_bytes = logits_algorithmic_bytes(case) / nck
+            achieved = lg_bytes / (lg_ms * 1e-3) / 1e9
+            kname = "logits_fp8" if case.fmt == inputs.FMT_FP8 else "logits_mxfp4"
+            roof = {"kernel": kname + " (indexer_mqa_logits_paged)", "bound": "hbm",
+                    "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(achieved / hbm, 4), "peak_source": src,
+                    "algorithmic_bytes": lg_bytes, "traffic": load_traffic(kname, args.workload)}
         full = None if args.skip_full_step else measure_full_step(dev, args)
         result = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": case.batch, "next_n": case.next_n,
+            "dtype": "e4m3" if case.fmt == inputs.FMT_FP8 else "e2m1", "data": "synthetic",
+            "config": {"workload": WORKLOAD if args.workload == "decode" else args.workload, "batch": case.batch, "next_n": case.next_n,
                        "heads": case.num_heads, "head_dim": case.head_dim, "page_kv": case.page_kv,
                        "topk": case.topk, "scored_pairs_per_step": pairs, "seed": case.meta["seed"],
                        "l2": "flushed between steps (1 GiB write)", "parallelism": "replicas"},
             "kernel_ms": {"schedule": round(statistics.mean(sched_ms), 5),
-                          "logits": round(lg_ms, 5), "topk": round(statistics.mean(topk_ms), 5)},
-            "roofline": {"kernel": "logits_fp8 (indexer_mqa_logits_paged)", "bound": "hbm",
-                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(achieved / hbm, 4), "peak_source": src,
-                         "algorithmic_bytes": lg_bytes, "traffic": traffic},
-            "gpu_launches": 3 * args.steps,
+                          "logits": round(statistics.mean(logits_ms), 5),
+                          "topk": round(statistics.mean(topk_ms), 5), "chunks": nck},
+            "roofline": roof,
+            "gpu_launches": 3 * nck * args.steps,
             "clocks": clocks,
             "e2e": e2e,
             "full_step": full,
@@ -343,23 +363,41 @@ def measure_full_step(dev, args):
             "launches_per_step": st.launches_per_step(), "device_status": status}
 
 
-def cpu_baseline(case, pairs):
-    """fp64 oracle (logits + full-sort top-k) on the host cores, all rows of one step."""
+def cpu_baseline(case, pairs, mac_budget=12e9):
+    """fp64 oracle (logits + full-sort top-k) on the host cores over a bounded,
+    contiguous block of rows of the same workload (all rows when they fit the
+    multiply-accumulate budget, ~10-30 s of CPU work)."""
     import oracle
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import parity
+    per_pair = case.num_heads * case.head_dim
+    vis = [parity.visible(case, r) for r in range(case.rows)]
+    if sum(vis) * per_pair <= mac_budget:
+        rb, re = 0, case.rows
+    else:
+        mid = case.rows // 2
+        rb = re = mid
+        acc = 0
+        while re < case.rows and acc + vis[re] * per_pair <= mac_budget:
+            acc += vis[re] * per_pair
+            re += 1
+        re = max(re, rb + 1)
     cache, _ = parity.oracle_cache(case.kcache, case.block_table)
-    q = case.q.cpu()
-    w = case.weights.cpu()
     ctx = case.context_lens.cpu()
     t0 = time.time()
-    lg = oracle.logits_fp8(q, w, cache, ctx, case.next_n, width=case.width)
-    oracle.topk(lg, ctx, case.next_n, case.topk)
+    if case.q_scales is None:
+        lg = oracle.logits_fp8(case.q.cpu(), case.weights.cpu(), cache, ctx, case.next_n, rb, re,
+                               width=case.width)
+    else:
+        lg = oracle.logits_mxfp4(case.q.cpu(), case.q_scales.cpu(), case.weights.cpu(), cache, ctx,
+                                 case.next_n, rb, re, width=case.width)
+    oracle.topk(lg, ctx, case.next_n, case.topk, rb, re)
     dt = time.time() - t0
-    return {"value": round(pairs / dt / 1e3, 2), "unit": UNIT, "cores": oracle.threads(),
+    sp = sum(vis[rb:re])
+    return {"value": round(sp / dt / 1e3, 2), "unit": UNIT, "cores": oracle.threads(),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "one full step of the same workload (all %d rows, %d scored pairs): "
-                      "fp64 logits + full-sort top-k" % (case.rows, pairs)}
+            "sample": "rows [%d, %d) of %d of the same workload (%d scored pairs): fp64 logits + "
+                      "full-sort top-k" % (rb, re, case.rows, sp)}
 
 
 def run_reference(args, rank, world):

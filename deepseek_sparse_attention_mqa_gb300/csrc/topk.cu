@@ -5,29 +5,35 @@
 // the work is bounded by each row's ACTUAL visible length, not by the
 // max-model-length width of the logits buffer.
 //
-// One CTA per row.  Logits are mapped to order-preserving uint32 keys.  The
-// row's key range [kmin, kmax] is split into 2048 bins by a right shift, which
-// bins in bit-pattern space: uniform in log scale, so outliers and wide value
-// ranges cost nothing.  One histogram pass finds the bin holding the k-th
-// largest key (refined with narrower bins while that bin is crowded), then one
-// output pass writes every position above that bin and collects the bin's few
-// elements as candidates, which are resolved exactly by the 64-bit order
-// (key, then lower position first) -- the same order as a full sort with ties
-// broken by position.  The row is kept in shared memory when it fits.
+// A cluster of C CTAs per row (C = 1..8, chosen so that all SMs have work even
+// for a 64-row decode batch); CTA c owns a contiguous slice of the row, keeps it
+// in shared memory as order-preserving uint32 keys, and the cluster cooperates
+// through distributed shared memory with CTA 0 as the meeting point:
+//  1. key range [kmin, kmax] of the row (cluster min/max reduction);
+//  2. 2048 bins over the range by a right shift -- bins uniform in bit-pattern
+//     space, i.e. log scale, so outliers and wide ranges cost nothing; one
+//     histogram round (local histograms added into CTA 0's) finds the bin of
+//     the k-th largest key, refined inside that bin while it is crowded;
+//  3. every position above that bin is written out directly (cluster-wide
+//     counter); the bin's few elements are appended to CTA 0 as candidates;
+//  4. CTA 0 resolves the candidates exactly by the 64-bit order (key, then lower
+//     position), the same order as a full sort with ties broken by position.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
 #include "host.h"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kBins = 2048;
 constexpr int kBinBits = 11;
-constexpr int kCandCap = 4096;          // threshold-bin candidates kept in shared memory
-constexpr int kRankCap = 1024;          // candidates resolved by direct ranking
-constexpr int kSmemRowCap = 40 * 1024;  // keys cached in shared memory (160 KB)
+constexpr int kCandCap = 4096;      // threshold-bin candidates collected in CTA 0
+constexpr int kRankCap = 512;       // candidates resolved by direct ranking
+constexpr int kSliceCap = 16384;    // keys per CTA kept in shared memory (64 KB)
+constexpr int kMaxCluster = 8;
 
 __device__ __forceinline__ uint64_t order64(uint32_t key, int pos)
 {
@@ -56,7 +62,7 @@ __device__ __forceinline__ int block_incl_scan(int v, int* ws, int* total)
         ws[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int t = ws[lane];
+        int t = lane < kThreads / 32 ? ws[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, t, o);
@@ -66,77 +72,108 @@ __device__ __forceinline__ int block_incl_scan(int v, int* ws, int* total)
         ws[lane] = t;
     }
     __syncthreads();
-    *total = ws[31];
+    *total = ws[kThreads / 32 - 1];
     return x + (warp > 0 ? ws[warp - 1] : 0);
 }
 
-// Warp-aggregated append: returns the slot of this lane's element (or -1).
-__device__ __forceinline__ int warp_append(bool take, int* counter)
+// Warp-aggregated append to a counter in CTA 0 (cluster address); returns this
+// lane's slot or -1.
+__device__ __forceinline__ int warp_append_cluster(bool take, uint32_t counter_addr)
 {
     const unsigned m = __ballot_sync(0xffffffffu, take);
     if (!m)
         return -1;
     const int lane = threadIdx.x & 31;
-    int base = 0;
-    if (lane == __ffs(m) - 1)
-        base = atomicAdd(counter, __popc(m));
-    base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-    return take ? base + __popc(m & ((1u << lane) - 1u)) : -1;
+    const int leader = __ffs(m) - 1;
+    uint32_t base = 0;
+    if (lane == leader)
+        base = atom_add_cluster(counter_addr, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return take ? static_cast<int>(base) + __popc(m & ((1u << lane) - 1u)) : -1;
 }
 
+struct TopkShared {
+    int hist[kBins];
+    uint32_t ck[kCandCap];
+    int cp[kCandCap];
+    int ws[32];
+    int bin, above;
+    int nout, ncand;
+    uint32_t kmin, kmax;
+};
+
 template <bool kCached>
-__global__ void __launch_bounds__(kTopkThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             const int32_t* __restrict__ context_lens, int next_n, int row_begin, int k,
             int32_t* __restrict__ idx, int64_t idx_stride, int32_t* __restrict__ count,
             int32_t* __restrict__ status)
 {
-    extern __shared__ uint32_t s_keys[];                 // [width] when kCached
-    __shared__ int s_hist[kBins];
-    __shared__ uint32_t s_ck[kCandCap];
-    __shared__ int s_cp[kCandCap];
-    __shared__ int s_ws[32];
-    __shared__ int s_bin, s_above_bin;
-    __shared__ int s_nout, s_ncand;
-    __shared__ unsigned s_kmin, s_kmax;
+    extern __shared__ uint32_t s_keys[];                 // [slice] when kCached
+    __shared__ TopkShared sh;
 
     const int tid = threadIdx.x, lane = tid & 31;
-    const int r = row_begin + blockIdx.x;
+    const uint32_t crank = cluster_ctarank();
+    const int C = static_cast<int>(gridDim.x);           // cluster spans gridDim.x
+    const int rloc = blockIdx.y;
+    const int r = row_begin + rloc;
     const int b = r / next_n, i = r % next_n;
     int vis = visible_len(max(0, context_lens[b]), next_n, i);
     if (vis > width) {
-        if (tid == 0 && status)
+        if (tid == 0 && crank == 0 && status)
             atomicOr(status, DSA_DEV_WIDTH);
         vis = width;
     }
-    const float* row = logits + static_cast<int64_t>(blockIdx.x) * stride;
-    int32_t* out = idx + static_cast<int64_t>(blockIdx.x) * idx_stride;
-    const int take = vis < k ? vis : k;
-    if (tid == 0 && count)
-        count[blockIdx.x] = take;
-    if (vis <= k) {
-        for (int s = tid; s < k; s += kTopkThreads)
-            out[s] = s < vis ? s : -1;
+    const float* row = logits + static_cast<int64_t>(rloc) * stride;
+    int32_t* out = idx + static_cast<int64_t>(rloc) * idx_stride;
+    if (vis <= k) {                                       // uniform over the cluster
+        if (crank == 0) {
+            if (tid == 0 && count)
+                count[rloc] = vis;
+            for (int s = tid; s < k; s += kThreads)
+                out[s] = s < vis ? s : -1;
+        }
         return;
     }
+    if (crank == 0 && tid == 0 && count)
+        count[rloc] = k;
 
-    // ---- keys (cached) and key range
+    // this CTA's slice [s_lo, s_hi) of the visible row (slice starts 16-byte aligned)
+    const int slice = (((vis + C - 1) / C) + 3) & ~3;
+    const int s_lo = min(vis, static_cast<int>(crank) * slice);
+    const int s_hi = min(vis, s_lo + slice);
+    const int n = s_hi - s_lo;
+
+    // CTA 0's copies of the shared reduction state (cluster addresses)
+    const uint32_t c0_kmin = mapa_shared(smem_u32(&sh.kmin), 0);
+    const uint32_t c0_kmax = mapa_shared(smem_u32(&sh.kmax), 0);
+    const uint32_t c0_hist = mapa_shared(smem_u32(&sh.hist[0]), 0);
+    const uint32_t c0_bin = mapa_shared(smem_u32(&sh.bin), 0);
+    const uint32_t c0_above = mapa_shared(smem_u32(&sh.above), 0);
+    const uint32_t c0_nout = mapa_shared(smem_u32(&sh.nout), 0);
+    const uint32_t c0_ncand = mapa_shared(smem_u32(&sh.ncand), 0);
+    const uint32_t c0_ck = mapa_shared(smem_u32(&sh.ck[0]), 0);
+    const uint32_t c0_cp = mapa_shared(smem_u32(&sh.cp[0]), 0);
+
     if (tid == 0) {
-        s_kmin = 0xFFFFFFFFu;
-        s_kmax = 0u;
-        s_nout = 0;
-        s_ncand = 0;
+        sh.kmin = 0xFFFFFFFFu;
+        sh.kmax = 0u;
+        sh.nout = 0;
+        sh.ncand = 0;
     }
-    __syncthreads();
+    cluster_sync();                                       // CTA 0's state initialised
+
+    // ---- 1. keys of the slice and the row's key range
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
     {
-        const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+        const float* src = row + s_lo;
+        const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
         int s0 = 0;
         if (vec) {
-            const int nv = vis >> 2;
-            const float4* row4 = reinterpret_cast<const float4*>(row);
-            for (int v = tid; v < nv; v += kTopkThreads) {
-                const float4 x = __ldg(row4 + v);
+            const int nv = n >> 2;
+            const float4* src4 = reinterpret_cast<const float4*>(src);
+            for (int v = tid; v < nv; v += kThreads) {
+                const float4 x = __ldg(src4 + v);
                 const uint32_t a = float_key(__float_as_uint(x.x)), bb = float_key(__float_as_uint(x.y));
                 const uint32_t c = float_key(__float_as_uint(x.z)), d = float_key(__float_as_uint(x.w));
                 if (kCached) {
@@ -150,8 +187,8 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             }
             s0 = nv << 2;
         }
-        for (int s = s0 + tid; s < vis; s += kTopkThreads) {
-            const uint32_t a = float_key(__float_as_uint(__ldg(row + s)));
+        for (int s = s0 + tid; s < n; s += kThreads) {
+            const uint32_t a = float_key(__float_as_uint(__ldg(src + s)));
             if (kCached)
                 s_keys[s] = a;
             kmin = min(kmin, a);
@@ -163,153 +200,160 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
         kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     }
-    if (lane == 0) {
-        atomicMin(&s_kmin, kmin);
-        atomicMax(&s_kmax, kmax);
+    if (lane == 0 && n > 0) {
+        red_min_cluster(c0_kmin, kmin);
+        red_max_cluster(c0_kmax, kmax);
     }
-    __syncthreads();
-    auto key_at = [&](int s) -> uint32_t {
-        return kCached ? s_keys[s] : float_key(__float_as_uint(__ldg(row + s)));
+    cluster_sync();
+    auto key_at = [&](int j) -> uint32_t {               // j: index within the slice
+        return kCached ? s_keys[j] : float_key(__float_as_uint(__ldg(row + s_lo + j)));
     };
+    uint32_t lo = ld_cluster_u32(c0_kmin), hi = ld_cluster_u32(c0_kmax);
 
-    // ---- histogram passes: find the bin of the k-th largest key
-    uint32_t lo = s_kmin, hi = s_kmax;
+    // ---- 2. histogram rounds: the bin of the k-th largest key
     int need = k;                 // still to take from keys in [lo, hi]
-    int shift = 0;
     while (true) {
         const uint64_t span = static_cast<uint64_t>(hi) - lo + 1;
-        shift = max(0, log2_ceil_u64(span) - kBinBits);
-        for (int j = tid; j < kBins; j += kTopkThreads)
-            s_hist[j] = 0;
-        __syncthreads();
-        for (int s = tid; s < vis; s += kTopkThreads) {
-            const uint32_t key = key_at(s);
+        const int shift = max(0, log2_ceil_u64(span) - kBinBits);
+        for (int j = tid; j < kBins; j += kThreads)
+            sh.hist[j] = 0;
+        cluster_sync();                                   // every histogram (CTA 0's too) zeroed
+        for (int j = tid; j < n; j += kThreads) {
+            const uint32_t key = key_at(j);
             if (key >= lo && key <= hi)
-                atomicAdd(&s_hist[(key - lo) >> shift], 1);
+                atomicAdd(&sh.hist[(key - lo) >> shift], 1);
         }
         __syncthreads();
-        // suffix counts from the top bin down: thread t owns bins 2047-2t, 2046-2t
-        const int b0 = kBins - 1 - 2 * tid, b1 = b0 - 1;
-        const int c0 = s_hist[b0], c1 = s_hist[b1];
-        int total;
-        const int incl = block_incl_scan(c0 + c1, s_ws, &total);
-        const int before = incl - c0 - c1;
-        if (before < need && need <= incl) {
-            if (before + c0 >= need) {
-                s_bin = b0;
-                s_above_bin = before;
-            } else {
-                s_bin = b1;
-                s_above_bin = before + c0;
+        if (crank != 0)
+            for (int j = tid; j < kBins; j += kThreads)
+                if (sh.hist[j])
+                    red_add_cluster(c0_hist + 4u * j, static_cast<uint32_t>(sh.hist[j]));
+        cluster_sync();                                   // CTA 0 holds the row histogram
+        if (crank == 0) {
+            // suffix counts from the top bin down: thread t owns bins 2047-4t .. 2044-4t
+            int c[4], loc = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                c[q] = sh.hist[kBins - 1 - 4 * tid - q];
+                loc += c[q];
+            }
+            int total;
+            const int incl = block_incl_scan(loc, sh.ws, &total);
+            int before = incl - loc;
+            if (before < need && need <= incl) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (before + c[q] >= need) {
+                        sh.bin = kBins - 1 - 4 * tid - q;
+                        sh.above = before;
+                        break;
+                    }
+                    before += c[q];
+                }
             }
         }
-        __syncthreads();
-        const int bin = s_bin;
-        need -= s_above_bin;
+        cluster_sync();                                   // decision visible in CTA 0
+        const int bin = static_cast<int>(ld_cluster_u32(c0_bin));
+        need -= static_cast<int>(ld_cluster_u32(c0_above));
+        const int in_bin = static_cast<int>(ld_cluster_u32(c0_hist + 4u * bin));
         const uint32_t blo = lo + (static_cast<uint32_t>(bin) << shift);
         const uint32_t bhi = static_cast<uint32_t>(
             min(static_cast<uint64_t>(hi), static_cast<uint64_t>(blo) + ((uint64_t(1) << shift) - 1)));
-        const int in_bin = s_hist[bin];
-        __syncthreads();
-        if (in_bin <= kCandCap || shift == 0) {
-            lo = blo;
-            hi = bhi;
-            break;
-        }
-        lo = blo;                 // crowded bin: refine inside it
+        lo = blo;
         hi = bhi;
+        if (in_bin <= kCandCap || shift == 0)
+            break;
+        cluster_sync();                                   // everyone read CTA 0's histogram
     }
-    // keys > hi are taken outright (k - need of them); keys in [lo, hi] are candidates
-    const int n_direct = k - need;
+    const int n_direct = k - need;                        // keys > hi are taken outright
 
-    // ---- output pass
-    int cand_total;
-    {
-        for (int base = 0; base < vis; base += kTopkThreads) {
-            const int s = base + tid;
-            uint32_t key = 0;
-            if (s < vis)
-                key = key_at(s);
-            const bool above = s < vis && key > hi;
-            const bool cand = s < vis && key >= lo && key <= hi;
-            const int slot = warp_append(above, &s_nout);
-            if (slot >= 0)
-                out[slot] = s;
-            const int cs = warp_append(cand, &s_ncand);
-            if (cs >= 0 && cs < kCandCap) {
-                s_ck[cs] = key;
-                s_cp[cs] = s;
-            }
+    // ---- 3. output pass: keys above the bin out, the bin's keys to CTA 0 as candidates
+    for (int base = 0; base < n; base += kThreads) {
+        const int j = base + tid;
+        uint32_t key = 0;
+        if (j < n)
+            key = key_at(j);
+        const bool above = j < n && key > hi;
+        const bool cand = j < n && key >= lo && key <= hi;
+        const int slot = warp_append_cluster(above, c0_nout);
+        if (slot >= 0)
+            out[slot] = s_lo + j;
+        const int cs = warp_append_cluster(cand, c0_ncand);
+        if (cs >= 0 && cs < kCandCap) {
+            st_cluster_u32(c0_ck + 4u * cs, key);
+            st_cluster_u32(c0_cp + 4u * cs, static_cast<uint32_t>(s_lo + j));
         }
-        __syncthreads();
-        cand_total = s_ncand;
     }
+    cluster_sync();                                       // all candidates landed in CTA 0
+    if (crank != 0)
+        return;
 
-    // ---- resolve the candidates: the `need` best by (key desc, position asc)
+    // ---- 4. CTA 0: the `need` best candidates by (key desc, position asc)
+    const int cand_total = sh.ncand;
     if (cand_total <= kCandCap) {
         if (cand_total <= kRankCap) {
             if (tid < cand_total) {
-                const uint64_t me = order64(s_ck[tid], s_cp[tid]);
+                const uint64_t me = order64(sh.ck[tid], sh.cp[tid]);
                 int rank = 0;
                 for (int j = 0; j < cand_total; ++j)
-                    rank += order64(s_ck[j], s_cp[j]) > me ? 1 : 0;
+                    rank += order64(sh.ck[j], sh.cp[j]) > me ? 1 : 0;
                 if (rank < need)
-                    out[n_direct + rank] = s_cp[tid];
+                    out[n_direct + rank] = sh.cp[tid];
             }
         } else {
             // radix selection on the 64-bit order, 8 bits at a time (high to low)
             uint64_t prefix = 0;
             int rem = need;
             for (int pass = 7; pass >= 0; --pass) {
-                const int sh = 8 * pass;
-                for (int j = tid; j < 256; j += kTopkThreads)
-                    s_hist[j] = 0;
+                const int sh8 = 8 * pass;
+                for (int j = tid; j < 256; j += kThreads)
+                    sh.hist[j] = 0;
                 __syncthreads();
-                for (int j = tid; j < cand_total; j += kTopkThreads) {
-                    const uint64_t o = order64(s_ck[j], s_cp[j]);
-                    const bool match = (pass == 7) || ((o >> (sh + 8)) == (prefix >> (sh + 8)));
-                    if (match)
-                        atomicAdd(&s_hist[(o >> sh) & 255], 1);
+                for (int j = tid; j < cand_total; j += kThreads) {
+                    const uint64_t o = order64(sh.ck[j], sh.cp[j]);
+                    if (pass == 7 || (o >> (sh8 + 8)) == (prefix >> (sh8 + 8)))
+                        atomicAdd(&sh.hist[(o >> sh8) & 255], 1);
                 }
                 __syncthreads();
                 if (tid == 0) {
                     int acc = 0;
                     for (int d = 255; d >= 0; --d) {
-                        if (acc + s_hist[d] >= rem) {
-                            s_bin = d;
-                            s_above_bin = acc;
+                        if (acc + sh.hist[d] >= rem) {
+                            sh.bin = d;
+                            sh.above = acc;
                             break;
                         }
-                        acc += s_hist[d];
+                        acc += sh.hist[d];
                     }
                 }
                 __syncthreads();
-                prefix |= static_cast<uint64_t>(s_bin) << sh;
-                rem -= s_above_bin;
+                prefix |= static_cast<uint64_t>(sh.bin) << sh8;
+                rem -= sh.above;
                 __syncthreads();
             }
-            // order values are unique: take every candidate >= prefix
+            // order values are unique: exactly `need` candidates are >= prefix
             if (tid == 0)
-                s_nout = n_direct;
+                sh.nout = n_direct;
             __syncthreads();
-            for (int base = 0; base < cand_total; base += kTopkThreads) {
+            const uint32_t my_nout = mapa_shared(smem_u32(&sh.nout), 0);
+            for (int base = 0; base < cand_total; base += kThreads) {
                 const int j = base + tid;
-                const bool t = j < cand_total && order64(s_ck[j], s_cp[j]) >= prefix;
-                const int slot = warp_append(t, &s_nout);
+                const bool t = j < cand_total && order64(sh.ck[j], sh.cp[j]) >= prefix;
+                const int slot = warp_append_cluster(t, my_nout);
                 if (slot >= 0)
-                    out[slot] = s_cp[j];
+                    out[slot] = sh.cp[j];
             }
         }
     } else {
-        // only when every candidate has one key value (shift == 0): take the
+        // every candidate carries one key value (shift reached 0): take the
         // `need` lowest positions holding it, in position order
         const uint32_t key_eq = lo;
         int seen = 0;
-        for (int base = 0; base < vis && seen < need; base += kTopkThreads) {
+        for (int base = 0; base < vis && seen < need; base += kThreads) {
             const int s = base + tid;
-            const int is_eq = (s < vis && key_at(s) == key_eq) ? 1 : 0;
+            const int is_eq = (s < vis && float_key(__float_as_uint(__ldg(row + s))) == key_eq) ? 1 : 0;
             int tot;
-            const int incl = block_incl_scan(is_eq, s_ws, &tot);
+            const int incl = block_incl_scan(is_eq, sh.ws, &tot);
             const int rank = seen + incl - 1;
             if (is_eq && rank < need)
                 out[n_direct + rank] = s;
@@ -322,25 +366,47 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
 
 dsa_status launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
-    (void)dev;
     const int rows = a.row_end - a.row_begin;
     if (rows <= 0)
         return DSA_OK;
-    const float* lg = a.logits;
-    if (a.logits_width <= kSmemRowCap) {
-        const int smem = a.logits_width * 4;
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem);
+    // cluster size: enough CTAs to cover ~1.5x the SMs, at least enough that a
+    // slice of the widest row fits in shared memory, at most 8
+    int C = 1;
+    while (C < kMaxCluster && (static_cast<int64_t>(a.logits_width) + C - 1) / C > kSliceCap)
+        C <<= 1;
+    while (C < kMaxCluster && static_cast<int64_t>(rows) * C * 2 < 3LL * dev.sm_count)
+        C <<= 1;
+    const int slice = static_cast<int>((((static_cast<int64_t>(a.logits_width) + C - 1) / C) + 3) & ~3LL);
+    const bool cached = slice <= kSliceCap;
+    const int smem = cached ? slice * 4 : 0;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, rows, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (cached) {
+        e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return cuda_fail(e);
-        topk_kernel<true><<<rows, kTopkThreads, smem, stream>>>(
-            lg, a.logits_row_stride, a.logits_width, a.context_lens, a.next_n, a.row_begin, a.k, a.idx,
-            a.idx_row_stride, a.count, a.status);
+        e = cudaLaunchKernelEx(&cfg, topk_kernel<true>, a.logits, a.logits_row_stride, a.logits_width,
+                               a.context_lens, a.next_n, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
+                               a.status);
     } else {
-        topk_kernel<false><<<rows, kTopkThreads, 0, stream>>>(
-            lg, a.logits_row_stride, a.logits_width, a.context_lens, a.next_n, a.row_begin, a.k, a.idx,
-            a.idx_row_stride, a.count, a.status);
+        e = cudaLaunchKernelEx(&cfg, topk_kernel<false>, a.logits, a.logits_row_stride, a.logits_width,
+                               a.context_lens, a.next_n, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
+                               a.status);
     }
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     return check_launch();
 }
 
