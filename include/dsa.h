@@ -156,8 +156,9 @@ DSA_API dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int b
  *           step under graph capture keeps a fixed width; a prefill sizes it to
  *           the actual longest visible length ("Add fp4 indexer for dsv4",
  *           prefill logits width note).
- * Supported: head_dim in {32, 64, 128}; num_heads in {4, 8, 16, 32, 64, 128};
- *           page_kv in {32, 64}; FP8 and MXFP4 (MXFP4 needs head_dim % 32 == 0).
+ * Supported: head_dim in {32, 64, 128} (FP8) or {64, 128} (MXFP4); num_heads in
+ *           {4, 8, 16, 32, 64, 128}; page_kv in {32, 64}.  MXFP4 at head_dim 128
+ *           also needs min(next_n, 256/num_heads) * num_heads <= 128.
  * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (sched_bytes), CUDA.
  */
 DSA_API dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_fmt,
