@@ -76,7 +76,7 @@ struct Mx4Layout {
     static constexpr int kConvStages = D == 128 ? 2 : kMaxConvStages;
     static constexpr int kNB = D / 32;                         // blocks (scales) per row
     static constexpr uint32_t kRawK = kTileTokens * D / 2;     // packed bytes per tile
-    static constexpr uint32_t kScSlot = 128;                   // bytes per page of exponents (<= 128)
+    static constexpr uint32_t kScSlot = 2 * D;                 // bytes per page of exponents (64 x D/32)
     static constexpr uint32_t kConvK = kTileTokens * D;        // e4m3 bytes per tile
     static constexpr uint32_t kLayout = D == 128 ? kLayoutSw128 : kLayoutSw64;
     static constexpr uint32_t kSbo = 8 * D;
