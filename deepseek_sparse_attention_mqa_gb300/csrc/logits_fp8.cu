@@ -325,7 +325,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         int nchunks = 0, L = 0, i0 = 0;
-        for (int t = t0; t < t1 && !*s_abort; ++t) {
+        for (int t = t0; t < t1 && !__any_sync(0xffffffffu, *s_abort); ++t) {
             const bool changed = w.seek(t) || (t == t0);
             if (changed) {
                 __syncwarp();
@@ -340,8 +340,9 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0 && p.status && visible_len(L, p.next_n, i0 + w.ui.nrows - 1) > p.logits_width)
                     atomicOr(p.status, DSA_DEV_WIDTH);
             }
-            if (!mbar_wait(smem_u32(&full_bar[stage]), phase) ||
-                !mbar_wait(smem_u32(&accf_bar[acc]), acc_phase)) {
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase) &&
+                                             mbar_wait(smem_u32(&accf_bar[acc]), acc_phase))) {
                 *s_abort = 1;
                 break;
             }

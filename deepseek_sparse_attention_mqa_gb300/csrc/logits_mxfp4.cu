@@ -422,7 +422,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         int cs = 0, acc = 0;
         uint32_t cph = 0, aph = 0;
         int L = 0, i0 = 0;
-        for (int t = t0; t < t1 && !*s_abort; ++t) {
+        for (int t = t0; t < t1 && !__any_sync(0xffffffffu, *s_abort); ++t) {
             const bool changed = w.seek(t) || (t == t0);
             if (changed) {
                 __syncwarp();
@@ -441,7 +441,8 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     visible_len(L, p.next_n, i0 + w.ui.nrows - 1) > p.logits_width)
                     atomicOr(p.status, DSA_DEV_WIDTH);
             }
-            if (!mbar_wait(smem_u32(&convf[cs]), cph) || !mbar_wait(smem_u32(&accf[acc]), aph)) {
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&convf[cs]), cph) && mbar_wait(smem_u32(&accf[acc]), aph))) {
                 *s_abort = 1;
                 break;
             }

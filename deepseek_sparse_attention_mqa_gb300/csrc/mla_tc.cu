@@ -313,7 +313,9 @@ sparse_mla_tc_kernel(const MlaParams p)
         for (int j = 0; j < nblk && ok; ++j) {
             const int sb = j & 1;
             const uint32_t ph = (j >> 1) & 1;
-            if (!mbar_wait(smem_u32(&s_full[sb]), ph)) {
+            // every wait outcome is made warp-uniform: the tcgen05 loads and stores
+            // below are .sync.aligned and must be executed by all 32 lanes together
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[sb]), ph))) {
                 ok = false;
                 break;
             }
@@ -328,7 +330,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                 mbar_arrive(smem_u32(&s_empty[sb]));
 
             // ---- exchange partial scores with the peer CTA (16-byte units, XOR-swizzled by row)
-            if (!mbar_wait_cluster(smem_u32(x_free), (j & 1) ^ 1)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(x_free), (j & 1) ^ 1))) {
                 ok = false;
                 break;
             }
@@ -340,7 +342,7 @@ sparse_mla_tc_kernel(const MlaParams p)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_remote(peer_x_full);
-            if (!mbar_wait_cluster(smem_u32(x_full), j & 1)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(x_full), j & 1))) {
                 ok = false;
                 break;
             }
@@ -367,7 +369,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                 mbar_arrive_remote(peer_x_free);
 
             // ---- scores in base 2; masked slots are -inf
-            if (!mbar_wait(smem_u32(&lat_full[sb]), ph)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_full[sb]), ph))) {
                 ok = false;
                 break;
             }
@@ -381,30 +383,36 @@ sparse_mla_tc_kernel(const MlaParams p)
             }
             // P of the previous block has been consumed (and O is stable) before
             // P is rewritten or O rescaled
-            if (j > 0 && !mbar_wait(smem_u32(p_empty), (j - 1) & 1)) {
+            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(p_empty), (j - 1) & 1))) {
                 ok = false;
                 break;
             }
             const float m_new = fmaxf(m_run, m_blk);
+            // lazily refreshed running max: a head moves its max only when it grew
+            // by more than 2^8; the O rescale runs for the whole warp (factor 1 on
+            // lanes whose max stays) because TMEM access is warp-collective
+            float f = 1.f;
             if (m_new > m_run + kRescaleLog2) {
                 if (m_run != -INFINITY) {
-                    const float f = exp2f(m_run - m_new);
+                    f = exp2f(m_run - m_new);
                     l_run *= f;
-                    // j > 0 here: O holds blocks < j
-                    tc_fence_after_sync();
-#pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t o[32];
-                        tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                        tmem_st_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
-                    }
-                    tmem_st_wait();
                 }
                 m_run = m_new;
+            }
+            if (__any_sync(0xffffffffu, f != 1.f)) {
+                // j > 0 here: O holds blocks < j and PV(j - 1) has completed
+                tc_fence_after_sync();
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                    tmem_st_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                }
+                tmem_st_wait();
             }
             // P (bf16, token scale folded in for V) -> row h of the swizzled K-major tile
 #pragma unroll
@@ -430,18 +438,18 @@ sparse_mla_tc_kernel(const MlaParams p)
         if (!ok)
             *s_abort = 1;
         // ---- epilogue: O / l -> bf16 out[row][h][crank*256 + v], lse (natural log)
-        const bool have = nblk > 0 && mbar_wait(smem_u32(o_done), 0) && ok && !*s_abort;
+        const bool have = __all_sync(0xffffffffu, nblk > 0 && ok && mbar_wait(smem_u32(o_done), 0) && !*s_abort);
         tc_fence_after_sync();
         const float inv = (have && l_run > 0.f) ? 1.f / l_run : 0.f;
-        if (h < p.num_heads) {
-            __nv_bfloat16* orow = p.out + (static_cast<int64_t>(row) * p.num_heads + h) * 512 + crank * 256;
+        __nv_bfloat16* orow = p.out + (static_cast<int64_t>(row) * p.num_heads + h) * 512 + crank * 256;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-                uint32_t o[32];
-                if (have) {
-                    tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
-                    tmem_ld_wait();
-                }
+        for (int c = 0; c < 8; ++c) {
+            uint32_t o[32];
+            if (have) {                                   // warp-uniform: all lanes load
+                tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                tmem_ld_wait();
+            }
+            if (h < p.num_heads) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
                     uint32_t pk[4];
@@ -455,10 +463,10 @@ sparse_mla_tc_kernel(const MlaParams p)
                     *reinterpret_cast<uint4*>(orow + c * 32 + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
-            if (crank == 0)
-                p.lse[static_cast<int64_t>(row) * p.num_heads + h] =
-                    (have && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
+        if (crank == 0 && h < p.num_heads)
+            p.lse[static_cast<int64_t>(row) * p.num_heads + h] =
+                (have && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
 
     __syncwarp();
