@@ -15,11 +15,13 @@
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer, kind::f8f6f4:
 //               D[128 tokens x N] += K_tile[128 x D] * Q[N x D]^T, N = rows x heads.
 //               Each TMEM lane is one token and each column one (row, head).
-//   warps 2-5   epilogue: tcgen05.ld of the thread's own lane, then the whole
-//               relu / head-weighting / k_scale reduction is thread-local (no
-//               shuffles), and each warp stores 32 consecutive logits per row.
-//   Two TMEM accumulators let the epilogue of tile i overlap the MMA of tile i+1;
-//   the stage ring keeps enough K bytes in flight to cover HBM latency.
+//   warps 2-9   epilogue, two warpgroups taking alternate tiles (so two warps per
+//               scheduler hide each other's TMEM-load and barrier latency):
+//               tcgen05.ld of the thread's own lane, then the whole relu /
+//               head-weighting / k_scale reduction is thread-local (no shuffles),
+//               and each warp stores 32 consecutive logits per row.
+//   Four TMEM accumulators let the epilogues of earlier tiles overlap the MMA of
+//   later ones; the stage ring keeps enough K bytes in flight to cover HBM latency.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,7 +36,8 @@ namespace dsa {
 namespace {
 
 constexpr int kMaxStages = 16;
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 320;  // 10 warps: producer, MMA, two epilogue warpgroups
+constexpr int kEpiWarps = 8;
 constexpr int kPageCache = 512; // physical page ids cached by the producer warp
 constexpr int kMaxAcc = 4;      // TMEM accumulators in flight
 
@@ -83,7 +86,7 @@ __host__ __device__ __forceinline__ SmemMap smem_map(int D, int stages, uint32_t
     m.q_off = m.k_off + stages * kTileTokens * D;
     m.sc_off = m.q_off + 2 * q_buf_bytes;
     m.w_off = m.sc_off + stages * kTileTokens * 4;
-    m.pc_off = m.w_off + 4 * kMaxUnitCols * 4;               // one weight copy per epilogue warp
+    m.pc_off = m.w_off + kEpiWarps * kMaxUnitCols * 4;       // one weight copy per epilogue warp
     m.bar_off = m.pc_off + kPageCache * 4;
     m.misc_off = m.bar_off + (2 * kMaxStages + 2 * kMaxAcc + 4 + 1) * 8;
     m.total = m.misc_off + 16;
@@ -136,7 +139,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1 + 4);   // MMA commit + 4 epilogue warps
+            mbar_init(smem_u32(&empty_bar[s]), 1 + 4);   // MMA commit + the tile's 4 epilogue warps
         }
         for (int a = 0; a < kMaxAcc; ++a) {
             mbar_init(smem_u32(&accf_bar[a]), 1);
@@ -318,6 +321,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     } else {
         // =========================== epilogue ===============================
         const int quarter = warp & 3;                 // TMEM lanes this warp may access
+        const int group = (warp - 2) >> 2;            // epilogue warpgroup: takes tiles t0+group, t0+group+2, ...
         const int tok = quarter * 32 + lane;          // token of this thread within the tile
         float* wS = sW + (warp - 2) * kMaxUnitCols;   // this warp's copy of the unit weights
         TileWalk w;
@@ -337,8 +341,20 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 __syncwarp();
                 L = max(0, p.context_lens[w.ui.seq]);
                 i0 = w.ui.first_row - w.ui.seq * p.next_n;
-                if (lane == 0 && p.status && visible_len(L, p.next_n, i0 + w.ui.nrows - 1) > p.logits_width)
+                if (lane == 0 && group == 0 && p.status &&
+                    visible_len(L, p.next_n, i0 + w.ui.nrows - 1) > p.logits_width)
                     atomicOr(p.status, DSA_DEV_WIDTH);
+            }
+            if (((t - t0) & 1) != group) {            // the other warpgroup's tile
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                if (++acc == p.n_acc) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+                continue;
             }
             // warp-uniform outcome: the TMEM loads below are warp-collective
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase) &&

@@ -10,8 +10,9 @@
 // GB300 design: one CLUSTER of two CTAs per query row.  The output O
 // (128 heads x 512 fp32) fills a whole TMEM, so it is split by value dims:
 // CTA 0 owns latent dims [0, 256) and CTA 1 owns [256, d_qk); each keeps its
-// part of Q (bf16, swizzled K-major) resident, gathers and widens its part of
-// the selected latent rows (FP8 -> bf16, exact) and computes a PARTIAL score
+// part of Q resident (f16, swizzled K-major, times a per-head power of two that
+// fits it to f16 range exactly), gathers and widens its part of the selected
+// latent rows (FP8 -> f16, exact) and computes a PARTIAL score
 // S_c = Q_c K_c^T on the tensor cores.  The two partials are exchanged through
 // distributed shared memory, so both CTAs hold the same S = S_0 + S_1 (identical
 // arithmetic, hence identical softmax decisions) and each accumulates its half
@@ -20,11 +21,12 @@
 //   warps 0-3  softmax: thread = head = TMEM lane.  Exchange partial scores,
 //              scale by token scale * softmax scale, online max / sum in base 2
 //              with a lazily refreshed running max (O in TMEM is rescaled only
-//              when the max grows by more than 2^8), write P (bf16, with the
-//              token scale folded in for V) to shared memory, finally normalise
+//              when the max grows by more than 2^8), write P (f16, with the
+//              token scale folded in for V; f16 rather than bf16 keeps its
+//              rounding at 2^-12) to shared memory, finally normalise
 //              O and store bf16 out / fp32 lse.
 //   warps 4-7  gather: per 64-token block, look up each selected token through
-//              the block table, load its FP8 slice, widen to bf16 into a 128B-
+//              the block table, load its FP8 slice, widen to f16 into a 128B-
 //              swizzled K-major tile (zeros for unused slots).
 //   warp 8     TMEM allocator + MMA issuer: S = Q K^T (M=128, N=64) and
 //              O += P V (M=128, N=256, V read MN-major from the same tile).
@@ -44,13 +46,14 @@ namespace {
 constexpr int kNT = 64;                 // selected tokens per block
 constexpr int kMaxChunks = 5;           // 64-dim chunks per CTA (576 = 4 + 5 chunks)
 constexpr int kVChunks = 4;             // 256 value dims per CTA
-constexpr int kQChunkBytes = 128 * 128; // 128 heads x 64 bf16
-constexpr int kLChunkBytes = kNT * 128; // 64 tokens x 64 bf16
+constexpr int kQChunkBytes = 128 * 128; // 128 heads x 64 f16
+constexpr int kLChunkBytes = kNT * 128; // 64 tokens x 64 f16
 constexpr int kThreads = 288;           // 9 warps
 constexpr int kConvWarp0 = 4;
 constexpr int kMmaWarp = 8;
 constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, O at 256
 constexpr float kRescaleLog2 = 8.f;     // refresh the running max only past 2^8
+constexpr int kGatherItems = (kNT * kMaxChunks * 4 + 127) / 128;   // 16-byte segments per gather thread
 
 struct MlaParams {
     const __nv_bfloat16* q;
@@ -77,7 +80,7 @@ struct MlaParams {
 };
 
 struct MlaSmem {
-    uint32_t q, lat, p, x, scale, valid, bar, misc, total;
+    uint32_t q, lat, p, x, scale, valid, qexp, bar, misc, total;
 };
 
 __host__ __device__ constexpr MlaSmem mla_smem()
@@ -89,14 +92,15 @@ __host__ __device__ constexpr MlaSmem mla_smem()
     m.x = m.p + 128 * 128;
     m.scale = m.x + 128 * kNT * 4;
     m.valid = m.scale + 2 * kNT * 4;
-    m.bar = m.valid + 2 * kNT * 4;
+    m.qexp = m.valid + 2 * kNT * 4;
+    m.bar = m.qexp + 128 * 4;
     m.misc = m.bar + 16 * 8;
     m.total = m.misc + 16;
     return m;
 }
 
-// 16 e4m3 bytes -> 16 bf16 (exact: every e4m3 value is a bf16 value).
-__device__ __forceinline__ void e4m3x16_to_bf16x16(const uint4 v, uint4& lo, uint4& hi)
+// 16 e4m3 bytes -> 16 f16 (exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ void e4m3x16_to_f16x16(const uint4 v, uint4& lo, uint4& hi)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[8];
@@ -106,13 +110,17 @@ __device__ __forceinline__ void e4m3x16_to_bf16x16(const uint4 v, uint4& lo, uin
         for (int hh = 0; hh < 2; ++hh) {
             const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hh)) & 0xFFFFu);
             const __half2_raw h2r = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-            const float2 f = __half22float2(__half2(h2r));
-            const __nv_bfloat162 b = __float22bfloat162_rn(f);
-            o[2 * i + hh] = *reinterpret_cast<const uint32_t*>(&b);
+            o[2 * i + hh] = static_cast<uint32_t>(h2r.x) | (static_cast<uint32_t>(h2r.y) << 16);
         }
     }
     lo = make_uint4(o[0], o[1], o[2], o[3]);
     hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// 2^e as fp32 for |e| <= 126 (exact).
+__device__ __forceinline__ float exp2_int(int e)
+{
+    return __int_as_float((127 + e) << 23);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -127,6 +135,7 @@ sparse_mla_tc_kernel(const MlaParams p)
     uint8_t* sX = smem + mp.x;
     float* sScale = reinterpret_cast<float*>(smem + mp.scale);
     int* sValid = reinterpret_cast<int*>(smem + mp.valid);
+    int* sQexp = reinterpret_cast<int*>(smem + mp.qexp);       // per-head power-of-two Q scale
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + mp.bar);
     uint64_t* q_full = bars + 0;
     uint64_t* lat_full = bars + 1;   // [2]
@@ -180,16 +189,50 @@ sparse_mla_tc_kernel(const MlaParams p)
     if (warp >= kConvWarp0 && warp < kMmaWarp) {
         // ================================ gather ================================
         const int ct = threadIdx.x - kConvWarp0 * 32;   // 0..127
-        // Q slice -> swizzled K-major tile: row = head, 8 units of 16 B per chunk
-        const int qunits = 128 * nchunk * 8;
-        for (int u = ct; u < qunits; u += 128) {
-            const int h = u / (nchunk * 8), rem = u % (nchunk * 8);
-            const int ch = rem >> 3, un = rem & 7;
-            uint4 v = make_uint4(0, 0, 0, 0);
+        // Q slice -> f16 swizzled K-major tile (row = head, 8 units of 16 B per
+        // chunk).  Thread ct owns head ct: Q is scaled by 2^e, e chosen per head
+        // from this CTA's slice so that max|q| 2^e lies in [2^14, 2^15) -- exact,
+        // and inside f16 range whatever the bf16 magnitudes; the partial scores
+        // are scaled back by 2^-e in fp32.
+        {
+            const int h = ct;
+            const __nv_bfloat16* qh =
+                p.q + (static_cast<int64_t>(row) * p.num_heads + h) * p.d_qk + c_lo * 64;
+            float amax = 0.f;
             if (h < p.num_heads)
-                v = *reinterpret_cast<const uint4*>(
-                    p.q + (static_cast<int64_t>(row) * p.num_heads + h) * p.d_qk + (c_lo + ch) * 64 + un * 8);
-            *reinterpret_cast<uint4*>(sQ + ch * kQChunkBytes + swizzled_offset(h, un, 128)) = v;
+                for (int u = 0; u < nchunk * 8; ++u) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(qh + u * 8);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[i]));
+                        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                }
+            int e = 0;
+            if (amax > 0.f && amax <= 3.0e38f) {
+                int ex;
+                frexpf(amax, &ex);                          // amax in [2^(ex-1), 2^ex)
+                e = max(-100, min(100, 15 - ex));
+            }
+            sQexp[h] = e;
+            const float sc = exp2_int(e);
+            for (int u = 0; u < nchunk * 8; ++u) {
+                uint4 o = make_uint4(0, 0, 0, 0);
+                if (h < p.num_heads) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(qh + u * 8);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t r4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[i]));
+                        const __half2 hf = __floats2half2_rn(f.x * sc, f.y * sc);
+                        r4[i] = *reinterpret_cast<const uint32_t*>(&hf);
+                    }
+                    o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+                }
+                *reinterpret_cast<uint4*>(sQ + (u >> 3) * kQChunkBytes + swizzled_offset(h, u & 7, 128)) = o;
+            }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -205,36 +248,59 @@ sparse_mla_tc_kernel(const MlaParams p)
                 break;
             }
             uint8_t* tile = sLat + st * (kMaxChunks * kLChunkBytes);
-            for (int w = ct; w < kNT * nseg; w += 128) {
-                const int t = w / nseg, seg = w % nseg;
-                const int jj = j * kNT + t;
-                int s = jj < p.k ? irow[jj] : -1;
-                int page = -1;
-                if (s >= 0) {
-                    const int lp = s / p.page_kv;
+            // three phases, each issuing all of this thread's independent loads
+            // back to back: selected indices, then block-table entries, then the
+            // latent segments (one memory latency each instead of one chain per item)
+            int tok[kGatherItems], pg[kGatherItems];
+#pragma unroll
+            for (int i = 0; i < kGatherItems; ++i) {
+                const int w = ct + 128 * i;
+                const int jj = j * kNT + w / nseg;
+                tok[i] = (w < kNT * nseg && jj < p.k) ? irow[jj] : -1;
+            }
+#pragma unroll
+            for (int i = 0; i < kGatherItems; ++i) {
+                pg[i] = -1;
+                if (tok[i] >= 0) {
+                    const int lp = tok[i] / p.page_kv;
                     if (lp < p.max_pages)
-                        page = p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp];
-                    if (page < 0 || page >= p.num_pages) {
-                        if (seg == 0 && p.status)
+                        pg[i] = p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp];
+                    if (pg[i] < 0 || pg[i] >= p.num_pages) {
+                        if ((ct + 128 * i) % nseg == 0 && p.status)
                             atomicOr(p.status, DSA_DEV_BAD_INDEX);
-                        s = -1;
+                        tok[i] = -1;
                     }
                 }
-                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                if (s >= 0) {
-                    const uint8_t* src = p.vals + page * p.vps + (s % p.page_kv) * p.vts + (c_lo * 64 + seg * 16);
-                    e4m3x16_to_bf16x16(*reinterpret_cast<const uint4*>(src), lo, hi);
+            }
+            uint4 raw[kGatherItems];
+#pragma unroll
+            for (int i = 0; i < kGatherItems; ++i) {
+                raw[i] = make_uint4(0, 0, 0, 0);
+                if (tok[i] >= 0) {
+                    const int seg = (ct + 128 * i) % nseg;
+                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + pg[i] * p.vps + (tok[i] % p.page_kv) * p.vts +
+                                                             (c_lo * 64 + seg * 16));
                 }
+            }
+#pragma unroll
+            for (int i = 0; i < kGatherItems; ++i) {
+                const int w = ct + 128 * i;
+                if (w >= kNT * nseg)
+                    continue;
+                const int t = w / nseg, seg = w % nseg;
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                if (tok[i] >= 0)
+                    e4m3x16_to_f16x16(raw[i], lo, hi);
                 uint8_t* chunk = tile + (seg >> 2) * kLChunkBytes;
                 const int un = (seg & 3) * 2;
                 *reinterpret_cast<uint4*>(chunk + swizzled_offset(t, un, 128)) = lo;
                 *reinterpret_cast<uint4*>(chunk + swizzled_offset(t, un + 1, 128)) = hi;
                 if (seg == 0) {
                     float sc = 0.f;
-                    if (s >= 0)
-                        sc = *reinterpret_cast<const float*>(p.scs + page * p.sps + (s % p.page_kv) * p.sts);
+                    if (tok[i] >= 0)
+                        sc = *reinterpret_cast<const float*>(p.scs + pg[i] * p.sps + (tok[i] % p.page_kv) * p.sts);
                     sScale[st * kNT + t] = sc;
-                    sValid[st * kNT + t] = s >= 0;
+                    sValid[st * kNT + t] = tok[i] >= 0;
                 }
             }
             fence_proxy_async_smem();
@@ -245,8 +311,8 @@ sparse_mla_tc_kernel(const MlaParams p)
     } else if (warp == kMmaWarp) {
         // ================================ MMA ===================================
         if (lane == 0) {
-            const uint32_t idesc_qk = make_idesc(1, 1, 0, 128, kNT);
-            const uint32_t idesc_pv = make_idesc(1, 1, 1, 128, 256);
+            const uint32_t idesc_qk = make_idesc(0, 0, 0, 128, kNT);     // f16 x f16 -> f32
+            const uint32_t idesc_pv = make_idesc(0, 0, 1, 128, 256);
             bool ok = mbar_wait(smem_u32(q_full), 0);
             auto issue_qk = [&](int j) -> bool {
                 const int st = j & 1;
@@ -309,7 +375,9 @@ sparse_mla_tc_kernel(const MlaParams p)
         const uint32_t peer_x_full = mapa_shared(smem_u32(x_full), peer);
         const uint32_t peer_x_free = mapa_shared(smem_u32(x_free), peer);
         float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
+        // this head's Q was stored times 2^e; partial scores are scaled back (exact)
+        bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(q_full), 0));
+        const float qback = exp2_int(-sQexp[h]);
         for (int j = 0; j < nblk && ok; ++j) {
             const int sb = j & 1;
             const uint32_t ph = (j >> 1) & 1;
@@ -328,6 +396,11 @@ sparse_mla_tc_kernel(const MlaParams p)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&s_empty[sb]));
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                ra[i] = __float_as_uint(__uint_as_float(ra[i]) * qback);
+                rb[i] = __float_as_uint(__uint_as_float(rb[i]) * qback);
+            }
 
             // ---- exchange partial scores with the peer CTA (16-byte units, XOR-swizzled by row)
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(x_free), (j & 1) ^ 1))) {
@@ -414,7 +487,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                 }
                 tmem_st_wait();
             }
-            // P (bf16, token scale folded in for V) -> row h of the swizzled K-major tile
+            // P (f16, token scale folded in for V) -> row h of the swizzled K-major tile
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 uint32_t pk[4];
@@ -424,7 +497,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                     const float p0 = (m_run == -INFINITY || sco[t] == -INFINITY) ? 0.f : exp2f(sco[t] - m_run);
                     const float p1 = (m_run == -INFINITY || sco[t + 1] == -INFINITY) ? 0.f : exp2f(sco[t + 1] - m_run);
                     l_run += p0 + p1;
-                    const __nv_bfloat162 b = __floats2bfloat162_rn(p0 * scl[t], p1 * scl[t + 1]);
+                    const __half2 b = __floats2half2_rn(p0 * scl[t], p1 * scl[t + 1]);
                     pk[q2] = *reinterpret_cast<const uint32_t*>(&b);
                 }
                 *reinterpret_cast<uint4*>(sP + swizzled_offset(h, u, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);

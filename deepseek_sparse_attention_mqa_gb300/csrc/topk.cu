@@ -99,6 +99,7 @@ struct TopkShared {
     int ws[32];
     int bin, above;
     int nout, ncand;
+    int res_above, res_cand;      // this CTA's reserved output / candidate ranges
     uint32_t kmin, kmax;
 };
 
@@ -267,21 +268,36 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     }
     const int n_direct = k - need;                        // keys > hi are taken outright
 
-    // ---- 3. output pass: keys above the bin out, the bin's keys to CTA 0 as candidates
-    for (int base = 0; base < n; base += kThreads) {
-        const int j = base + tid;
-        uint32_t key = 0;
-        if (j < n)
-            key = key_at(j);
-        const bool above = j < n && key > hi;
-        const bool cand = j < n && key >= lo && key <= hi;
-        const int slot = warp_append_cluster(above, c0_nout);
-        if (slot >= 0)
-            out[slot] = s_lo + j;
-        const int cs = warp_append_cluster(cand, c0_ncand);
-        if (cs >= 0 && cs < kCandCap) {
-            st_cluster_u32(c0_ck + 4u * cs, key);
-            st_cluster_u32(c0_cp + 4u * cs, static_cast<uint32_t>(s_lo + j));
+    // ---- 3. output pass: keys above the bin out, the bin's keys to CTA 0 as
+    // candidates.  Each CTA counts first and reserves its ranges with one
+    // cluster atomic per counter, then writes at thread-local offsets.
+    int n_above = 0, n_cand = 0;
+    for (int j = tid; j < n; j += kThreads) {
+        const uint32_t key = key_at(j);
+        n_above += key > hi ? 1 : 0;
+        n_cand += (key >= lo && key <= hi) ? 1 : 0;
+    }
+    int tot_above, tot_cand;
+    const int off_above = block_incl_scan(n_above, sh.ws, &tot_above) - n_above;
+    const int off_cand = block_incl_scan(n_cand, sh.ws, &tot_cand) - n_cand;
+    if (tid == 0) {
+        sh.res_above = tot_above ? static_cast<int>(atom_add_cluster(c0_nout, static_cast<uint32_t>(tot_above))) : 0;
+        sh.res_cand = tot_cand ? static_cast<int>(atom_add_cluster(c0_ncand, static_cast<uint32_t>(tot_cand))) : 0;
+    }
+    __syncthreads();
+    {
+        int oa = sh.res_above + off_above, oc = sh.res_cand + off_cand;
+        for (int j = tid; j < n; j += kThreads) {
+            const uint32_t key = key_at(j);
+            if (key > hi) {
+                out[oa++] = s_lo + j;
+            } else if (key >= lo) {
+                if (oc < kCandCap) {
+                    st_cluster_u32(c0_ck + 4u * oc, key);
+                    st_cluster_u32(c0_cp + 4u * oc, static_cast<uint32_t>(s_lo + j));
+                }
+                ++oc;
+            }
         }
     }
     cluster_sync();                                       // all candidates landed in CTA 0
