@@ -22,6 +22,7 @@ EXPORTS = (
     "dsa_status_string", "dsa_last_cuda_error", "dsa_version", "dsa_indexer_schedule_bytes",
     "dsa_indexer_build_schedule", "indexer_mqa_logits_paged", "dsa_topk_workspace_bytes",
     "indexer_topk", "dsa_sparse_mla_workspace_bytes", "sparse_mla_decode", "dsa_get_device_status",
+    "indexer_mqa_logits_paged_noalloc",
 )
 
 
@@ -80,6 +81,10 @@ def lib():
         L.indexer_mqa_logits_paged.argtypes = [
             _vp, _vp, _i, _vp, _i, ctypes.POINTER(PagedCache), _vp, _i, _i, _i, _i, _vp, _sz,
             _vp, _i64, _i, _vp, _vp]
+        L.indexer_mqa_logits_paged_noalloc.restype = _i
+        L.indexer_mqa_logits_paged_noalloc.argtypes = [
+            _vp, _vp, _i, _vp, _i, ctypes.POINTER(PagedCache), _vp, _i, _i, _i, _i, _vp, _i64, _i,
+            _vp, _vp]
         L.dsa_topk_workspace_bytes.restype = _sz
         L.dsa_topk_workspace_bytes.argtypes = [_i, _i, _i]
         L.indexer_topk.restype = _i
@@ -148,6 +153,17 @@ def mqa_logits(q, q_scales, fmt, weights, num_heads, cache: PagedCache, context_
         _ptr(context_lens), batch, next_n, row_begin, row_end, _ptr(sched),
         sched.numel() * sched.element_size(), _ptr(logits), logits.stride(0), int(logits_width),
         _ptr(status), _stream(stream)), "indexer_mqa_logits_paged")
+
+
+def mqa_logits_noalloc(q, q_scales, fmt, weights, num_heads, cache: PagedCache, context_lens,
+                       batch, next_n, row_begin, row_end, logits, logits_width, status=None,
+                       stream=None):
+    """indexer_mqa_logits_paged_noalloc: the schedule lives in the library's fixed
+    device array, so no schedule buffer is passed."""
+    _check(lib().indexer_mqa_logits_paged_noalloc(
+        _ptr(q), _ptr(q_scales), int(fmt), _ptr(weights), num_heads, ctypes.byref(cache),
+        _ptr(context_lens), batch, next_n, row_begin, row_end, _ptr(logits), logits.stride(0),
+        int(logits_width), _ptr(status), _stream(stream)), "indexer_mqa_logits_paged_noalloc")
 
 
 def topk_workspace_bytes(rows, width, k) -> int:

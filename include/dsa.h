@@ -170,6 +170,37 @@ DSA_API dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales,
                                     int32_t* status_dev, void* stream);
 
 /*
+ * Allocation-free variant of indexer_mqa_logits_paged() (no counterpart on the
+ * pages; it exists for callers of this library that cannot allocate device
+ * memory -- e.g. a plugin running under a host framework that owns the device
+ * allocator and offers no hook, or a serving path that forbids cudaMalloc
+ * while handling requests).
+ *
+ * Same arguments, operation, outputs and errors as indexer_mqa_logits_paged(),
+ * minus the schedule buffer: the schedule is built into a fixed 256 KiB array
+ * inside the library (one per GPU the process uses, held until exit), then the
+ * logits kernel runs on it -- two launches on `stream`, nothing allocated.
+ *  - Limit: at most 16382 work units (units = sequences for decode with
+ *    next_n * num_heads <= 256; ceil(rows / (256 / num_heads)) for prefill);
+ *    larger calls return DSA_ERR_CAPACITY and enqueue nothing.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race on it and must be serialised by the
+ *    caller.  Nothing needs clearing between calls: each call rewrites every
+ *    schedule word it later reads.
+ */
+DSA_API dsa_status indexer_mqa_logits_paged_noalloc(const void* q, const void* q_scales, int q_fmt,
+                                                    const float* weights, int num_heads,
+                                                    const dsa_paged_cache* k,
+                                                    const int32_t* context_lens, int batch,
+                                                    int next_n, int row_begin, int row_end,
+                                                    float* logits, int64_t logits_row_stride,
+                                                    int logits_width, int32_t* status_dev,
+                                                    void* stream);
+
+/*
  * Per-row top-k of the indexer logits ("feat(deepseek_v4): Add fp4 indexer for
  * dsv4": indexer_score_topk; "Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels":
  * dynamic per-row top-k lengths).  For each row, the k largest of
