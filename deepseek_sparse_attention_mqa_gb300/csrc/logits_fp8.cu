@@ -8,10 +8,13 @@
 // TMA warps each owning a KV group, 2-3 stages to fit SM120's 99 KiB.
 //
 // GB300 design (one persistent CTA per SM, warp-specialised):
-//   warp 0      TMA producer: per 128-token tile, one 3-D box per physical page
-//               (2 boxes at page 64, 4 at page 32) into a 128B/64B/32B-swizzled
-//               K-major stage, plus one box of per-token fp32 scales per page;
-//               the unit's q rows ([rows x heads, D], K-major) once per unit.
+//   warps 0,10-12  TMA producers, taking tiles round-robin: per 128-token tile,
+//               one 3-D box per physical page (2 boxes at page 64, 4 at page 32)
+//               into a 128B/64B/32B-swizzled K-major stage, plus one box of
+//               per-token fp32 scales per page; warp 0 also loads the unit's q
+//               rows ([rows x heads, D], K-major) once per unit.  A single
+//               producer warp spends about twice the HBM time of a tile on the
+//               copies' issue and the page bookkeeping, so several share it.
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer, kind::f8f6f4:
 //               D[128 tokens x N] += K_tile[128 x D] * Q[N x D]^T, N = rows x heads.
 //               Each TMEM lane is one token and each column one (row, head).
@@ -36,9 +39,10 @@ namespace dsa {
 namespace {
 
 constexpr int kMaxStages = 16;
-constexpr int kThreads = 320;  // 10 warps: producer, MMA, two epilogue warpgroups
 constexpr int kEpiWarps = 8;
-constexpr int kPageCache = 512; // physical page ids cached by the producer warp
+constexpr int kProd = 4;        // TMA producer warps (warp 0 and the warps after the epilogue)
+constexpr int kThreads = 32 * (2 + kEpiWarps + kProd - 1);  // producers, MMA, two epilogue warpgroups
+constexpr int kPageCache = 512; // physical page ids cached by each producer warp
 constexpr int kMaxAcc = 4;      // TMEM accumulators in flight
 
 struct LogitsParams {
@@ -87,7 +91,7 @@ __host__ __device__ __forceinline__ SmemMap smem_map(int D, int stages, uint32_t
     m.sc_off = m.q_off + 2 * q_buf_bytes;
     m.w_off = m.sc_off + stages * kTileTokens * 4;
     m.pc_off = m.w_off + kEpiWarps * kMaxUnitCols * 4;       // one weight copy per epilogue warp
-    m.bar_off = m.pc_off + kPageCache * 4;
+    m.bar_off = m.pc_off + kProd * kPageCache * 4;
     m.misc_off = m.bar_off + (2 * kMaxStages + 2 * kMaxAcc + 4 + 1) * 8;
     m.total = m.misc_off + 16;
     return m;
@@ -168,25 +172,30 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int P = p.page_kv;
     const int pages_per_tile = kTileTokens / P;
 
-    if (warp == 0) {
-        // =========================== TMA producer ===========================
-        // The whole warp walks the tiles; lane 0 issues the copies.  Physical
-        // page ids are fetched by all 32 lanes at once into a shared-memory
-        // cache (one global-memory latency per refill instead of one per tile).
+    if (warp == 0 || warp >= 2 + kEpiWarps) {
+        // =========================== TMA producers ==========================
+        // kProd warps share the tile stream: producer pi issues the tiles whose
+        // CTA-local ordinal j has j % kProd == pi, so the per-tile work around
+        // the copies (page lookup, barrier waits, descriptor fetch) of several
+        // tiles overlaps.  The stage count is a multiple of kProd, so every
+        // stage has exactly one producer and its empty/full phases advance in
+        // that producer's order.  Producer 0 also loads each unit's q rows.
+        // Physical page ids are fetched by all 32 lanes at once into the warp's
+        // own shared-memory cache (one global-memory latency per refill).
+        const int pi = warp == 0 ? 0 : warp - (1 + kEpiWarps);
+        int* my_pages = s_pages + pi * kPageCache;
         TileWalk w;
         w.start(wp, units, total_tiles, t0);
-        int stage = 0;
-        uint32_t phase = 0;
         int ucount = 0;
         long long issued = 0;
         int pc_unit = -1, pc_lp0 = 0, pc_cnt = 0;
         for (int t = t0; t < t1; ++t) {
-            if (*s_abort)
+            if (__any_sync(0xffffffffu, *s_abort))
                 break;
             const bool changed = w.seek(t) || (t == t0);
             int ok = 1;
             if (changed) {
-                if (lane == 0) {
+                if (pi == 0 && lane == 0) {
                     const int qb = ucount & 1;
                     ok = mbar_wait(smem_u32(&qe_bar[qb]), ((ucount >> 1) & 1) ^ 1);
                     if (ok) {
@@ -197,6 +206,17 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 ++ucount;
             }
+            const int j = t - t0;
+            if (j % kProd != pi) {
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    if (lane == 0)
+                        *s_abort = 1;
+                    break;
+                }
+                continue;
+            }
+            const int stage = j % p.stages;
+            const uint32_t phase = static_cast<uint32_t>((j / p.stages) & 1);
             const int tt = t - w.ui.tile_begin;              // tile index inside the unit
             const int lp_first = tt * pages_per_tile;
             if (w.u != pc_unit || lp_first + pages_per_tile > pc_lp0 + pc_cnt) {
@@ -211,7 +231,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     int pg = -1;
                     if (lp < lp_vis && lp < p.max_pages)
                         pg = p.block_table[static_cast<int64_t>(w.ui.seq) * p.bt_stride + lp];
-                    s_pages[i] = pg;
+                    my_pages[i] = pg;
                 }
                 __syncwarp();
                 pc_unit = w.u;
@@ -223,13 +243,13 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (ok) {
                     int phys[kTileTokens / 32];
                     uint32_t bytes = 0;
-                    for (int j = 0; j < pages_per_tile; ++j) {
-                        const int lp = lp_first + j;
-                        phys[j] = -1;
+                    for (int jp = 0; jp < pages_per_tile; ++jp) {
+                        const int lp = lp_first + jp;
+                        phys[jp] = -1;
                         if (lp * P < w.ui.vis_max) {
-                            const int pg = s_pages[lp - pc_lp0];
+                            const int pg = my_pages[lp - pc_lp0];
                             if (pg >= 0 && pg < p.num_pages) {
-                                phys[j] = pg;
+                                phys[jp] = pg;
                                 bytes += static_cast<uint32_t>(P) * (D + 4);
                             } else if (p.status) {
                                 atomicOr(p.status, DSA_DEV_BAD_PAGE);
@@ -238,11 +258,11 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     }
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
-                    for (int j = 0; j < pages_per_tile; ++j) {
-                        if (phys[j] < 0)
+                    for (int jp = 0; jp < pages_per_tile; ++jp) {
+                        if (phys[jp] < 0)
                             continue;
-                        tma_load_3d(smem_u32(sK + stage * T::kTileBytes + j * P * D), &tm_k, fb, 0, 0, phys[j]);
-                        tma_load_2d(smem_u32(sS + stage * kTileTokens + j * P), &tm_s, fb, 0, phys[j]);
+                        tma_load_3d(smem_u32(sK + stage * T::kTileBytes + jp * P * D), &tm_k, fb, 0, 0, phys[jp]);
+                        tma_load_2d(smem_u32(sS + stage * kTileTokens + jp * P), &tm_s, fb, 0, phys[jp]);
                     }
                 }
             }
@@ -253,18 +273,20 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 break;
             }
             ++issued;
-            if (++stage == p.stages) {
-                stage = 0;
-                phase ^= 1;
-            }
         }
         // drain: every copy this warp issued has landed before the CTA exits
+        // (its stages are its own, so the last stages/kProd of its tiles are
+        // the only ones whose full phase may still be pending)
         if (lane == 0) {
-            const long long lo = issued > p.stages ? issued - p.stages : 0;
-            for (long long j = lo; j < issued; ++j)
-                mbar_wait(smem_u32(&full_bar[j % p.stages]), static_cast<uint32_t>((j / p.stages) & 1));
-            for (int j = ucount > 2 ? ucount - 2 : 0; j < ucount; ++j)
-                mbar_wait(smem_u32(&qf_bar[j & 1]), static_cast<uint32_t>((j >> 1) & 1));
+            const long long per = p.stages / kProd;
+            const long long lo = issued > per ? issued - per : 0;
+            for (long long n = lo; n < issued; ++n) {
+                const long long jj = pi + n * kProd;
+                mbar_wait(smem_u32(&full_bar[jj % p.stages]), static_cast<uint32_t>((jj / p.stages) & 1));
+            }
+            if (pi == 0)
+                for (int u = ucount > 2 ? ucount - 2 : 0; u < ucount; ++u)
+                    mbar_wait(smem_u32(&qf_bar[u & 1]), static_cast<uint32_t>((u >> 1) & 1));
         }
     } else if (warp == 1) {
         // =========================== MMA issuer =============================
@@ -514,9 +536,10 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
 
     // as many stages as fit next to the q buffers
     const int budget = std::min(dev.max_smem_optin, 227 * 1024) - 1024;
+    // (a multiple of the producer count: each producer owns every kProd-th stage)
     int stages = kMaxStages;
-    while (stages > 2 && static_cast<int>(smem_map(D, stages, q_buf_bytes).total) > budget)
-        --stages;
+    while (stages > kProd && static_cast<int>(smem_map(D, stages, q_buf_bytes).total) > budget)
+        stages -= kProd;
     const SmemMap mp = smem_map(D, stages, q_buf_bytes);
     if (static_cast<int>(mp.total) > budget)
         return DSA_ERR_UNSUPPORTED;

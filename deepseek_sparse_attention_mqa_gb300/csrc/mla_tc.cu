@@ -53,7 +53,7 @@ constexpr int kConvWarp0 = 4;
 constexpr int kMmaWarp = 8;
 constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, O at 256
 constexpr float kRescaleLog2 = 8.f;     // refresh the running max only past 2^8
-constexpr int kGatherItems = (kNT * kMaxChunks * 4 + 127) / 128;   // 16-byte segments per gather thread
+constexpr int kGatherItems = (16 * kMaxChunks * 4 + 31) / 32;      // 16-byte segments per gather lane
 
 struct MlaParams {
     const __nv_bfloat16* q;
@@ -241,67 +241,73 @@ sparse_mla_tc_kernel(const MlaParams p)
 
         const int32_t* irow = p.idx + static_cast<int64_t>(row) * p.idx_stride;
         const int nseg = nchunk * 4;                    // 16-byte FP8 segments per token
-        for (int j = 0; j < nblk && !*s_abort; ++j) {
+        const int gw = warp - kConvWarp0;               // this warp gathers tokens [16 gw, 16 gw + 16) of a block
+        // Resolve the warp's 16 tokens of block jb (lane l < 16 owns one): index ->
+        // block table -> byte offset of the latent row and its fp32 scale.
+        auto resolve = [&](int jb, int64_t& off, int& valid, float& scale) {
+            off = 0;
+            valid = 0;
+            scale = 0.f;
+            const int jj = jb * kNT + gw * 16 + lane;
+            if (lane < 16 && jb < nblk && jj < p.k) {
+                const int s = irow[jj];
+                if (s >= 0) {
+                    const int lp = s / p.page_kv;
+                    const int pg = lp < p.max_pages ? p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp] : -1;
+                    if (pg >= 0 && pg < p.num_pages) {
+                        off = pg * p.vps + (s % p.page_kv) * p.vts;
+                        scale = *reinterpret_cast<const float*>(p.scs + pg * p.sps + (s % p.page_kv) * p.sts);
+                        valid = 1;
+                    } else if (p.status) {
+                        atomicOr(p.status, DSA_DEV_BAD_INDEX);
+                    }
+                }
+            }
+        };
+        int64_t off_n;
+        int valid_n;
+        float scale_n;
+        resolve(0, off_n, valid_n, scale_n);
+        for (int j = 0; j < nblk && !__any_sync(0xffffffffu, *s_abort); ++j) {
             const int st = j & 1;
-            if (!mbar_wait(smem_u32(&lat_empty[st]), ((j >> 1) & 1) ^ 1)) {
+            const int64_t off_c = off_n;
+            const int valid_c = valid_n;
+            const float scale_c = scale_n;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_empty[st]), ((j >> 1) & 1) ^ 1))) {
                 *s_abort = 1;
                 break;
             }
             uint8_t* tile = sLat + st * (kMaxChunks * kLChunkBytes);
-            // three phases, each issuing all of this thread's independent loads
-            // back to back: selected indices, then block-table entries, then the
-            // latent segments (one memory latency each instead of one chain per item)
-            int tok[kGatherItems], pg[kGatherItems];
-#pragma unroll
-            for (int i = 0; i < kGatherItems; ++i) {
-                const int w = ct + 128 * i;
-                const int jj = j * kNT + w / nseg;
-                tok[i] = (w < kNT * nseg && jj < p.k) ? irow[jj] : -1;
-            }
-#pragma unroll
-            for (int i = 0; i < kGatherItems; ++i) {
-                pg[i] = -1;
-                if (tok[i] >= 0) {
-                    const int lp = tok[i] / p.page_kv;
-                    if (lp < p.max_pages)
-                        pg[i] = p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp];
-                    if (pg[i] < 0 || pg[i] >= p.num_pages) {
-                        if ((ct + 128 * i) % nseg == 0 && p.status)
-                            atomicOr(p.status, DSA_DEV_BAD_INDEX);
-                        tok[i] = -1;
-                    }
-                }
-            }
+            // all of this lane's 16-byte segments of the block, issued back to back
             uint4 raw[kGatherItems];
 #pragma unroll
             for (int i = 0; i < kGatherItems; ++i) {
+                const int flat = i * 32 + lane;
+                const int tl = flat / nseg, seg = flat % nseg;
+                const int64_t o = __shfl_sync(0xffffffffu, off_c, tl & 15);
+                const int v = __shfl_sync(0xffffffffu, valid_c, tl & 15);
                 raw[i] = make_uint4(0, 0, 0, 0);
-                if (tok[i] >= 0) {
-                    const int seg = (ct + 128 * i) % nseg;
-                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + pg[i] * p.vps + (tok[i] % p.page_kv) * p.vts +
-                                                             (c_lo * 64 + seg * 16));
-                }
+                if (flat < 16 * nseg && v)
+                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + o + (c_lo * 64 + seg * 16));
             }
+            // the next block's index -> page -> scale chain runs while those loads fly
+            resolve(j + 1, off_n, valid_n, scale_n);
 #pragma unroll
             for (int i = 0; i < kGatherItems; ++i) {
-                const int w = ct + 128 * i;
-                if (w >= kNT * nseg)
+                const int flat = i * 32 + lane;
+                if (flat >= 16 * nseg)
                     continue;
-                const int t = w / nseg, seg = w % nseg;
-                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                if (tok[i] >= 0)
-                    e4m3x16_to_f16x16(raw[i], lo, hi);
+                const int tl = flat / nseg, seg = flat % nseg;
+                uint4 lo, hi;
+                e4m3x16_to_f16x16(raw[i], lo, hi);       // zero bytes (unused slot) -> zeros
                 uint8_t* chunk = tile + (seg >> 2) * kLChunkBytes;
                 const int un = (seg & 3) * 2;
-                *reinterpret_cast<uint4*>(chunk + swizzled_offset(t, un, 128)) = lo;
-                *reinterpret_cast<uint4*>(chunk + swizzled_offset(t, un + 1, 128)) = hi;
-                if (seg == 0) {
-                    float sc = 0.f;
-                    if (tok[i] >= 0)
-                        sc = *reinterpret_cast<const float*>(p.scs + pg[i] * p.sps + (tok[i] % p.page_kv) * p.sts);
-                    sScale[st * kNT + t] = sc;
-                    sValid[st * kNT + t] = tok[i] >= 0;
-                }
+                *reinterpret_cast<uint4*>(chunk + swizzled_offset(gw * 16 + tl, un, 128)) = lo;
+                *reinterpret_cast<uint4*>(chunk + swizzled_offset(gw * 16 + tl, un + 1, 128)) = hi;
+            }
+            if (lane < 16) {
+                sScale[st * kNT + gw * 16 + lane] = scale_c;
+                sValid[st * kNT + gw * 16 + lane] = valid_c;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -408,10 +414,12 @@ sparse_mla_tc_kernel(const MlaParams p)
                 break;
             }
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const uint32_t* src = u < 8 ? &ra[4 * u] : &rb[4 * (u - 8)];
-                st_cluster_v4(peer_x_row + ((u ^ (h & 7)) << 4), src[0], src[1], src[2], src[3]);
-            }
+            for (int u = 0; u < 8; ++u)
+                st_cluster_v4(peer_x_row + ((u ^ (h & 7)) << 4), ra[4 * u], ra[4 * u + 1], ra[4 * u + 2], ra[4 * u + 3]);
+#pragma unroll
+            for (int u = 8; u < 16; ++u)
+                st_cluster_v4(peer_x_row + ((u ^ (h & 7)) << 4), rb[4 * u - 32], rb[4 * u - 31], rb[4 * u - 30],
+                              rb[4 * u - 29]);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_remote(peer_x_full);
@@ -423,7 +431,10 @@ sparse_mla_tc_kernel(const MlaParams p)
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const float4 x = *reinterpret_cast<const float4*>(sX + h * (kNT * 4) + ((u ^ (h & 7)) << 4));
-                const uint32_t* own = u < 8 ? &ra[4 * u] : &rb[4 * (u - 8)];
+                uint32_t own[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    own[q] = u < 8 ? ra[4 * u + q] : rb[4 * (u - 8) + q];
                 // both CTAs form partial(CTA 0) + partial(CTA 1) in the same order
                 if (crank == 0) {
                     sco[4 * u + 0] = __uint_as_float(own[0]) + x.x;
