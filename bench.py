@@ -15,7 +15,10 @@ paged MQA logits + top-k (3 libdsa launches).  Reported:
 * roofline     the logits kernel: algorithmic bytes per launch / its event time
                vs the measured HBM copy bandwidth;
 * full_step    the whole graph-captured step of the full decode workload
-               (indexer + top-k + sparse MLA, 128 heads 576/512) in us/step;
+               (indexer + top-k + sparse MLA, 128 heads 576/512) in us/step,
+               with each stage also timed alone and the sparse MLA's tensor
+               roofline; full_step_indexer_h64 is the same step with the decode
+               indexer shape (64 heads x 128) in place of 4 heads x 32;
 * cpu_baseline the fp64 oracle on the host cores over a bounded sample.
 
 ``--impl reference`` times the oracle itself (the only reference available
@@ -254,6 +257,7 @@ def run_ours(args, rank, world, local):
                     "frac": round(achieved / hbm, 4), "peak_source": src,
                     "algorithmic_bytes": lg_bytes, "traffic": load_traffic(kname, args.workload)}
         full = None if args.skip_full_step else measure_full_step(dev, args)
+        full64 = None if args.skip_full_step else measure_full_step(dev, args, "full_step_h64")
         result = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -271,6 +275,7 @@ def run_ours(args, rank, world, local):
             "clocks": clocks,
             "e2e": e2e,
             "full_step": full,
+            "full_step_indexer_h64": full64,
         }
         if not args.skip_cpu:
             result["cpu_baseline"] = cpu_baseline(case, pairs)
@@ -323,13 +328,14 @@ def measure_e2e(st, case, args, pairs, dev):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
-def measure_full_step(dev, args):
-    """Full decode step of the full-step workload (indexer 4 heads x 32, page 64,
-    lens U[8192,131072], top-k 2048, sparse MLA 128 heads 576/512 on an FP8
-    latent) captured in one CUDA graph; us/step over replays, L2 flushed."""
+def measure_full_step(dev, args, workload="full_step"):
+    """Full decode step (indexer, top-k, sparse MLA 128 heads 576/512 on an FP8
+    latent, lens U[8192,131072], top-k 2048) captured in one CUDA graph; us/step
+    over replays, L2 flushed.  Also times each stage alone (eager launches,
+    events on the launching stream)."""
     from deepseek_sparse_attention_mqa_gb300 import inputs
     from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
-    case = inputs.make_case("full_step", device=dev)
+    case = inputs.make_case(workload, device=dev)
     st = SparseAttentionStep(case, with_mla=True)
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
@@ -355,11 +361,37 @@ def measure_full_step(dev, args):
         e1.synchronize()
         if i >= 3:
             times.append(e0.elapsed_time(e1) * 1e3)
+    # per-stage device time, eager (one chunk: decode rows fit the logits budget)
+    stage = {"indexer": [], "topk": [], "mla": []}
+    (rb, re), = [(a, b) for a, b in st.chunks if b > a]
+    for i in range(n):
+        flush.fill_(float(i))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        st.indexer_chunk(rb, re)
+        ev[1].record(stream)
+        st.topk_chunk(rb, re)
+        ev[2].record(stream)
+        st.mla()
+        ev[3].record(stream)
+        ev[3].synchronize()
+        stage["indexer"].append(ev[0].elapsed_time(ev[1]) * 1e3)
+        stage["topk"].append(ev[1].elapsed_time(ev[2]) * 1e3)
+        stage["mla"].append(ev[2].elapsed_time(ev[3]) * 1e3)
     status = st.device_status()
-    return {"workload": "full sparse-attention decode step: batch 64, indexer 4 heads x 32 FP8 page 64, "
-                        "lens U[8192,131072], top-k 2048, sparse MLA 128 heads q/k 576 v 512 FP8 latent",
+    # sparse MLA tensor work: QK^T over d_qk and PV over d_v for every (row, head, selected token)
+    mla_us = statistics.median(stage["mla"])
+    mla_flops = 2.0 * case.rows * case.mla_heads * case.topk * (case.d_qk + case.d_v)
+    _, bf16, _, src = measured_peaks()
+    return {"workload": "full sparse-attention decode step: batch 64, indexer %d heads x %d FP8 page 64, "
+                        "lens U[8192,131072], top-k 2048, sparse MLA 128 heads q/k 576 v 512 FP8 latent"
+                        % (case.num_heads, case.head_dim),
             "us_per_step_median": round(statistics.median(times), 2),
             "us_per_step_mean": round(statistics.mean(times), 2), "replays": n,
+            "stage_us_median": {k: round(statistics.median(v), 2) for k, v in stage.items()},
+            "mla_roofline": {"bound": "tensor", "achieved": round(mla_flops / (mla_us * 1e-6) / 1e12, 1),
+                             "peak": bf16, "unit": "TFLOP/s", "frac": round(mla_flops / (mla_us * 1e-6) / 1e12 / bf16, 4),
+                             "peak_source": src + " bf16 burst (f16 operands run at the bf16 rate)"},
             "launches_per_step": st.launches_per_step(), "device_status": status}
 
 

@@ -7,24 +7,28 @@
 // straddles two non-contiguous pages (BLOCK_KV = min(PAGE_KV, 64)), several
 // TMA warps each owning a KV group, 2-3 stages to fit SM120's 99 KiB.
 //
-// GB300 design (one persistent CTA per SM, warp-specialised):
-//   warps 0,10-12  TMA producers, taking tiles round-robin: per 128-token tile,
-//               one 3-D box per physical page (2 boxes at page 64, 4 at page 32)
-//               into a 128B/64B/32B-swizzled K-major stage, plus one box of
-//               per-token fp32 scales per page; warp 0 also loads the unit's q
-//               rows ([rows x heads, D], K-major) once per unit.  A single
-//               producer warp spends about twice the HBM time of a tile on the
-//               copies' issue and the page bookkeeping, so several share it.
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer, kind::f8f6f4:
-//               D[128 tokens x N] += K_tile[128 x D] * Q[N x D]^T, N = rows x heads.
-//               Each TMEM lane is one token and each column one (row, head).
-//   warps 2-9   epilogue, two warpgroups taking alternate tiles (so two warps per
-//               scheduler hide each other's TMEM-load and barrier latency):
-//               tcgen05.ld of the thread's own lane, then the whole relu /
-//               head-weighting / k_scale reduction is thread-local (no shuffles),
-//               and each warp stores 32 consecutive logits per row.
-//   Four TMEM accumulators let the epilogues of earlier tiles overlap the MMA of
-//   later ones; the stage ring keeps enough K bytes in flight to cover HBM latency.
+// GB300 design (one persistent CTA per SM, warp-specialised).  Every role walks
+// the CTA's 128-token tiles in order; tile j (CTA-local ordinal) lives in stage
+// j % stages and accumulator j % n_acc.  Each role is split over several warps
+// that take tiles round-robin, because on this part a single thread's chain of
+// barrier waits, copy or MMA issues and commits per tile costs more than the
+// tile's HBM time:
+//   warps 0-3   TMA producers (tile j -> warp j % 4): per tile, one 3-D box per
+//               physical page (2 at page 64, 4 at page 32, one lane each) into a
+//               128B/64B/32B-swizzled K-major stage, and the per-token fp32
+//               scales with one 16-byte cp.async per lane; warp 0 also loads
+//               each unit's q rows ([rows x heads, D], K-major).
+//   warps 4-5   single-thread tcgen05.mma issuers (tile j -> warp j % 2),
+//               kind::f8f6f4: D[128 tokens x N] += K_tile[128 x D] * Q[N x D]^T,
+//               N = rows x heads; each TMEM lane is one token and each column
+//               one (row, head).  Warp 4 also owns the TMEM allocation.
+//   warps 6-    epilogue, 2 warpgroups (4 when heads <= 8, whose tiles carry
+//               little arithmetic per barrier round trip), tile j -> group
+//               j % groups: tcgen05.ld of the thread's own lane, then the relu /
+//               head-weighting / k_scale reduction is thread-local (no
+//               shuffles), and each warp stores 32 consecutive logits per row.
+//   Up to eight TMEM accumulators let the epilogues of earlier tiles overlap the
+//   MMAs of later ones; the stage ring keeps K bytes in flight.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,17 +43,29 @@ namespace dsa {
 namespace {
 
 constexpr int kMaxStages = 16;
-constexpr int kEpiWarps = 8;
-constexpr int kProd = 4;        // TMA producer warps (warp 0 and the warps after the epilogue)
-constexpr int kThreads = 32 * (2 + kEpiWarps + kProd - 1);  // producers, MMA, two epilogue warpgroups
-constexpr int kPageCache = 512; // physical page ids cached by each producer warp
-constexpr int kMaxAcc = 4;      // TMEM accumulators in flight
+constexpr int kProd = 4;                  // TMA producer warps: 0 .. kProd-1
+constexpr int kMma = 2;                   // MMA issuer warps: kProd .. kProd+kMma-1
+constexpr int kEpiWarp0 = kProd + kMma;   // first epilogue warp
+constexpr int kPageCache = 128;           // physical page ids cached by each producer warp
+constexpr int kMaxAcc = 8;                // TMEM accumulators in flight
+constexpr int kMaxR = 8;                  // 128-token tiles per super-tile
+constexpr uint32_t kMaxStageKBytes = 32768;
+
+// Epilogue warpgroups and block size per head count.
+template <int H>
+struct Fp8Roles {
+    static constexpr int kGroups = H <= 8 ? 4 : 2;
+    static constexpr int kEpiWarps = 4 * kGroups;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+};
 
 struct LogitsParams {
     const int32_t* sched;
     const int32_t* context_lens;
     const int32_t* block_table;
     int64_t bt_stride;
+    const uint8_t* scales;      // fp32 per token, page stride sc_page_stride bytes
+    int64_t sc_page_stride;
     int max_pages;
     int num_pages;
     int page_kv;
@@ -63,16 +79,19 @@ struct LogitsParams {
     int64_t logits_stride;
     int logits_width;
     int32_t* status;
-    int stages;
+    int R;              // 128-token tiles per super-tile (1, 2, 4 or 8)
+    int stages;         // super-tile stages (multiple of kProd, kMma and n_grp)
     int n_cols;         // MMA N (multiple of 16)
-    uint32_t acc_cols;  // TMEM columns per accumulator (power of two >= 32, >= n_cols)
-    int n_acc;          // accumulators (n_acc * acc_cols <= 512, power of two total)
+    int w_cols;         // n_cols rounded up to the 32-column epilogue chunk
+    uint32_t acc_cols;  // TMEM columns per 128-token block (power of two >= 32, >= n_cols)
+    int n_acc;          // super-tile accumulators (n_acc * R * acc_cols <= 512)
+    int n_grp;          // active epilogue warpgroups (divides n_acc)
     uint32_t q_buf_bytes;
 };
 
 template <int D>
 struct Fp8Tile {
-    static constexpr uint32_t kTileBytes = kTileTokens * D;   // K bytes per stage
+    static constexpr uint32_t kBlockBytes = kTileTokens * D;   // K bytes of one 128-token block
     static constexpr uint32_t kLayout = D == 128 ? kLayoutSw128 : (D == 64 ? kLayoutSw64 : kLayoutSw32);
     static constexpr uint32_t kSbo = 8 * D;                    // 8 rows per swizzle atom
     static constexpr int kKSteps = D / 32;                      // K = 32 bytes per MMA
@@ -83,30 +102,69 @@ struct SmemMap {
     uint32_t k_off, q_off, sc_off, w_off, pc_off, bar_off, misc_off, total;
 };
 
-__host__ __device__ __forceinline__ SmemMap smem_map(int D, int stages, uint32_t q_buf_bytes)
+__host__ __device__ __forceinline__ SmemMap smem_map(int D, int R, int stages, uint32_t q_buf_bytes, int w_cols,
+                                                     int epi_warps)
 {
     SmemMap m;
     m.k_off = 0;
-    m.q_off = m.k_off + stages * kTileTokens * D;
+    m.q_off = m.k_off + stages * R * kTileTokens * D;
     m.sc_off = m.q_off + 2 * q_buf_bytes;
-    m.w_off = m.sc_off + stages * kTileTokens * 4;
-    m.pc_off = m.w_off + kEpiWarps * kMaxUnitCols * 4;       // one weight copy per epilogue warp
+    m.w_off = m.sc_off + stages * R * kTileTokens * 4;
+    m.pc_off = m.w_off + epi_warps * w_cols * 4;             // one weight copy per epilogue warp
     m.bar_off = m.pc_off + kProd * kPageCache * 4;
-    m.misc_off = m.bar_off + (2 * kMaxStages + 2 * kMaxAcc + 4 + 1) * 8;
+    m.misc_off = m.bar_off + (2 * kMaxStages + 2 * kMaxAcc + 4 + kMma) * 8;
     m.total = m.misc_off + 16;
     return m;
 }
 
+// Walks this CTA's super-tiles.  A super-tile is up to R consecutive 128-token
+// tiles of ONE unit, aligned to the unit's first tile; it belongs to the CTA
+// whose tile range [t0, t1) holds its first tile (it may run past t1).  Every
+// role walks the same sequence, so the super-tile ordinal j is the same in all.
+struct SuperWalk {
+    TileWalk w;
+    int R, t1, ts, nt;   // current super-tile: tiles [ts, ts + nt) of unit w.u
+
+    __device__ __forceinline__ void settle()
+    {
+        if (ts >= w.ui.tile_end)
+            ts = w.ui.tile_end;              // the next unit's first tile
+        w.seek(ts);
+        nt = min(R, w.ui.tile_end - ts);
+    }
+    __device__ __forceinline__ void start(const WalkParams& wp, const SchedUnit* units, int total, int t0,
+                                          int t1_, int R_)
+    {
+        R = R_;
+        t1 = t1_;
+        w.start(wp, units, total, t0);
+        const int off = max(0, t0 - w.ui.tile_begin);
+        ts = w.ui.tile_begin + ((off + R - 1) / R) * R;
+        settle();
+    }
+    __device__ __forceinline__ bool valid() const { return ts < t1 && nt > 0; }
+    __device__ __forceinline__ void next()
+    {
+        ts += R;
+        settle();
+    }
+    // first tile of the super-tile inside its unit
+    __device__ __forceinline__ int tile_in_unit() const { return ts - w.ui.tile_begin; }
+};
+
 template <int D, int H>
-__global__ void __launch_bounds__(kThreads, 1)
-logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_s,
-                  const __grid_constant__ CUtensorMap tm_q, const LogitsParams p)
+__global__ void __launch_bounds__(Fp8Roles<H>::kThreads, 1)
+logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                  const LogitsParams p)
 {
     using T = Fp8Tile<D>;
+    constexpr int kEpiWarps = Fp8Roles<H>::kEpiWarps;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemMap mp = smem_map(D, p.stages, p.q_buf_bytes);
+    const SmemMap mp = smem_map(D, p.R, p.stages, p.q_buf_bytes, p.w_cols, kEpiWarps);
+    const uint32_t stage_bytes = static_cast<uint32_t>(p.R) * T::kBlockBytes;
+    const int stage_tokens = p.R * kTileTokens;
     uint8_t* sK = smem + mp.k_off;
     uint8_t* sQ = smem + mp.q_off;
     float* sS = reinterpret_cast<float*>(smem + mp.sc_off);
@@ -119,7 +177,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint64_t* acce_bar = accf_bar + kMaxAcc;         // [kMaxAcc]
     uint64_t* qf_bar = acce_bar + kMaxAcc;           // [2]
     uint64_t* qe_bar = qf_bar + 2;                   // [2]
-    uint64_t* done_bar = qe_bar + 2;                 // [1]
+    uint64_t* done_bar = qe_bar + 2;                 // [kMma]
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc_off);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc_off + 4);
 
@@ -143,7 +201,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1 + 4);   // MMA commit + the tile's 4 epilogue warps
+            mbar_init(smem_u32(&empty_bar[s]), 1 + 4);   // MMA commit + the super-tile's 4 epilogue warps
         }
         for (int a = 0; a < kMaxAcc; ++a) {
             mbar_init(smem_u32(&accf_bar[a]), 1);
@@ -151,62 +209,59 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&qf_bar[a]), 1);
-            mbar_init(smem_u32(&qe_bar[a]), 1);
+            mbar_init(smem_u32(&qe_bar[a]), kMma);        // every MMA warp has finished with the unit
         }
-        mbar_init(smem_u32(done_bar), 1);
+        for (int a = 0; a < kMma; ++a)
+            mbar_init(smem_u32(&done_bar[a]), 1);
         *s_abort = 0;
         fence_barrier_init();
         tma_prefetch_map(&tm_k);
-        tma_prefetch_map(&tm_s);
         tma_prefetch_map(&tm_q);
     }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), p.n_acc * p.acc_cols);
+    if (warp == kProd) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), p.n_acc * p.R * p.acc_cols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *s_tmem;
+    const uint32_t acc_stride = static_cast<uint32_t>(p.R) * p.acc_cols;   // TMEM columns per super-tile
     const WalkParams wp{p.context_lens, p.next_n, p.num_units};
     const int P = p.page_kv;
     const int pages_per_tile = kTileTokens / P;
 
-    if (warp == 0 || warp >= 2 + kEpiWarps) {
+    if (warp < kProd) {
         // =========================== TMA producers ==========================
-        // kProd warps share the tile stream: producer pi issues the tiles whose
-        // CTA-local ordinal j has j % kProd == pi, so the per-tile work around
-        // the copies (page lookup, barrier waits, descriptor fetch) of several
-        // tiles overlaps.  The stage count is a multiple of kProd, so every
-        // stage has exactly one producer and its empty/full phases advance in
-        // that producer's order.  Producer 0 also loads each unit's q rows.
-        // Physical page ids are fetched by all 32 lanes at once into the warp's
-        // own shared-memory cache (one global-memory latency per refill).
-        const int pi = warp == 0 ? 0 : warp - (1 + kEpiWarps);
+        // Producer pi issues the super-tiles whose CTA-local ordinal j has
+        // j % kProd == pi.  The stage count is a multiple of kProd, so every
+        // stage has exactly one producer and its phases advance in that
+        // producer's order.  Physical page ids are fetched by all 32 lanes at
+        // once into the warp's own shared-memory cache.
+        const int pi = warp;
         int* my_pages = s_pages + pi * kPageCache;
-        TileWalk w;
-        w.start(wp, units, total_tiles, t0);
-        int ucount = 0;
+        SuperWalk w;
+        w.start(wp, units, total_tiles, t0, t1, p.R);
+        int ucount = 0, unit = -1;
         long long issued = 0;
         int pc_unit = -1, pc_lp0 = 0, pc_cnt = 0;
-        for (int t = t0; t < t1; ++t) {
+        for (int j = 0; w.valid(); ++j, w.next()) {
             if (__any_sync(0xffffffffu, *s_abort))
                 break;
-            const bool changed = w.seek(t) || (t == t0);
             int ok = 1;
-            if (changed) {
+            if (w.w.u != unit) {
+                unit = w.w.u;
                 if (pi == 0 && lane == 0) {
                     const int qb = ucount & 1;
                     ok = mbar_wait(smem_u32(&qe_bar[qb]), ((ucount >> 1) & 1) ^ 1);
                     if (ok) {
                         mbar_arrive_expect_tx(smem_u32(&qf_bar[qb]), static_cast<uint32_t>(p.n_cols) * D);
                         tma_load_2d(smem_u32(sQ + qb * p.q_buf_bytes), &tm_q, smem_u32(&qf_bar[qb]), 0,
-                                    w.ui.first_row * H);
+                                    w.w.ui.first_row * H);
                     }
                 }
                 ++ucount;
             }
-            const int j = t - t0;
             if (j % kProd != pi) {
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     if (lane == 0)
@@ -217,66 +272,74 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
             const int stage = j % p.stages;
             const uint32_t phase = static_cast<uint32_t>((j / p.stages) & 1);
-            const int tt = t - w.ui.tile_begin;              // tile index inside the unit
-            const int lp_first = tt * pages_per_tile;
-            if (w.u != pc_unit || lp_first + pages_per_tile > pc_lp0 + pc_cnt) {
+            const UnitInfo& ui = w.w.ui;
+            const int lp_first = w.tile_in_unit() * pages_per_tile;
+            const int npages = w.nt * pages_per_tile;
+            if (w.w.u != pc_unit || lp_first + npages > pc_lp0 + pc_cnt) {
                 // refill: this unit's pages from lp_first up to what this CTA will use
-                const int tiles_here = min(t1, w.ui.tile_end) - w.ui.tile_begin;
-                const int lp_vis = (w.ui.vis_max + P - 1) / P;
+                const int tiles_here = min(t1 + p.R - 1, ui.tile_end) - ui.tile_begin;
+                const int lp_vis = (ui.vis_max + P - 1) / P;
                 const int lp_end = min(tiles_here * pages_per_tile, lp_vis);
-                const int cnt = min(kPageCache, max(lp_end - lp_first, pages_per_tile));
+                const int cnt = min(kPageCache, max(lp_end - lp_first, npages));
                 __syncwarp();
                 for (int i = lane; i < cnt; i += 32) {
                     const int lp = lp_first + i;
                     int pg = -1;
                     if (lp < lp_vis && lp < p.max_pages)
-                        pg = p.block_table[static_cast<int64_t>(w.ui.seq) * p.bt_stride + lp];
+                        pg = p.block_table[static_cast<int64_t>(ui.seq) * p.bt_stride + lp];
                     my_pages[i] = pg;
                 }
                 __syncwarp();
-                pc_unit = w.u;
+                pc_unit = w.w.u;
                 pc_lp0 = lp_first;
                 pc_cnt = cnt;
             }
-            if (lane == 0 && ok) {
+            if (lane == 0 && ok)
                 ok = mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1);
-                if (ok) {
-                    int phys[kTileTokens / 32];
-                    uint32_t bytes = 0;
-                    for (int jp = 0; jp < pages_per_tile; ++jp) {
-                        const int lp = lp_first + jp;
-                        phys[jp] = -1;
-                        if (lp * P < w.ui.vis_max) {
-                            const int pg = my_pages[lp - pc_lp0];
-                            if (pg >= 0 && pg < p.num_pages) {
-                                phys[jp] = pg;
-                                bytes += static_cast<uint32_t>(P) * (D + 4);
-                            } else if (p.status) {
-                                atomicOr(p.status, DSA_DEV_BAD_PAGE);
-                            }
-                        }
-                    }
-                    const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    for (int jp = 0; jp < pages_per_tile; ++jp) {
-                        if (phys[jp] < 0)
-                            continue;
-                        tma_load_3d(smem_u32(sK + stage * T::kTileBytes + jp * P * D), &tm_k, fb, 0, 0, phys[jp]);
-                        tma_load_2d(smem_u32(sS + stage * kTileTokens + jp * P), &tm_s, fb, 0, phys[jp]);
-                    }
-                }
-            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0)
                     *s_abort = 1;
                 break;
             }
+            // The whole warp issues the super-tile: per 128-token block, lane l
+            // copies the fp32 scales of tokens [4l, 4l + 4) with one 16-byte
+            // cp.async (tracked by the full barrier through
+            // cp.async.mbarrier.arrive), and lane jp < pages issues the TMA box
+            // of page jp.  The cp.async arrivals are registered before the
+            // producer's own arrive, and the expected TMA bytes before any box
+            // is issued, so the phase cannot complete early.
+            const uint32_t fb = smem_u32(&full_bar[stage]);
+            auto page_of = [&](int jp) -> int {
+                const int lp = lp_first + jp;
+                if (lp * P >= ui.vis_max)
+                    return -1;                             // past the visible length: not loaded
+                const int pg = my_pages[lp - pc_lp0];
+                return (pg >= 0 && pg < p.num_pages) ? pg : -2;
+            };
+            for (int m = 0; m < w.nt; ++m) {
+                const int tok0 = m * kTileTokens + lane * 4;
+                const int pg = page_of(tok0 / P);
+                if (pg >= 0)
+                    cp_async_16(smem_u32(sS + stage * stage_tokens + tok0),
+                                p.scales + static_cast<int64_t>(pg) * p.sc_page_stride + (tok0 % P) * 4);
+            }
+            cp_async_mbar_arrive(fb);
+            const int pg_k = lane < npages ? page_of(lane) : -1;
+            if (pg_k == -2 && p.status)
+                atomicOr(p.status, DSA_DEV_BAD_PAGE);
+            const uint32_t kmask = __ballot_sync(0xffffffffu, pg_k >= 0);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(__popc(kmask)) * static_cast<uint32_t>(P) * D);
+            __syncwarp();
+            if (pg_k >= 0)
+                tma_load_3d(smem_u32(sK + stage * stage_bytes + lane * P * D), &tm_k, fb, 0, 0, pg_k);
             ++issued;
         }
         // drain: every copy this warp issued has landed before the CTA exits
-        // (its stages are its own, so the last stages/kProd of its tiles are
-        // the only ones whose full phase may still be pending)
+        // (its stages are its own, so the last stages/kProd of its super-tiles
+        // are the only ones whose full phase may still be pending)
         if (lane == 0) {
             const long long per = p.stages / kProd;
             const long long lo = issued > per ? issued - per : 0;
@@ -288,45 +351,59 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 for (int u = ucount > 2 ? ucount - 2 : 0; u < ucount; ++u)
                     mbar_wait(smem_u32(&qf_bar[u & 1]), static_cast<uint32_t>((u >> 1) & 1));
         }
-    } else if (warp == 1) {
-        // =========================== MMA issuer =============================
+    } else if (warp < kEpiWarp0) {
+        // =========================== MMA issuers ============================
+        // Warp mi issues the super-tiles with j % kMma == mi: per 128-token
+        // block m, D[acc + m * acc_cols] = K_block_m Q^T over D / 32 k-steps.
+        // Every MMA warp walks all super-tiles to follow the unit changes: each
+        // waits for the unit's q rows and commits the unit's q buffer release
+        // (qe counts kMma commits), so the buffer is reloaded only after the
+        // MMAs of all of them have read it.  stages and n_acc are multiples of
+        // kMma, so a stage or an accumulator is only ever used by one warp.
+        const int mi = warp - kProd;
         if (lane == 0) {
             const uint32_t idesc = make_idesc(0, 0, 0, 128, static_cast<uint32_t>(p.n_cols));
-            TileWalk w;
-            w.start(wp, units, total_tiles, t0);
+            SuperWalk w;
+            w.start(wp, units, total_tiles, t0, t1, p.R);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            int ucount = 0, qb = 0;
-            for (int t = t0; t < t1 && !*s_abort; ++t) {
-                const bool changed = w.seek(t) || (t == t0);
-                if (changed) {
+            int ucount = 0, qb = 0, unit = -1;
+            bool ok = true;
+            for (int j = 0; w.valid() && !*s_abort; ++j) {
+                if (w.w.u != unit) {
+                    unit = w.w.u;
                     qb = ucount & 1;
                     if (!mbar_wait(smem_u32(&qf_bar[qb]), (ucount >> 1) & 1)) {
-                        *s_abort = 1;
+                        ok = false;
                         break;
                     }
                     ++ucount;
                 }
-                if (!mbar_wait(smem_u32(&acce_bar[acc]), acc_phase ^ 1) ||
-                    !mbar_wait(smem_u32(&full_bar[stage]), phase)) {
-                    *s_abort = 1;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols;
-                const uint32_t a_base = smem_u32(sK + stage * T::kTileBytes);
-                const uint32_t b_base = smem_u32(sQ + qb * p.q_buf_bytes);
+                if (j % kMma == mi) {
+                    if (!mbar_wait(smem_u32(&acce_bar[acc]), acc_phase ^ 1) ||
+                        !mbar_wait(smem_u32(&full_bar[stage]), phase)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc) * acc_stride;
+                    const uint32_t a0 = smem_u32(sK + stage * stage_bytes);
+                    const uint32_t b_base = smem_u32(sQ + qb * p.q_buf_bytes);
+                    for (int m = 0; m < w.nt; ++m) {
 #pragma unroll
-                for (int k = 0; k < T::kKSteps; ++k) {
-                    const uint64_t ad = make_smem_desc(a_base + k * 32, 16, T::kSbo, T::kLayout);
-                    const uint64_t bd = make_smem_desc(b_base + k * 32, 16, T::kSbo, T::kLayout);
-                    umma_f8f6f4(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < T::kKSteps; ++k) {
+                            const uint64_t ad = make_smem_desc(a0 + m * T::kBlockBytes + k * 32, 16, T::kSbo, T::kLayout);
+                            const uint64_t bd = make_smem_desc(b_base + k * 32, 16, T::kSbo, T::kLayout);
+                            umma_f8f6f4(d0 + m * p.acc_cols, ad, bd, idesc, k > 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(smem_u32(&empty_bar[stage]));
+                    umma_commit(smem_u32(&accf_bar[acc]));
                 }
-                umma_commit(smem_u32(&empty_bar[stage]));
-                umma_commit(smem_u32(&accf_bar[acc]));
-                const bool unit_ends = (t + 1 == t1) || (t + 1 >= w.ui.tile_end);
-                if (unit_ends)
-                    umma_commit(smem_u32(&qe_bar[qb]));
+                const int u_now = w.w.u;
+                w.next();
+                if (!w.valid() || w.w.u != u_now)
+                    umma_commit(smem_u32(&qe_bar[qb]));    // last super-tile of this unit here
                 if (++stage == p.stages) {
                     stage = 0;
                     phase ^= 1;
@@ -336,38 +413,42 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     acc_phase ^= 1;
                 }
             }
+            if (!ok)
+                *s_abort = 1;
             // every MMA issued by this thread has completed before TMEM is released
-            umma_commit(smem_u32(done_bar));
-            mbar_wait(smem_u32(done_bar), 0);
+            umma_commit(smem_u32(&done_bar[mi]));
+            mbar_wait(smem_u32(&done_bar[mi]), 0);
         }
     } else {
         // =========================== epilogue ===============================
+        const int ew = warp - kEpiWarp0;
         const int quarter = warp & 3;                 // TMEM lanes this warp may access
-        const int group = (warp - 2) >> 2;            // epilogue warpgroup: takes tiles t0+group, t0+group+2, ...
-        const int tok = quarter * 32 + lane;          // token of this thread within the tile
-        float* wS = sW + (warp - 2) * kMaxUnitCols;   // this warp's copy of the unit weights
-        TileWalk w;
-        w.start(wp, units, total_tiles, t0);
+        const int group = ew >> 2;                    // takes the super-tiles with j % n_grp == group
+        const int tok = quarter * 32 + lane;          // token of this thread within each 128-token block
+        float* wS = sW + ew * p.w_cols;               // this warp's copy of the unit weights
+        SuperWalk w;
+        w.start(wp, units, total_tiles, t0, t1, p.R);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
-        int nchunks = 0, L = 0, i0 = 0;
-        for (int t = t0; t < t1 && !__any_sync(0xffffffffu, *s_abort); ++t) {
-            const bool changed = w.seek(t) || (t == t0);
-            if (changed) {
+        int nchunks = 0, L = 0, i0 = 0, unit = -1;
+        for (int j = 0; w.valid() && group < p.n_grp && !__any_sync(0xffffffffu, *s_abort); ++j, w.next()) {
+            const UnitInfo& ui = w.w.ui;
+            if (w.w.u != unit) {
+                unit = w.w.u;
                 __syncwarp();
-                const int ncols_valid = w.ui.nrows * H;
+                const int ncols_valid = ui.nrows * H;
                 nchunks = (ncols_valid + 31) / 32;
-                const float* wsrc = p.weights + static_cast<int64_t>(w.ui.first_row) * H;
-                for (int c = lane; c < kMaxUnitCols; c += 32)
+                const float* wsrc = p.weights + static_cast<int64_t>(ui.first_row) * H;
+                for (int c = lane; c < p.w_cols; c += 32)
                     wS[c] = c < ncols_valid ? wsrc[c] : 0.f;
                 __syncwarp();
-                L = max(0, p.context_lens[w.ui.seq]);
-                i0 = w.ui.first_row - w.ui.seq * p.next_n;
-                if (lane == 0 && group == 0 && p.status &&
-                    visible_len(L, p.next_n, i0 + w.ui.nrows - 1) > p.logits_width)
+                L = max(0, p.context_lens[ui.seq]);
+                i0 = ui.first_row - ui.seq * p.next_n;
+                if (lane == 0 && ew == 0 && p.status &&
+                    visible_len(L, p.next_n, i0 + ui.nrows - 1) > p.logits_width)
                     atomicOr(p.status, DSA_DEV_WIDTH);
             }
-            if (((t - t0) & 1) != group) {            // the other warpgroup's tile
+            if (j % p.n_grp != group) {               // another warpgroup's super-tile
                 if (++stage == p.stages) {
                     stage = 0;
                     phase ^= 1;
@@ -385,81 +466,99 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 break;
             }
             tc_fence_after_sync();
-            const float kscale = sS[stage * kTileTokens + tok];
+            const int nt = w.nt;
+            float kscale[kMaxR];
+#pragma unroll
+            for (int m = 0; m < kMaxR; ++m)
+                kscale[m] = m < nt ? sS[stage * stage_tokens + m * kTileTokens + tok] : 0.f;
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&empty_bar[stage]));
 
-            const int s = (t - w.ui.tile_begin) * kTileTokens + tok;
-            const uint32_t t_acc = tmem_base + static_cast<uint32_t>(acc) * p.acc_cols +
-                                   (static_cast<uint32_t>(quarter * 32) << 16);
-            // store one finished logit of unit row i
-            auto emit = [&](int i, float v) {
-                if (i < w.ui.nrows) {
-                    const int vis = min(visible_len(L, p.next_n, i0 + i), p.logits_width);
-                    if (s < vis)
-                        p.logits[static_cast<int64_t>(w.ui.first_row + i - p.row_begin) * p.logits_stride + s] =
-                            kscale * v;
-                }
-            };
-            float cur = 0.f;                           // running row sum (H >= 32)
-            auto process = [&](const uint32_t (&r)[32], int c) {
-                const float4* w4 = reinterpret_cast<const float4*>(wS + c * 32);
-                if constexpr (H >= 32) {
-                    // one row per chunk: 8 independent partial sums
-                    float part[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        part[j] = 0.f;
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        const float4 wv = w4[q4];
-                        part[(4 * q4 + 0) & 7] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), part[(4 * q4 + 0) & 7]);
-                        part[(4 * q4 + 1) & 7] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), part[(4 * q4 + 1) & 7]);
-                        part[(4 * q4 + 2) & 7] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), part[(4 * q4 + 2) & 7]);
-                        part[(4 * q4 + 3) & 7] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), part[(4 * q4 + 3) & 7]);
+            const int s_base = w.tile_in_unit() * kTileTokens + tok;
+            const uint32_t acc_base = tmem_base + static_cast<uint32_t>(acc) * acc_stride +
+                                      (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+            for (int m = 0; m < nt; ++m) {
+                const int s = s_base + m * kTileTokens;
+                const float ks = kscale[m];
+                const uint32_t t_acc = acc_base + m * p.acc_cols;
+                // store one finished logit of unit row i
+                auto emit = [&](int i, float v) {
+                    if (i < ui.nrows) {
+                        const int vis = min(visible_len(L, p.next_n, i0 + i), p.logits_width);
+                        if (s < vis)
+                            p.logits[static_cast<int64_t>(ui.first_row + i - p.row_begin) * p.logits_stride + s] =
+                                ks * v;
                     }
-                    cur += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-                    if (((c + 1) * 32) % H == 0) {
-                        emit((c * 32) / H, cur);
-                        cur = 0.f;
+                };
+                float cur = 0.f;                       // running row sum (H >= 32)
+                auto process = [&](const uint32_t (&r)[32], int c) {
+                    const float4* w4 = reinterpret_cast<const float4*>(wS + c * 32);
+                    if constexpr (H >= 32) {
+                        // one row per chunk: 8 independent partial sums
+                        float part[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            part[q] = 0.f;
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            const float4 wv = w4[q4];
+                            part[(4 * q4 + 0) & 7] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), part[(4 * q4 + 0) & 7]);
+                            part[(4 * q4 + 1) & 7] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), part[(4 * q4 + 1) & 7]);
+                            part[(4 * q4 + 2) & 7] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), part[(4 * q4 + 2) & 7]);
+                            part[(4 * q4 + 3) & 7] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), part[(4 * q4 + 3) & 7]);
+                        }
+                        cur += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                        if (((c + 1) * 32) % H == 0) {
+                            emit((c * 32) / H, cur);
+                            cur = 0.f;
+                        }
+                    } else {
+                        // 32 / H rows per chunk, each summed over its H columns
+                        constexpr int kRowsPerChunk = 32 / H;
+                        float rs[kRowsPerChunk];
+#pragma unroll
+                        for (int i = 0; i < kRowsPerChunk; ++i)
+                            rs[i] = 0.f;
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            const float4 wv = w4[q4];
+                            rs[(4 * q4 + 0) / H] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), rs[(4 * q4 + 0) / H]);
+                            rs[(4 * q4 + 1) / H] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), rs[(4 * q4 + 1) / H]);
+                            rs[(4 * q4 + 2) / H] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), rs[(4 * q4 + 2) / H]);
+                            rs[(4 * q4 + 3) / H] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), rs[(4 * q4 + 3) / H]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < kRowsPerChunk; ++i)
+                            emit(c * kRowsPerChunk + i, rs[i]);
                     }
-                } else {
-                    // 32 / H rows per chunk, each summed over its H columns
-                    constexpr int kRowsPerChunk = 32 / H;
-                    float rs[kRowsPerChunk];
-#pragma unroll
-                    for (int i = 0; i < kRowsPerChunk; ++i)
-                        rs[i] = 0.f;
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        const float4 wv = w4[q4];
-                        rs[(4 * q4 + 0) / H] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), rs[(4 * q4 + 0) / H]);
-                        rs[(4 * q4 + 1) / H] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), rs[(4 * q4 + 1) / H]);
-                        rs[(4 * q4 + 2) / H] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), rs[(4 * q4 + 2) / H]);
-                        rs[(4 * q4 + 3) / H] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), rs[(4 * q4 + 3) / H]);
+                };
+                // two 32-column TMEM loads in flight per round, or one where the
+                // block is larger (heads <= 8: four epilogue warpgroups, fewer
+                // registers per thread)
+                constexpr int kPerRound = Fp8Roles<H>::kGroups == 2 ? 2 : 1;
+                for (int c = 0; c < nchunks; c += kPerRound) {
+                    uint32_t r[kPerRound][32];
+                    tmem_ld_32x32b_x32(t_acc + c * 32, r[0]);
+                    if constexpr (kPerRound == 2) {
+                        if (c + 1 < nchunks)
+                            tmem_ld_32x32b_x32(t_acc + (c + 1) * 32, r[kPerRound - 1]);
                     }
-#pragma unroll
-                    for (int i = 0; i < kRowsPerChunk; ++i)
-                        emit(c * kRowsPerChunk + i, rs[i]);
+                    tmem_ld_wait();
+                    if (m + 1 == nt && c + kPerRound >= nchunks) {
+                        // last TMEM reads of this accumulator are in registers: release it early
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(smem_u32(&acce_bar[acc]));
+                    }
+                    process(r[0], c);
+                    if constexpr (kPerRound == 2) {
+                        if (c + 1 < nchunks)
+                            process(r[kPerRound - 1], c + 1);
+                    }
                 }
-            };
-            for (int c = 0; c < nchunks; c += 2) {
-                uint32_t ra[32], rb[32];
-                tmem_ld_32x32b_x32(t_acc + c * 32, ra);
-                if (c + 1 < nchunks)
-                    tmem_ld_32x32b_x32(t_acc + (c + 1) * 32, rb);
-                tmem_ld_wait();
-                if (c + 2 >= nchunks) {
-                    // last TMEM reads of this accumulator are in registers: release it early
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_u32(&acce_bar[acc]));
-                }
-                process(ra, c);
-                if (c + 1 < nchunks)
-                    process(rb, c + 1);
             }
             if (nchunks == 0) {
                 tc_fence_before_sync();
@@ -484,8 +583,19 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (warp == 1)
-        tmem_dealloc(tmem_base, p.n_acc * p.acc_cols);
+    if (warp == kProd)
+        tmem_dealloc(tmem_base, p.n_acc * p.R * p.acc_cols);
+}
+
+constexpr int lcm2(int a, int b)
+{
+    int x = a, y = b;
+    while (y) {
+        const int t = x % y;
+        x = y;
+        y = t;
+    }
+    return a / x * b;
 }
 
 template <int D, int H>
@@ -499,10 +609,11 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     while (acc_cols < static_cast<uint32_t>(n_cols))
         acc_cols <<= 1;
     const uint32_t q_buf_bytes = ((static_cast<uint32_t>(n_cols) * D + 1023u) / 1024u) * 1024u;
+    const int w_cols = ((n_cols + 31) / 32) * 32;
 
-    // tensor maps: K values [num_pages][P][D] bytes, scales [num_pages][P] fp32,
-    // q [rows_total*H][D] bytes
-    CUtensorMap tm_k, tm_s, tm_q;
+    // tensor maps: K values [num_pages][P][D] bytes, q [rows_total*H][D] bytes
+    // (the fp32 token scales are copied with cp.async)
+    CUtensorMap tm_k, tm_q;
     const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                            : (D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     {
@@ -516,15 +627,6 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
             return st;
     }
     {
-        const uint64_t dims[2] = {static_cast<uint64_t>(P), static_cast<uint64_t>(k->num_pages)};
-        const uint64_t strides[1] = {static_cast<uint64_t>(k->sc_page_stride)};
-        const uint32_t box[2] = {static_cast<uint32_t>(P), 1};
-        dsa_status st = encode_tiled(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, k->scales, dims, strides, box,
-                                     CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (st != DSA_OK)
-            return st;
-    }
-    {
         const uint64_t rows_total = static_cast<uint64_t>(a.batch) * a.next_n * H;
         const uint64_t dims[2] = {static_cast<uint64_t>(D), rows_total};
         const uint64_t strides[1] = {static_cast<uint64_t>(D)};
@@ -534,14 +636,24 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
             return st;
     }
 
-    // as many stages as fit next to the q buffers
+    // Super-tile size: as many 128-token tiles as keep a stage within 32 KB of K
+    // and two super-tile accumulators within the 512 TMEM columns (at most 8).
+    int R = kMaxR;
+    while (R > 1 && (static_cast<uint32_t>(R) * kTileTokens * D > kMaxStageKBytes || R * acc_cols > 256u))
+        R >>= 1;
+    const int n_acc = static_cast<int>(std::min<uint32_t>(kMaxAcc, 512u / (static_cast<uint32_t>(R) * acc_cols)));
+    const int n_grp = std::min(Fp8Roles<H>::kGroups, n_acc);
+    // As many stages as fit next to the q buffers, a multiple of the producer,
+    // MMA-warp and epilogue-group counts (each stage then has one owner of each
+    // kind, so no barrier is waited on by a role that lags a full phase behind).
+    const int step = lcm2(lcm2(kProd, kMma), n_grp);
     const int budget = std::min(dev.max_smem_optin, 227 * 1024) - 1024;
-    // (a multiple of the producer count: each producer owns every kProd-th stage)
-    int stages = kMaxStages;
-    while (stages > kProd && static_cast<int>(smem_map(D, stages, q_buf_bytes).total) > budget)
-        stages -= kProd;
-    const SmemMap mp = smem_map(D, stages, q_buf_bytes);
-    if (static_cast<int>(mp.total) > budget)
+    constexpr int kEpiWarps = Fp8Roles<H>::kEpiWarps;
+    int stages = (kMaxStages / step) * step;
+    while (stages > step && static_cast<int>(smem_map(D, R, stages, q_buf_bytes, w_cols, kEpiWarps).total) > budget)
+        stages -= step;
+    const SmemMap mp = smem_map(D, R, stages, q_buf_bytes, w_cols, kEpiWarps);
+    if (static_cast<int>(mp.total) > budget || n_acc % lcm2(kMma, n_grp) != 0)
         return DSA_ERR_UNSUPPORTED;
     const int smem_bytes = static_cast<int>(mp.total) + 1024;
 
@@ -550,6 +662,8 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     p.context_lens = a.context_lens;
     p.block_table = k->block_table;
     p.bt_stride = k->bt_row_stride;
+    p.scales = static_cast<const uint8_t*>(k->scales);
+    p.sc_page_stride = k->sc_page_stride;
     p.max_pages = k->max_pages_per_seq;
     p.num_pages = k->num_pages;
     p.page_kv = P;
@@ -563,17 +677,20 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     p.logits_stride = a.logits_row_stride;
     p.logits_width = a.logits_width;
     p.status = a.status;
+    p.R = R;
     p.stages = stages;
     p.n_cols = n_cols;
+    p.w_cols = w_cols;
     p.acc_cols = acc_cols;
-    p.n_acc = static_cast<int>(std::min<uint32_t>(kMaxAcc, 512u / acc_cols));
+    p.n_acc = n_acc;
+    p.n_grp = n_grp;
     p.q_buf_bytes = q_buf_bytes;
 
     auto kern = logits_fp8_kernel<D, H>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    kern<<<dev.sm_count, kThreads, smem_bytes, stream>>>(tm_k, tm_s, tm_q, p);
+    kern<<<dev.sm_count, Fp8Roles<H>::kThreads, smem_bytes, stream>>>(tm_k, tm_q, p);
     return check_launch();
 }
 

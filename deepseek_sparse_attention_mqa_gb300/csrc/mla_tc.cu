@@ -320,11 +320,13 @@ sparse_mla_tc_kernel(const MlaParams p)
             const uint32_t idesc_qk = make_idesc(0, 0, 0, 128, kNT);     // f16 x f16 -> f32
             const uint32_t idesc_pv = make_idesc(0, 0, 1, 128, 256);
             bool ok = mbar_wait(smem_u32(q_full), 0);
-            auto issue_qk = [&](int j) -> bool {
+            // Two independent streams share this thread: S(j) = Q K_j^T once block j
+            // is gathered (and the S buffer is free), and O += P_j V_j once the
+            // softmax has written P_j.  Whichever is ready is issued, so a PV never
+            // waits behind the gather of a later block (which itself waits for
+            // that PV to free its latent buffer).
+            auto issue_qk = [&](int j) {
                 const int st = j & 1;
-                if (!mbar_wait(smem_u32(&lat_full[st]), (j >> 1) & 1) ||
-                    !mbar_wait(smem_u32(&s_empty[st]), ((j >> 1) & 1) ^ 1))
-                    return false;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(st * kNT);
                 const uint32_t qa = smem_u32(sQ);
@@ -338,19 +340,8 @@ sparse_mla_tc_kernel(const MlaParams p)
                     }
                 }
                 umma_commit(smem_u32(&s_full[st]));
-                return true;
             };
-            if (ok && nblk > 0)
-                ok = issue_qk(0);
-            for (int j = 0; j < nblk && ok && !*s_abort; ++j) {
-                if (j + 1 < nblk && !issue_qk(j + 1)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(smem_u32(p_full), j & 1)) {
-                    ok = false;
-                    break;
-                }
+            auto issue_pv = [&](int j) {
                 tc_fence_after_sync();
                 // O[:, v] += P[:, t] V[t, v]: A = P (K-major over tokens), B = V read
                 // MN-major from the latent tile (64-dim blocks 8 KB apart = LBO,
@@ -366,6 +357,32 @@ sparse_mla_tc_kernel(const MlaParams p)
                 }
                 umma_commit(smem_u32(p_empty));
                 umma_commit(smem_u32(&lat_empty[j & 1]));
+            };
+            int jq = 0, jp = 0;                         // next QK / PV block to issue
+            uint64_t t_idle = 0;
+            while (ok && jp < nblk && !*s_abort) {
+                bool progress = false;
+                // QK(jq): its latent block is gathered and S buffer jq & 1 was read
+                if (jq < nblk && mbar_test_wait(smem_u32(&lat_full[jq & 1]), (jq >> 1) & 1) &&
+                    mbar_test_wait(smem_u32(&s_empty[jq & 1]), ((jq >> 1) & 1) ^ 1)) {
+                    issue_qk(jq++);
+                    progress = true;
+                }
+                // PV(jp): P_jp is written (S(jp) was issued before, so jp < jq)
+                if (jp < jq && mbar_test_wait(smem_u32(p_full), jp & 1)) {
+                    issue_pv(jp++);
+                    progress = true;
+                }
+                if (progress) {
+                    t_idle = 0;
+                    continue;
+                }
+                __nanosleep(20);                        // leave issue slots to the warps sharing this SMSP
+                if (t_idle == 0) {
+                    t_idle = global_timer_ns();
+                } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+                    ok = false;
+                }
             }
             if (!ok)
                 *s_abort = 1;

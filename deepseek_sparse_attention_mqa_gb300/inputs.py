@@ -19,6 +19,7 @@ pages) and the five named workloads:
 * ``prefill``    one causal sequence of 16384 tokens, H 64, D 128, page 64, top-k 2048
 * ``full_step``  batch 64, next_n 1, H 4, D 32, page 64, lens U[8192, 131072], top-k 2048,
                  MLA 128 heads over an FP8 latent (q/k 576, v 512), scale 1/sqrt(192)
+* ``full_step_h64``  the same with the decode indexer shape, H 64, D 128
 
 Draw order (one ``torch.Generator`` seeded with ``seed``): context lengths,
 physical page permutation, K values, K scales, q, weights, then the MLA latent
@@ -113,6 +114,13 @@ CONFIGS = {
                       mla=dict(heads=128, d_qk=576, d_v=512, fmt=FMT_FP8,
                                scale=1.0 / math.sqrt(192)),
                       seed=4),
+    # the same step with the decode workload's indexer shape (64 heads x 128)
+    "full_step_h64": dict(batch=64, next_n=1, num_heads=64, head_dim=128, page_kv=64, fmt=FMT_FP8,
+                          lens=("uniform", 8192, 131072), pool_factor=1, w_div=8.0,
+                          topk=2048, width=131072,
+                          mla=dict(heads=128, d_qk=576, d_v=512, fmt=FMT_FP8,
+                                   scale=1.0 / math.sqrt(192)),
+                          seed=4),
 }
 
 # Lengths forced onto the first sequences of the log-uniform workload: empty
