@@ -47,6 +47,26 @@ __device__ __forceinline__ int find_unit(const SchedUnit* units, int num_units, 
     return lo;
 }
 
+// find_unit by one whole warp: each round probes 32 evenly spaced units at
+// once (one global-memory latency per round instead of one per halving), so a
+// CTA finds its first unit in two rounds for up to 1024 units.  All 32 lanes
+// must call it; every lane returns the same unit.
+__device__ __forceinline__ int find_unit_warp(const SchedUnit* units, int num_units, int t)
+{
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = num_units;                  // answer in [lo, hi); units[lo].tile_begin <= t
+    while (hi - lo > 1) {
+        const int span = hi - lo;
+        const int idx = lo + static_cast<int>((static_cast<long long>(span) * lane) / 32);
+        const unsigned le = __ballot_sync(0xffffffffu, units[idx].tile_begin <= t);
+        const int k = 31 - __clz(le);            // last probe at or before t (lane 0 always is)
+        const int nlo = lo + static_cast<int>((static_cast<long long>(span) * k) / 32);
+        hi = k == 31 ? hi : lo + static_cast<int>((static_cast<long long>(span) * (k + 1)) / 32);
+        lo = nlo;
+    }
+    return lo;
+}
+
 // Walks this CTA's tiles [t0, t1) unit by unit; identical in every role.
 struct TileWalk {
     const WalkParams* p;
@@ -56,10 +76,15 @@ struct TileWalk {
     UnitInfo ui;
     __device__ __forceinline__ void start(const WalkParams& pp, const SchedUnit* us, int total, int t0)
     {
+        start_at(pp, us, total, t0, find_unit(us, pp.num_units, t0));
+    }
+    // start from a unit found beforehand (find_unit / find_unit_warp of t0)
+    __device__ __forceinline__ void start_at(const WalkParams& pp, const SchedUnit* us, int total, int t0, int u0)
+    {
         p = &pp;
         units = us;
         total_tiles = total;
-        u = find_unit(us, pp.num_units, t0);
+        u = u0;
         ui = load_unit(pp, us, total, u);
         while (t0 >= ui.tile_end && u + 1 < pp.num_units) {
             ++u;

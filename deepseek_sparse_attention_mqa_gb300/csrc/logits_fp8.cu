@@ -80,7 +80,7 @@ struct LogitsParams {
     int logits_width;
     int32_t* status;
     int R;              // 128-token tiles per super-tile (1, 2, 4 or 8)
-    int stages;         // super-tile stages (multiple of kProd, kMma and n_grp)
+    int stages;         // super-tile stages (multiple of kMma and n_grp)
     int n_cols;         // MMA N (multiple of 16)
     int w_cols;         // n_cols rounded up to the 32-column epilogue chunk
     uint32_t acc_cols;  // TMEM columns per 128-token block (power of two >= 32, >= n_cols)
@@ -133,11 +133,11 @@ struct SuperWalk {
         nt = min(R, w.ui.tile_end - ts);
     }
     __device__ __forceinline__ void start(const WalkParams& wp, const SchedUnit* units, int total, int t0,
-                                          int t1_, int R_)
+                                          int t1_, int R_, int u0)
     {
         R = R_;
         t1 = t1_;
-        w.start(wp, units, total, t0);
+        w.start_at(wp, units, total, t0, u0);
         const int off = max(0, t0 - w.ui.tile_begin);
         ts = w.ui.tile_begin + ((off + R - 1) / R) * R;
         settle();
@@ -180,6 +180,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint64_t* done_bar = qe_bar + 2;                 // [kMma]
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc_off);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc_off + 4);
+    volatile int* s_u0 = reinterpret_cast<volatile int*>(smem + mp.misc_off + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -200,7 +201,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&full_bar[s]), kProd);     // one arrive (with its TMA bytes) per producer warp
             mbar_init(smem_u32(&empty_bar[s]), 1 + 4);   // MMA commit + the super-tile's 4 epilogue warps
         }
         for (int a = 0; a < kMaxAcc; ++a) {
@@ -222,10 +223,16 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), p.n_acc * p.R * p.acc_cols);
         tmem_relinquish();
     }
+    if (warp == kProd + 1) {
+        const int u0 = find_unit_warp(units, p.num_units, t0);
+        if (lane == 0)
+            *s_u0 = u0;
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *s_tmem;
+    const int u0 = *s_u0;                            // the unit of tile t0
     const uint32_t acc_stride = static_cast<uint32_t>(p.R) * p.acc_cols;   // TMEM columns per super-tile
     const WalkParams wp{p.context_lens, p.next_n, p.num_units};
     const int P = p.page_kv;
@@ -233,22 +240,28 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     if (warp < kProd) {
         // =========================== TMA producers ==========================
-        // Producer pi issues the super-tiles whose CTA-local ordinal j has
-        // j % kProd == pi.  The stage count is a multiple of kProd, so every
-        // stage has exactly one producer and its phases advance in that
-        // producer's order.  Physical page ids are fetched by all 32 lanes at
-        // once into the warp's own shared-memory cache.
+        // All kProd producer warps issue every super-tile together: warp pi
+        // copies the pages jp with jp % kProd == pi (one lane per page, one TMA
+        // box each) and the token scales of the 128-token blocks m with
+        // m % kProd == pi, so the serial issue latency of the boxes is split
+        // kProd ways.  Each warp arrives once on the stage's full barrier
+        // (count kProd) with the bytes of its own boxes.  Physical page ids are
+        // fetched by all 32 lanes at once into the warp's own shared-memory
+        // cache.
         const int pi = warp;
         int* my_pages = s_pages + pi * kPageCache;
         SuperWalk w;
-        w.start(wp, units, total_tiles, t0, t1, p.R);
+        w.start(wp, units, total_tiles, t0, t1, p.R, u0);
         int ucount = 0, unit = -1;
         long long issued = 0;
         int pc_unit = -1, pc_lp0 = 0, pc_cnt = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         for (int j = 0; w.valid(); ++j, w.next()) {
             if (__any_sync(0xffffffffu, *s_abort))
                 break;
             int ok = 1;
+            const UnitInfo& ui = w.w.ui;
             if (w.w.u != unit) {
                 unit = w.w.u;
                 if (pi == 0 && lane == 0) {
@@ -257,22 +270,11 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     if (ok) {
                         mbar_arrive_expect_tx(smem_u32(&qf_bar[qb]), static_cast<uint32_t>(p.n_cols) * D);
                         tma_load_2d(smem_u32(sQ + qb * p.q_buf_bytes), &tm_q, smem_u32(&qf_bar[qb]), 0,
-                                    w.w.ui.first_row * H);
+                                    ui.first_row * H);
                     }
                 }
                 ++ucount;
             }
-            if (j % kProd != pi) {
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    if (lane == 0)
-                        *s_abort = 1;
-                    break;
-                }
-                continue;
-            }
-            const int stage = j % p.stages;
-            const uint32_t phase = static_cast<uint32_t>((j / p.stages) & 1);
-            const UnitInfo& ui = w.w.ui;
             const int lp_first = w.tile_in_unit() * pages_per_tile;
             const int npages = w.nt * pages_per_tile;
             if (w.w.u != pc_unit || lp_first + npages > pc_lp0 + pc_cnt) {
@@ -302,13 +304,13 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                     *s_abort = 1;
                 break;
             }
-            // The whole warp issues the super-tile: per 128-token block, lane l
-            // copies the fp32 scales of tokens [4l, 4l + 4) with one 16-byte
-            // cp.async (tracked by the full barrier through
-            // cp.async.mbarrier.arrive), and lane jp < pages issues the TMA box
-            // of page jp.  The cp.async arrivals are registered before the
-            // producer's own arrive, and the expected TMA bytes before any box
-            // is issued, so the phase cannot complete early.
+            // This warp's share: per owned 128-token block m, lane l copies the
+            // fp32 scales of tokens [4l, 4l + 4) with one 16-byte cp.async
+            // (tracked by the full barrier through cp.async.mbarrier.arrive),
+            // and lane i issues the TMA box of page pi + i * kProd.  The
+            // cp.async arrivals are registered before the warp's own arrive, and
+            // the expected TMA bytes before any box is issued, so the phase
+            // cannot complete early.
             const uint32_t fb = smem_u32(&full_bar[stage]);
             auto page_of = [&](int jp) -> int {
                 const int lp = lp_first + jp;
@@ -317,7 +319,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int pg = my_pages[lp - pc_lp0];
                 return (pg >= 0 && pg < p.num_pages) ? pg : -2;
             };
-            for (int m = 0; m < w.nt; ++m) {
+            for (int m = pi; m < w.nt; m += kProd) {
                 const int tok0 = m * kTileTokens + lane * 4;
                 const int pg = page_of(tok0 / P);
                 if (pg >= 0)
@@ -325,7 +327,8 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                                 p.scales + static_cast<int64_t>(pg) * p.sc_page_stride + (tok0 % P) * 4);
             }
             cp_async_mbar_arrive(fb);
-            const int pg_k = lane < npages ? page_of(lane) : -1;
+            const int jp = pi + lane * kProd;
+            const int pg_k = jp < npages ? page_of(jp) : -1;
             if (pg_k == -2 && p.status)
                 atomicOr(p.status, DSA_DEV_BAD_PAGE);
             const uint32_t kmask = __ballot_sync(0xffffffffu, pg_k >= 0);
@@ -334,19 +337,20 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 mbar_arrive_expect_tx(fb, static_cast<uint32_t>(__popc(kmask)) * static_cast<uint32_t>(P) * D);
             __syncwarp();
             if (pg_k >= 0)
-                tma_load_3d(smem_u32(sK + stage * stage_bytes + lane * P * D), &tm_k, fb, 0, 0, pg_k);
+                tma_load_3d(smem_u32(sK + stage * stage_bytes + jp * P * D), &tm_k, fb, 0, 0, pg_k);
             ++issued;
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1;
+            }
         }
         // drain: every copy this warp issued has landed before the CTA exits
-        // (its stages are its own, so the last stages/kProd of its super-tiles
-        // are the only ones whose full phase may still be pending)
+        // (a stage is reissued only after its previous contents were consumed,
+        // so only the last `stages` super-tiles may still be in flight)
         if (lane == 0) {
-            const long long per = p.stages / kProd;
-            const long long lo = issued > per ? issued - per : 0;
-            for (long long n = lo; n < issued; ++n) {
-                const long long jj = pi + n * kProd;
+            const long long lo = issued > p.stages ? issued - p.stages : 0;
+            for (long long jj = lo; jj < issued; ++jj)
                 mbar_wait(smem_u32(&full_bar[jj % p.stages]), static_cast<uint32_t>((jj / p.stages) & 1));
-            }
             if (pi == 0)
                 for (int u = ucount > 2 ? ucount - 2 : 0; u < ucount; ++u)
                     mbar_wait(smem_u32(&qf_bar[u & 1]), static_cast<uint32_t>((u >> 1) & 1));
@@ -364,7 +368,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         if (lane == 0) {
             const uint32_t idesc = make_idesc(0, 0, 0, 128, static_cast<uint32_t>(p.n_cols));
             SuperWalk w;
-            w.start(wp, units, total_tiles, t0, t1, p.R);
+            w.start(wp, units, total_tiles, t0, t1, p.R, u0);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             int ucount = 0, qb = 0, unit = -1;
@@ -427,7 +431,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int tok = quarter * 32 + lane;          // token of this thread within each 128-token block
         float* wS = sW + ew * p.w_cols;               // this warp's copy of the unit weights
         SuperWalk w;
-        w.start(wp, units, total_tiles, t0, t1, p.R);
+        w.start(wp, units, total_tiles, t0, t1, p.R, u0);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         int nchunks = 0, L = 0, i0 = 0, unit = -1;
@@ -459,13 +463,12 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 }
                 continue;
             }
-            // warp-uniform outcome: the TMEM loads below are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase) &&
-                                             mbar_wait(smem_u32(&accf_bar[acc]), acc_phase))) {
+            // the token scales are read as soon as the stage has landed, and the
+            // stage released, before the MMAs are waited for
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase))) {
                 *s_abort = 1;
                 break;
             }
-            tc_fence_after_sync();
             const int nt = w.nt;
             float kscale[kMaxR];
 #pragma unroll
@@ -474,6 +477,12 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&empty_bar[stage]));
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&accf_bar[acc]), acc_phase))) {
+                *s_abort = 1;
+                break;
+            }
+            tc_fence_after_sync();
 
             const int s_base = w.tile_in_unit() * kTileTokens + tok;
             const uint32_t acc_base = tmem_base + static_cast<uint32_t>(acc) * acc_stride +
@@ -643,10 +652,10 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
         R >>= 1;
     const int n_acc = static_cast<int>(std::min<uint32_t>(kMaxAcc, 512u / (static_cast<uint32_t>(R) * acc_cols)));
     const int n_grp = std::min(Fp8Roles<H>::kGroups, n_acc);
-    // As many stages as fit next to the q buffers, a multiple of the producer,
-    // MMA-warp and epilogue-group counts (each stage then has one owner of each
-    // kind, so no barrier is waited on by a role that lags a full phase behind).
-    const int step = lcm2(lcm2(kProd, kMma), n_grp);
+    // As many stages as fit next to the q buffers, a multiple of the MMA-warp
+    // and epilogue-group counts (each stage then has one owner of each kind, so
+    // no barrier is waited on by a role that lags a full phase behind).
+    const int step = lcm2(kMma, n_grp);
     const int budget = std::min(dev.max_smem_optin, 227 * 1024) - 1024;
     constexpr int kEpiWarps = Fp8Roles<H>::kEpiWarps;
     int stages = (kMaxStages / step) * step;
