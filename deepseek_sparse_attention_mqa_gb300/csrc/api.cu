@@ -230,7 +230,7 @@ dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_f
     // units of at most 128 columns (rows x heads) in the 512 TMEM columns
     if (q_fmt == DSA_KV_MXFP4 && D == 128 && unit_rows(next_n, num_heads) * num_heads > 128)
         return DSA_ERR_UNSUPPORTED;
-    if (!q || !aligned16(q) || !weights || !logits || !sched || !aligned16(sched) ||
+    if (!q || !aligned16(q) || !weights || !aligned16(weights) || !logits || !sched || !aligned16(sched) ||
         (batch > 0 && !context_lens))
         return DSA_ERR_INVALID_ARG;
     if (logits_width < 0 || logits_row_stride < logits_width)

@@ -37,21 +37,29 @@ __host__ __device__ __forceinline__ int unit_rows(int next_n, int num_heads)
 // Layout of the caller-owned schedule buffer (int32 words):
 //   header[0..7]: magic, num_units, rows_per_unit, row_begin, row_end, next_n,
 //                 total_tiles, batch
-//   units[num_units] (16-byte records): first_row (absolute), nrows, seq,
-//                 tile_begin (prefix of 128-token tiles over the units)
-constexpr int32_t kSchedMagic = 0x44534131;  // "DSA1"
+//   units[num_units] (32-byte records): first_row (absolute), nrows, seq,
+//                 tile_begin (prefix of 128-token tiles over the units),
+//                 tile_end, vis_max (largest visible length of the unit's
+//                 rows), ctx_len (the sequence's context length, >= 0), 0.
+//                 A record is everything a kernel needs about its unit, read
+//                 with one 32-byte load and no dependent lookups.
+constexpr int32_t kSchedMagic = 0x44534132;  // "DSA2"
 constexpr int kSchedHeaderWords = 8;
 
-struct SchedUnit {
+struct __align__(16) SchedUnit {
     int32_t first_row;
     int32_t nrows;
     int32_t seq;
     int32_t tile_begin;
+    int32_t tile_end;
+    int32_t vis_max;
+    int32_t ctx_len;
+    int32_t pad;
 };
 
 __host__ __device__ __forceinline__ int64_t sched_bytes_for_units(int64_t num_units)
 {
-    return static_cast<int64_t>(kSchedHeaderWords) * 4 + num_units * 16;
+    return static_cast<int64_t>(kSchedHeaderWords) * 4 + num_units * static_cast<int64_t>(sizeof(SchedUnit));
 }
 
 // Number of units covering rows [row_begin, row_end): per sequence, the rows it

@@ -15,22 +15,42 @@ struct WalkParams {
 };
 
 struct UnitInfo {
-    int seq, first_row, nrows, tile_begin, tile_end, vis_max;
+    int seq, first_row, nrows, tile_begin, tile_end, vis_max, ctx_len;
 };
 
-__device__ __forceinline__ UnitInfo load_unit(const WalkParams& p, const SchedUnit* units,
-                                              int total_tiles, int u)
+// One schedule record (32 bytes, two 16-byte loads).
+__device__ __forceinline__ SchedUnit fetch_unit(const SchedUnit* units, int u)
+{
+    const int4* src = reinterpret_cast<const int4*>(units + u);
+    const int4 a = src[0], b = src[1];
+    SchedUnit su;
+    su.first_row = a.x;
+    su.nrows = a.y;
+    su.seq = a.z;
+    su.tile_begin = a.w;
+    su.tile_end = b.x;
+    su.vis_max = b.y;
+    su.ctx_len = b.z;
+    su.pad = b.w;
+    return su;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(const SchedUnit& su)
 {
     UnitInfo ui;
-    const SchedUnit su = units[u];
     ui.seq = su.seq;
     ui.first_row = su.first_row;
     ui.nrows = su.nrows;
     ui.tile_begin = su.tile_begin;
-    ui.tile_end = (u + 1 < p.num_units) ? units[u + 1].tile_begin : total_tiles;
-    const int L = max(0, p.context_lens[su.seq]);
-    ui.vis_max = visible_len(L, p.next_n, su.first_row + su.nrows - 1 - su.seq * p.next_n);
+    ui.tile_end = su.tile_end;
+    ui.vis_max = su.vis_max;
+    ui.ctx_len = su.ctx_len;
     return ui;
+}
+
+__device__ __forceinline__ UnitInfo load_unit(const WalkParams&, const SchedUnit* units, int, int u)
+{
+    return unit_info(fetch_unit(units, u));
 }
 
 // Last unit whose tile_begin <= t (units with no tiles are skipped naturally).
@@ -67,37 +87,44 @@ __device__ __forceinline__ int find_unit_warp(const SchedUnit* units, int num_un
     return lo;
 }
 
-// Walks this CTA's tiles [t0, t1) unit by unit; identical in every role.
+// Walks this CTA's tiles [t0, t1) unit by unit; identical in every role.  The
+// record of the next unit is fetched as soon as a unit is entered, so a unit
+// change costs no global-memory round trip.
 struct TileWalk {
-    const WalkParams* p;
     const SchedUnit* units;
-    int total_tiles;
+    int num_units;
     int u;
     UnitInfo ui;
+    SchedUnit nx;            // record of unit u + 1 (when it exists)
     __device__ __forceinline__ void start(const WalkParams& pp, const SchedUnit* us, int total, int t0)
     {
         start_at(pp, us, total, t0, find_unit(us, pp.num_units, t0));
     }
     // start from a unit found beforehand (find_unit / find_unit_warp of t0)
-    __device__ __forceinline__ void start_at(const WalkParams& pp, const SchedUnit* us, int total, int t0, int u0)
+    __device__ __forceinline__ void start_at(const WalkParams& pp, const SchedUnit* us, int, int t0, int u0)
     {
-        p = &pp;
         units = us;
-        total_tiles = total;
+        num_units = pp.num_units;
         u = u0;
-        ui = load_unit(pp, us, total, u);
-        while (t0 >= ui.tile_end && u + 1 < pp.num_units) {
-            ++u;
-            ui = load_unit(pp, us, total, u);
-        }
+        ui = unit_info(fetch_unit(us, u));
+        if (u + 1 < num_units)
+            nx = fetch_unit(us, u + 1);
+        while (t0 >= ui.tile_end && u + 1 < num_units)
+            advance();
+    }
+    __device__ __forceinline__ void advance()
+    {
+        ++u;
+        ui = unit_info(nx);
+        if (u + 1 < num_units)
+            nx = fetch_unit(units, u + 1);
     }
     // Advance to the unit that owns tile t; returns true if the unit changed.
     __device__ __forceinline__ bool seek(int t)
     {
         bool changed = false;
-        while (t >= ui.tile_end && u + 1 < p->num_units) {
-            ++u;
-            ui = load_unit(*p, units, total_tiles, u);
+        while (t >= ui.tile_end && u + 1 < num_units) {
+            advance();
             changed = true;
         }
         return changed;

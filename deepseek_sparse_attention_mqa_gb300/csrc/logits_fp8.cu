@@ -22,11 +22,13 @@
 //               kind::f8f6f4: D[128 tokens x N] += K_tile[128 x D] * Q[N x D]^T,
 //               N = rows x heads; each TMEM lane is one token and each column
 //               one (row, head).  Warp 4 also owns the TMEM allocation.
-//   warps 6-    epilogue, 2 warpgroups (4 when heads <= 8, whose tiles carry
-//               little arithmetic per barrier round trip), tile j -> group
-//               j % groups: tcgen05.ld of the thread's own lane, then the relu /
+//   warp 6      q rows + head weights of each unit (TMA / bulk copies into
+//               one of two buffers), running up to one unit ahead.
+//   warps 7-14  epilogue, 2 warpgroups, super-tile j -> group j % 2:
+//               tcgen05.ld of the thread's own lane, then the relu /
 //               head-weighting / k_scale reduction is thread-local (no
-//               shuffles), and each warp stores 32 consecutive logits per row.
+//               shuffles, rows of a unit past its last row skipped), and each
+//               warp stores 32 consecutive logits per row.
 //   Up to eight TMEM accumulators let the epilogues of earlier tiles overlap the
 //   MMAs of later ones; the stage ring keeps K bytes in flight.
 #include <cuda.h>
@@ -45,7 +47,8 @@ namespace {
 constexpr int kMaxStages = 16;
 constexpr int kProd = 4;                  // TMA producer warps: 0 .. kProd-1
 constexpr int kMma = 2;                   // MMA issuer warps: kProd .. kProd+kMma-1
-constexpr int kEpiWarp0 = kProd + kMma;   // first epilogue warp
+constexpr int kQWarp = kProd + kMma;      // q rows + unit weights loader
+constexpr int kEpiWarp0 = kQWarp + 1;     // first epilogue warp
 constexpr int kPageCache = 128;           // physical page ids cached by each producer warp
 constexpr int kMaxAcc = 8;                // TMEM accumulators in flight
 constexpr int kMaxR = 8;                  // 128-token tiles per super-tile
@@ -54,7 +57,7 @@ constexpr uint32_t kMaxStageKBytes = 32768;
 // Epilogue warpgroups and block size per head count.
 template <int H>
 struct Fp8Roles {
-    static constexpr int kGroups = H <= 8 ? 4 : 2;
+    static constexpr int kGroups = 2;
     static constexpr int kEpiWarps = 4 * kGroups;
     static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 };
@@ -99,7 +102,7 @@ struct Fp8Tile {
 
 // Shared memory map (offsets from a 1024-aligned base).
 struct SmemMap {
-    uint32_t k_off, q_off, sc_off, w_off, pc_off, bar_off, misc_off, total;
+    uint32_t k_off, q_off, sc_off, w_off, ks_off, pc_off, bar_off, misc_off, total;
 };
 
 __host__ __device__ __forceinline__ SmemMap smem_map(int D, int R, int stages, uint32_t q_buf_bytes, int w_cols,
@@ -110,7 +113,8 @@ __host__ __device__ __forceinline__ SmemMap smem_map(int D, int R, int stages, u
     m.q_off = m.k_off + stages * R * kTileTokens * D;
     m.sc_off = m.q_off + 2 * q_buf_bytes;
     m.w_off = m.sc_off + stages * R * kTileTokens * 4;
-    m.pc_off = m.w_off + epi_warps * w_cols * 4;             // one weight copy per epilogue warp
+    m.ks_off = m.w_off + 2 * w_cols * 4;                     // unit weights, one slot per q buffer
+    m.pc_off = m.ks_off + epi_warps * R * 32 * 4;            // token scales per epilogue warp
     m.bar_off = m.pc_off + kProd * kPageCache * 4;
     m.misc_off = m.bar_off + (2 * kMaxStages + 2 * kMaxAcc + 4 + kMma) * 8;
     m.total = m.misc_off + 16;
@@ -168,7 +172,8 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     uint8_t* sK = smem + mp.k_off;
     uint8_t* sQ = smem + mp.q_off;
     float* sS = reinterpret_cast<float*>(smem + mp.sc_off);
-    float* sW = reinterpret_cast<float*>(smem + mp.w_off);
+    float* sW = reinterpret_cast<float*>(smem + mp.w_off);       // [2][w_cols] unit weights
+    float* sKs = reinterpret_cast<float*>(smem + mp.ks_off);
     int* s_pages = reinterpret_cast<int*>(smem + mp.pc_off);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + mp.bar_off);
     uint64_t* full_bar = bars;                       // [stages]
@@ -210,7 +215,8 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&qf_bar[a]), 1);
-            mbar_init(smem_u32(&qe_bar[a]), kMma);        // every MMA warp has finished with the unit
+            // every MMA warp and every active epilogue warp has finished with the unit
+            mbar_init(smem_u32(&qe_bar[a]), kMma + 4 * p.n_grp);
         }
         for (int a = 0; a < kMma; ++a)
             mbar_init(smem_u32(&done_bar[a]), 1);
@@ -252,7 +258,6 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         int* my_pages = s_pages + pi * kPageCache;
         SuperWalk w;
         w.start(wp, units, total_tiles, t0, t1, p.R, u0);
-        int ucount = 0, unit = -1;
         long long issued = 0;
         int pc_unit = -1, pc_lp0 = 0, pc_cnt = 0;
         int stage = 0;
@@ -262,19 +267,6 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 break;
             int ok = 1;
             const UnitInfo& ui = w.w.ui;
-            if (w.w.u != unit) {
-                unit = w.w.u;
-                if (pi == 0 && lane == 0) {
-                    const int qb = ucount & 1;
-                    ok = mbar_wait(smem_u32(&qe_bar[qb]), ((ucount >> 1) & 1) ^ 1);
-                    if (ok) {
-                        mbar_arrive_expect_tx(smem_u32(&qf_bar[qb]), static_cast<uint32_t>(p.n_cols) * D);
-                        tma_load_2d(smem_u32(sQ + qb * p.q_buf_bytes), &tm_q, smem_u32(&qf_bar[qb]), 0,
-                                    ui.first_row * H);
-                    }
-                }
-                ++ucount;
-            }
             const int lp_first = w.tile_in_unit() * pages_per_tile;
             const int npages = w.nt * pages_per_tile;
             if (w.w.u != pc_unit || lp_first + npages > pc_lp0 + pc_cnt) {
@@ -351,11 +343,50 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const long long lo = issued > p.stages ? issued - p.stages : 0;
             for (long long jj = lo; jj < issued; ++jj)
                 mbar_wait(smem_u32(&full_bar[jj % p.stages]), static_cast<uint32_t>((jj / p.stages) & 1));
-            if (pi == 0)
-                for (int u = ucount > 2 ? ucount - 2 : 0; u < ucount; ++u)
-                    mbar_wait(smem_u32(&qf_bar[u & 1]), static_cast<uint32_t>((u >> 1) & 1));
         }
-    } else if (warp < kEpiWarp0) {
+    } else if (warp == kQWarp) {
+        // ======================= q rows + unit weights ======================
+        // Runs ahead of the MMA warps by up to one unit: as soon as a q buffer
+        // is released (qe: its unit's MMAs and epilogues are done), the next
+        // unit's q rows ([rows x heads, D]) and head weights ([rows x heads]
+        // fp32, zero-padded to w_cols) are copied into it.
+        SuperWalk w;
+        w.start(wp, units, total_tiles, t0, t1, p.R, u0);
+        int ucount = 0, unit = -1;
+        bool ok = true;
+        for (; w.valid(); w.next()) {
+            if (w.w.u == unit)
+                continue;
+            unit = w.w.u;
+            const UnitInfo& ui = w.w.ui;
+            const int qb = ucount & 1;
+            if (lane == 0)
+                ok = mbar_wait(smem_u32(&qe_bar[qb]), ((ucount >> 1) & 1) ^ 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok || *s_abort)
+                break;
+            const int nw = ui.nrows * H;
+            float* wdst = sW + qb * p.w_cols;
+            for (int c = nw + lane; c < p.w_cols; c += 32)
+                wdst[c] = 0.f;
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t qfb = smem_u32(&qf_bar[qb]);
+                mbar_arrive_expect_tx(qfb, static_cast<uint32_t>(p.n_cols) * D + static_cast<uint32_t>(nw) * 4u);
+                tma_load_2d(smem_u32(sQ + qb * p.q_buf_bytes), &tm_q, qfb, 0, ui.first_row * H);
+                bulk_load(smem_u32(wdst), p.weights + static_cast<int64_t>(ui.first_row) * H,
+                          static_cast<uint32_t>(nw) * 4u, qfb);
+            }
+            ++ucount;
+        }
+        if (lane == 0) {
+            if (!ok)
+                *s_abort = 1;
+            // drain: the last (at most two) copies have landed before the CTA exits
+            for (int u = ucount > 2 ? ucount - 2 : 0; u < ucount; ++u)
+                mbar_wait(smem_u32(&qf_bar[u & 1]), static_cast<uint32_t>((u >> 1) & 1));
+        }
+    } else if (warp < kQWarp) {
         // =========================== MMA issuers ============================
         // Warp mi issues the super-tiles with j % kMma == mi: per 128-token
         // block m, D[acc + m * acc_cols] = K_block_m Q^T over D / 32 k-steps.
@@ -429,51 +460,44 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int quarter = warp & 3;                 // TMEM lanes this warp may access
         const int group = ew >> 2;                    // takes the super-tiles with j % n_grp == group
         const int tok = quarter * 32 + lane;          // token of this thread within each 128-token block
-        float* wS = sW + ew * p.w_cols;               // this warp's copy of the unit weights
+        float* myks = sKs + ew * p.R * 32;            // this warp's token scales of the current super-tile
         SuperWalk w;
         w.start(wp, units, total_tiles, t0, t1, p.R, u0);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
-        int nchunks = 0, L = 0, i0 = 0, unit = -1;
-        for (int j = 0; w.valid() && group < p.n_grp && !__any_sync(0xffffffffu, *s_abort); ++j, w.next()) {
+        int nchunks = 0, L = 0, i0 = 0, unit = -1, ucount = 0, qb = 0;
+        const float* wS = sW;                         // the current unit's head weights
+        for (int j = 0; w.valid() && group < p.n_grp && !__any_sync(0xffffffffu, *s_abort); ++j) {
             const UnitInfo& ui = w.w.ui;
             if (w.w.u != unit) {
                 unit = w.w.u;
-                __syncwarp();
-                const int ncols_valid = ui.nrows * H;
-                nchunks = (ncols_valid + 31) / 32;
-                const float* wsrc = p.weights + static_cast<int64_t>(ui.first_row) * H;
-                for (int c = lane; c < p.w_cols; c += 32)
-                    wS[c] = c < ncols_valid ? wsrc[c] : 0.f;
-                __syncwarp();
-                L = max(0, p.context_lens[ui.seq]);
+                qb = ucount & 1;
+                // the unit's weights arrive with its q rows
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&qf_bar[qb]), (ucount >> 1) & 1))) {
+                    *s_abort = 1;
+                    break;
+                }
+                ++ucount;
+                wS = sW + qb * p.w_cols;
+                nchunks = (ui.nrows * H + 31) / 32;
+                L = ui.ctx_len;
                 i0 = ui.first_row - ui.seq * p.next_n;
                 if (lane == 0 && ew == 0 && p.status &&
                     visible_len(L, p.next_n, i0 + ui.nrows - 1) > p.logits_width)
                     atomicOr(p.status, DSA_DEV_WIDTH);
             }
-            if (j % p.n_grp != group) {               // another warpgroup's super-tile
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-                if (++acc == p.n_acc) {
-                    acc = 0;
-                    acc_phase ^= 1;
-                }
-                continue;
-            }
+            if (j % p.n_grp == group) {
             // the token scales are read as soon as the stage has landed, and the
             // stage released, before the MMAs are waited for
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase))) {
                 *s_abort = 1;
                 break;
             }
+            // this thread's token scales move to the warp's own scratch before the
+            // stage is released
             const int nt = w.nt;
-            float kscale[kMaxR];
-#pragma unroll
-            for (int m = 0; m < kMaxR; ++m)
-                kscale[m] = m < nt ? sS[stage * stage_tokens + m * kTileTokens + tok] : 0.f;
+            for (int m = 0; m < nt; ++m)
+                myks[m * 32 + lane] = sS[stage * stage_tokens + m * kTileTokens + tok];
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&empty_bar[stage]));
@@ -490,7 +514,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll 1
             for (int m = 0; m < nt; ++m) {
                 const int s = s_base + m * kTileTokens;
-                const float ks = kscale[m];
+                const float ks = myks[m * 32 + lane];
                 const uint32_t t_acc = acc_base + m * p.acc_cols;
                 // store one finished logit of unit row i
                 auto emit = [&](int i, float v) {
@@ -524,23 +548,22 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                             cur = 0.f;
                         }
                     } else {
-                        // 32 / H rows per chunk, each summed over its H columns
+                        // 32 / H rows per chunk, each summed over its H columns; rows
+                        // past the unit's last row are skipped (warp-uniform)
                         constexpr int kRowsPerChunk = 32 / H;
-                        float rs[kRowsPerChunk];
+                        const int nv = ui.nrows - c * kRowsPerChunk;
 #pragma unroll
-                        for (int i = 0; i < kRowsPerChunk; ++i)
-                            rs[i] = 0.f;
+                        for (int i = 0; i < kRowsPerChunk; ++i) {
+                            if (i < nv) {
+                                float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
-                            const float4 wv = w4[q4];
-                            rs[(4 * q4 + 0) / H] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), rs[(4 * q4 + 0) / H]);
-                            rs[(4 * q4 + 1) / H] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), rs[(4 * q4 + 1) / H]);
-                            rs[(4 * q4 + 2) / H] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), rs[(4 * q4 + 2) / H]);
-                            rs[(4 * q4 + 3) / H] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), rs[(4 * q4 + 3) / H]);
+                                for (int hh = 0; hh < H; hh += 2) {
+                                    acc0 = fmaf(wS[c * 32 + i * H + hh], fmaxf(__uint_as_float(r[i * H + hh]), 0.f), acc0);
+                                    acc1 = fmaf(wS[c * 32 + i * H + hh + 1], fmaxf(__uint_as_float(r[i * H + hh + 1]), 0.f), acc1);
+                                }
+                                emit(c * kRowsPerChunk + i, acc0 + acc1);
+                            }
                         }
-#pragma unroll
-                        for (int i = 0; i < kRowsPerChunk; ++i)
-                            emit(c * kRowsPerChunk + i, rs[i]);
                     }
                 };
                 // two 32-column TMEM loads in flight per round, or one where the
@@ -575,6 +598,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 if (lane == 0)
                     mbar_arrive(smem_u32(&acce_bar[acc]));
             }
+            }
             if (++stage == p.stages) {
                 stage = 0;
                 phase ^= 1;
@@ -582,6 +606,15 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             if (++acc == p.n_acc) {
                 acc = 0;
                 acc_phase ^= 1;
+            }
+            // past the unit's last super-tile here: this warp is done with its
+            // q buffer and weights
+            const int u_now = w.w.u;
+            w.next();
+            if (!w.valid() || w.w.u != u_now) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&qe_bar[qb]));
             }
         }
     }

@@ -23,8 +23,8 @@
 namespace dsa {
 namespace {
 
-// 256 KiB: 32 header bytes + 16 bytes per work unit -> up to 16382 units
-// (e.g. a decode batch of 16382 sequences, or a prefill chunk of 65528 rows at
+// 256 KiB: 32 header bytes + 32 bytes per work unit -> up to 8191 units
+// (e.g. a decode batch of 8191 sequences, or a prefill chunk of 32764 rows at
 // 64 heads).
 constexpr size_t kNoallocSchedBytes = 256 * 1024;
 

@@ -124,6 +124,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 1-D bulk copy global -> shared by the TMA unit, counted on the mbarrier's
+// transaction bytes; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 16-byte global -> shared copy through the load/store path (no register
 // staging); both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src)

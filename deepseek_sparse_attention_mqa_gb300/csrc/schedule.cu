@@ -62,13 +62,14 @@ build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int n
 
     for (int base = 0; base < num_units; base += kSchedThreads) {
         const int u = base + tid;
-        int seq = 0, first_row = 0, nrows = 0, tiles = 0;
+        int seq = 0, first_row = 0, nrows = 0, tiles = 0, vis = 0, ctx = 0;
         if (u < num_units) {
             unit_rows_of(u, next_n, G, row_begin, row_end, &seq, &first_row, &nrows);
             if (seq < batch && nrows > 0) {
                 const int L = context_lens[seq];
+                ctx = L < 0 ? 0 : L;
                 const int last_i = first_row + nrows - 1 - seq * next_n;
-                const int vis = visible_len(L < 0 ? 0 : L, next_n, last_i);
+                vis = visible_len(ctx, next_n, last_i);
                 tiles = (vis + kTileTokens - 1) / kTileTokens;
             } else if (status) {
                 atomicOr(status, DSA_DEV_SCHEDULE);
@@ -104,6 +105,10 @@ build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int n
             su.nrows = nrows;
             su.seq = seq;
             su.tile_begin = excl;
+            su.tile_end = excl + tiles;
+            su.vis_max = vis;
+            su.ctx_len = ctx;
+            su.pad = 0;
             units[u] = su;
         }
         __syncthreads();

@@ -17,7 +17,8 @@
 //  3. every position above that bin is written out directly (cluster-wide
 //     counter); the bin's few elements are appended to CTA 0 as candidates;
 //  4. CTA 0 resolves the candidates exactly by the 64-bit order (key, then lower
-//     position), the same order as a full sort with ties broken by position.
+//     position), the same order as a full sort with ties broken by position,
+//     with a parallel radix selection (11-bit digits, block-wide scans).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -31,15 +32,8 @@ constexpr int kThreads = 512;
 constexpr int kBins = 2048;
 constexpr int kBinBits = 11;
 constexpr int kCandCap = 4096;      // threshold-bin candidates collected in CTA 0
-constexpr int kRankCap = 512;       // candidates resolved by direct ranking
 constexpr int kSliceCap = 16384;    // keys per CTA kept in shared memory (64 KB)
 constexpr int kMaxCluster = 8;
-
-__device__ __forceinline__ uint64_t order64(uint32_t key, int pos)
-{
-    // larger key first, then lower position first
-    return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(pos));
-}
 
 __device__ __forceinline__ int log2_ceil_u64(uint64_t v)
 {
@@ -76,28 +70,12 @@ __device__ __forceinline__ int block_incl_scan(int v, int* ws, int* total)
     return x + (warp > 0 ? ws[warp - 1] : 0);
 }
 
-// Warp-aggregated append to a counter in CTA 0 (cluster address); returns this
-// lane's slot or -1.
-__device__ __forceinline__ int warp_append_cluster(bool take, uint32_t counter_addr)
-{
-    const unsigned m = __ballot_sync(0xffffffffu, take);
-    if (!m)
-        return -1;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(m) - 1;
-    uint32_t base = 0;
-    if (lane == leader)
-        base = atom_add_cluster(counter_addr, __popc(m));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    return take ? static_cast<int>(base) + __popc(m & ((1u << lane) - 1u)) : -1;
-}
-
 struct TopkShared {
     int hist[kBins];
     uint32_t ck[kCandCap];
     int cp[kCandCap];
     int ws[32];
-    int bin, above;
+    int bin, above, in_bin;
     int nout, ncand;
     int res_above, res_cand;      // this CTA's reserved output / candidate ranges
     uint32_t kmin, kmax;
@@ -304,61 +282,78 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     if (crank != 0)
         return;
 
-    // ---- 4. CTA 0: the `need` best candidates by (key desc, position asc)
+    // ---- 4. CTA 0: the `need` best candidates by (key desc, position asc).
+    // Radix selection on o = (key - lo) << 32 | ~position, 11 bits at a time
+    // from the top, each digit found by a block-wide scan of the digit
+    // histogram; it stops as soon as the chosen digit's bin holds exactly the
+    // number still needed (then every candidate matching the prefix is in).
     const int cand_total = sh.ncand;
     if (cand_total <= kCandCap) {
-        if (cand_total <= kRankCap) {
-            if (tid < cand_total) {
-                const uint64_t me = order64(sh.ck[tid], sh.cp[tid]);
-                int rank = 0;
-                for (int j = 0; j < cand_total; ++j)
-                    rank += order64(sh.ck[j], sh.cp[j]) > me ? 1 : 0;
-                if (rank < need)
-                    out[n_direct + rank] = sh.cp[tid];
-            }
-        } else {
-            // radix selection on the 64-bit order, 8 bits at a time (high to low)
-            uint64_t prefix = 0;
-            int rem = need;
-            for (int pass = 7; pass >= 0; --pass) {
-                const int sh8 = 8 * pass;
-                for (int j = tid; j < 256; j += kThreads)
-                    sh.hist[j] = 0;
-                __syncthreads();
-                for (int j = tid; j < cand_total; j += kThreads) {
-                    const uint64_t o = order64(sh.ck[j], sh.cp[j]);
-                    if (pass == 7 || (o >> (sh8 + 8)) == (prefix >> (sh8 + 8)))
-                        atomicAdd(&sh.hist[(o >> sh8) & 255], 1);
-                }
-                __syncthreads();
-                if (tid == 0) {
-                    int acc = 0;
-                    for (int d = 255; d >= 0; --d) {
-                        if (acc + sh.hist[d] >= rem) {
-                            sh.bin = d;
-                            sh.above = acc;
-                            break;
-                        }
-                        acc += sh.hist[d];
-                    }
-                }
-                __syncthreads();
-                prefix |= static_cast<uint64_t>(sh.bin) << sh8;
-                rem -= sh.above;
-                __syncthreads();
-            }
-            // order values are unique: exactly `need` candidates are >= prefix
-            if (tid == 0)
-                sh.nout = n_direct;
+        const int key_bits = log2_ceil_u64(static_cast<uint64_t>(hi - lo) + 1);
+        auto cand_order = [&](int j) -> uint64_t {
+            return (static_cast<uint64_t>(sh.ck[j] - lo) << 32) |
+                   static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(sh.cp[j]));
+        };
+        uint64_t prefix = 0;
+        int rem = need;
+        int top = 32 + key_bits;                          // bits [0, top) still undecided
+        while (top > 0) {
+            const int lo_bit = max(0, top - kBinBits);
+            const uint64_t mask = (uint64_t(1) << (top - lo_bit)) - 1;
+            for (int j = tid; j < kBins; j += kThreads)
+                sh.hist[j] = 0;
             __syncthreads();
-            const uint32_t my_nout = mapa_shared(smem_u32(&sh.nout), 0);
-            for (int base = 0; base < cand_total; base += kThreads) {
-                const int j = base + tid;
-                const bool t = j < cand_total && order64(sh.ck[j], sh.cp[j]) >= prefix;
-                const int slot = warp_append_cluster(t, my_nout);
-                if (slot >= 0)
-                    out[slot] = sh.cp[j];
+            for (int j = tid; j < cand_total; j += kThreads) {
+                const uint64_t o = cand_order(j);
+                if (top >= 64 || (o >> top) == (prefix >> top))
+                    atomicAdd(&sh.hist[(o >> lo_bit) & mask], 1);
             }
+            __syncthreads();
+            // suffix counts from the top bin down: thread t owns bins 2047-4t .. 2044-4t
+            int c[4], loc = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                c[q] = sh.hist[kBins - 1 - 4 * tid - q];
+                loc += c[q];
+            }
+            int total;
+            const int incl = block_incl_scan(loc, sh.ws, &total);
+            int before = incl - loc;
+            if (before < rem && rem <= incl) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (before + c[q] >= rem) {
+                        sh.bin = kBins - 1 - 4 * tid - q;
+                        sh.above = before;
+                        sh.in_bin = c[q];
+                        break;
+                    }
+                    before += c[q];
+                }
+            }
+            __syncthreads();
+            prefix |= static_cast<uint64_t>(sh.bin) << lo_bit;
+            rem -= sh.above;
+            const int in_bin = sh.in_bin;
+            top = lo_bit;
+            __syncthreads();
+            if (in_bin == rem)
+                break;                                    // the whole bin is taken
+        }
+        // selected: candidates whose bits [top, 64) are >= the prefix's
+        if (tid == 0)
+            sh.nout = n_direct;
+        __syncthreads();
+        for (int base = 0; base < cand_total; base += kThreads) {
+            const int j = base + tid;
+            const bool t = j < cand_total && (top >= 64 ? true : (cand_order(j) >> top) >= (prefix >> top));
+            const unsigned m = __ballot_sync(0xffffffffu, t);
+            int slot = 0;
+            if (lane == __ffs(m) - 1)
+                slot = atomicAdd(&sh.nout, __popc(m));
+            slot = __shfl_sync(0xffffffffu, slot, m ? __ffs(m) - 1 : 0) + __popc(m & ((1u << lane) - 1u));
+            if (t)
+                out[slot] = sh.cp[j];
         }
     } else {
         // every candidate carries one key value (shift reached 0): take the

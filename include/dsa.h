@@ -146,7 +146,7 @@ DSA_API dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int b
  *           MXFP4: [rows_total, num_heads, head_dim/2] packed e2m1, with
  * q_scales: [rows_total, num_heads, head_dim/32] ue8m0 (MXFP4 only, else NULL).
  * q_fmt:    must equal k->fmt (DSA_KV_FP8_E4M3 or DSA_KV_MXFP4).
- * weights:  fp32 [rows_total, num_heads].
+ * weights:  fp32 [rows_total, num_heads], 16-byte aligned.
  * k:        the paged indexer K cache; FP8 caches carry k_scale per token,
  *           MXFP4 caches carry block scales only (k_scale = 1).
  * sched:    built by dsa_indexer_build_schedule() with the same batch, next_n,
@@ -180,7 +180,7 @@ DSA_API dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales,
  * minus the schedule buffer: the schedule is built into a fixed 256 KiB array
  * inside the library (one per GPU the process uses, held until exit), then the
  * logits kernel runs on it -- two launches on `stream`, nothing allocated.
- *  - Limit: at most 16382 work units (units = sequences for decode with
+ *  - Limit: at most 8191 work units (units = sequences for decode with
  *    next_n * num_heads <= 256; ceil(rows / (256 / num_heads)) for prefill);
  *    larger calls return DSA_ERR_CAPACITY and enqueue nothing.
  *  - The first call on a device looks up the array's device address (once per

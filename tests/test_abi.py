@@ -48,15 +48,15 @@ def test_paged_cache_struct_layout():
 
 def test_schedule_bytes_counts_units(L):
     # decode: one unit per sequence (64 heads -> at most 4 rows per unit, next_n 1)
-    assert L.dsa_indexer_schedule_bytes(64, 1, 64, 0, 64) == 32 + 16 * 64
+    assert L.dsa_indexer_schedule_bytes(64, 1, 64, 0, 64) == 32 + 32 * 64
     # next_n 3 with 64 heads: 3 rows fit one MMA (192 columns) -> one unit per sequence
-    assert L.dsa_indexer_schedule_bytes(5, 3, 64, 0, 15) == 32 + 16 * 5
+    assert L.dsa_indexer_schedule_bytes(5, 3, 64, 0, 15) == 32 + 32 * 5
     # prefill chunk: 4 rows per unit
-    assert L.dsa_indexer_schedule_bytes(1, 16384, 64, 0, 8192) == 32 + 16 * 2048
-    assert L.dsa_indexer_schedule_bytes(1, 16384, 64, 8192, 16384) == 32 + 16 * 2048
+    assert L.dsa_indexer_schedule_bytes(1, 16384, 64, 0, 8192) == 32 + 32 * 2048
+    assert L.dsa_indexer_schedule_bytes(1, 16384, 64, 8192, 16384) == 32 + 32 * 2048
     # a range cutting through sequences: rows 2..9 of next_n 4 (H=128 -> 2 rows/unit)
     # seq0 rows 2,3 -> 1 unit; seq1 rows 4..7 -> 2 units; seq2 rows 8,9 -> 1 unit
-    assert L.dsa_indexer_schedule_bytes(3, 4, 128, 2, 10) == 32 + 16 * 4
+    assert L.dsa_indexer_schedule_bytes(3, 4, 128, 2, 10) == 32 + 32 * 4
     # invalid row ranges give 0
     assert L.dsa_indexer_schedule_bytes(2, 1, 64, 0, 3) == 0
     assert L.dsa_indexer_schedule_bytes(2, 0, 64, 0, 0) == 0

@@ -113,11 +113,18 @@ def test_schedule_buffer_contents():
     st.indexer_chunk(0, case.rows)
     torch.cuda.synchronize()
     s = st.sched.cpu().numpy()
-    assert s[0] == 0x44534131 and s[1] == 4 and s[2] == 2 and s[3] == 0 and s[4] == 8
-    units = s[8:8 + 16].reshape(4, 4)
-    tiles = [(parity.visible(case, 2 * b + 1) + 127) // 128 for b in range(4)]
+    assert s[0] == 0x44534132 and s[1] == 4 and s[2] == 2 and s[3] == 0 and s[4] == 8
+    # 32-byte records: first_row, nrows, seq, tile_begin, tile_end, vis_max, ctx_len, 0
+    units = s[8:8 + 32].reshape(4, 8)
+    vis = [parity.visible(case, 2 * b + 1) for b in range(4)]
+    tiles = [(v + 127) // 128 for v in vis]
+    begins = list(np.concatenate([[0], np.cumsum(tiles)[:-1]]))
     assert list(units[:, 0]) == [0, 2, 4, 6] and list(units[:, 1]) == [2] * 4
-    assert list(units[:, 3]) == list(np.concatenate([[0], np.cumsum(tiles)[:-1]]))
+    assert list(units[:, 2]) == [0, 1, 2, 3]
+    assert list(units[:, 3]) == begins
+    assert list(units[:, 4]) == [b + t for b, t in zip(begins, tiles)]
+    assert list(units[:, 5]) == vis
+    assert list(units[:, 6]) == [0, 129, 5000, 128] and list(units[:, 7]) == [0] * 4
     assert s[6] == sum(tiles)
 
 

@@ -84,7 +84,7 @@ def test_mxfp4_through_the_noalloc_entry_point():
 
 
 def test_too_many_work_units_is_refused():
-    # 70000 prefill rows at 64 heads = 17500 units > 16382: refused on the host,
+    # 70000 prefill rows at 64 heads = 17500 units > 8191: refused on the host,
     # before any pointer is touched
     L = _abi.lib()
     fake = ctypes.c_void_p(0x1000)
