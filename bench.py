@@ -286,12 +286,24 @@ def run_ours(args, rank, world, local):
 
 
 def load_traffic(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from one ncu
+    capture (profiles/traffic.json), or None when there is none or the kernel's
+    sources changed since it was taken."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    return d.get("%s/%s" % (kernel, workload))
+        d = json.load(f).get("%s/%s" % (kernel, workload))
+    if not d:
+        return None
+    h = hashlib.sha256()
+    for name in d["source_files"]:
+        with open(os.path.join(ROOT, "deepseek_sparse_attention_mqa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != d["source_sha256_16"]:
+        return None
+    return d["traffic_bytes_per_launch"]
 
 
 def measure_e2e(st, case, args, pairs, dev):
