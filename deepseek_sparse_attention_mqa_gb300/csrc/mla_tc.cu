@@ -48,9 +48,10 @@ constexpr int kMaxChunks = 5;           // 64-dim chunks per CTA (576 = 4 + 5 ch
 constexpr int kVChunks = 4;             // 256 value dims per CTA
 constexpr int kQChunkBytes = 128 * 128; // 128 heads x 64 f16
 constexpr int kLChunkBytes = kNT * 128; // 64 tokens x 64 f16
-constexpr int kThreads = 288;           // 9 warps
-constexpr int kConvWarp0 = 4;
+constexpr int kThreads = 416;           // 13 warps
+constexpr int kConvWarp0 = 4;           // gather warps 4-7
 constexpr int kMmaWarp = 8;
+constexpr int kSoftWarp1 = 9;           // softmax warps 0-3 (tokens 0-31) and 9-12 (tokens 32-63)
 constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, O at 256
 constexpr float kRescaleLog2 = 8.f;     // refresh the running max only past 2^8
 constexpr int kGatherItems = (16 * kMaxChunks * 4 + 31) / 32;      // 16-byte segments per gather lane
@@ -80,7 +81,7 @@ struct MlaParams {
 };
 
 struct MlaSmem {
-    uint32_t q, lat, p, x, scale, valid, qexp, bar, misc, total;
+    uint32_t q, lat, p, x, scale, valid, qexp, red, bar, misc, total;
 };
 
 __host__ __device__ constexpr MlaSmem mla_smem()
@@ -93,8 +94,9 @@ __host__ __device__ constexpr MlaSmem mla_smem()
     m.scale = m.x + 128 * kNT * 4;
     m.valid = m.scale + 2 * kNT * 4;
     m.qexp = m.valid + 2 * kNT * 4;
-    m.bar = m.qexp + 128 * 4;
-    m.misc = m.bar + 16 * 8;
+    m.red = m.qexp + 128 * 4;
+    m.bar = m.red + 2 * 2 * 128 * 4;
+    m.misc = m.bar + 24 * 8;
     m.total = m.misc + 16;
     return m;
 }
@@ -136,6 +138,8 @@ sparse_mla_tc_kernel(const MlaParams p)
     float* sScale = reinterpret_cast<float*>(smem + mp.scale);
     int* sValid = reinterpret_cast<int*>(smem + mp.valid);
     int* sQexp = reinterpret_cast<int*>(smem + mp.qexp);       // per-head power-of-two Q scale
+    float* sMax = reinterpret_cast<float*>(smem + mp.red);        // [2][128] block max per half
+    float* sSum = sMax + 2 * 128;                                  // [2][128] final sum per half
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + mp.bar);
     uint64_t* q_full = bars + 0;
     uint64_t* lat_full = bars + 1;   // [2]
@@ -147,6 +151,7 @@ sparse_mla_tc_kernel(const MlaParams p)
     uint64_t* p_full = bars + 11;
     uint64_t* p_empty = bars + 12;
     uint64_t* o_done = bars + 13;
+    uint64_t* pair_bar = bars + 14;  // [4] the two softmax warps of a lane quarter
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc + 4);
 
@@ -166,13 +171,15 @@ sparse_mla_tc_kernel(const MlaParams p)
             mbar_init(smem_u32(&lat_full[i]), 4);
             mbar_init(smem_u32(&lat_empty[i]), 1);
             mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&s_empty[i]), 4);
+            mbar_init(smem_u32(&s_empty[i]), 8);
         }
-        mbar_init(smem_u32(x_full), 4);
-        mbar_init(smem_u32(x_free), 4);
-        mbar_init(smem_u32(p_full), 4);
+        mbar_init(smem_u32(x_full), 1);            // local expect_tx + the peer's st.async bytes
+        mbar_init(smem_u32(x_free), 8);            // the peer's 8 softmax warps
+        mbar_init(smem_u32(p_full), 8);
         mbar_init(smem_u32(p_empty), 1);
         mbar_init(smem_u32(o_done), 1);
+        for (int i = 0; i < 4; ++i)
+            mbar_init(smem_u32(&pair_bar[i]), 2);
         *s_abort = 0;
         fence_barrier_init();
     }
@@ -264,34 +271,35 @@ sparse_mla_tc_kernel(const MlaParams p)
                 }
             }
         };
-        int64_t off_n;
-        int valid_n;
-        float scale_n;
-        resolve(0, off_n, valid_n, scale_n);
+        // The loads of block j + 1 are issued as soon as block j is stored, so they
+        // fly while the indices of block j + 2 are resolved and while the latent
+        // buffer of block j + 1 is waited for.
+        auto issue_loads = [&](uint4 (&raw)[kGatherItems], int64_t off, int valid) {
+#pragma unroll
+            for (int i = 0; i < kGatherItems; ++i) {
+                const int flat = i * 32 + lane;
+                const int tl = flat / nseg, seg = flat % nseg;
+                const int64_t o = __shfl_sync(0xffffffffu, off, tl & 15);
+                const int v = __shfl_sync(0xffffffffu, valid, tl & 15);
+                raw[i] = make_uint4(0, 0, 0, 0);
+                if (flat < 16 * nseg && v)
+                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + o + (c_lo * 64 + seg * 16));
+            }
+        };
+        int64_t off_a, off_b;
+        int valid_a, valid_b;
+        float scale_a, scale_b;
+        uint4 raw[kGatherItems];
+        resolve(0, off_a, valid_a, scale_a);
+        issue_loads(raw, off_a, valid_a);
+        resolve(1, off_b, valid_b, scale_b);
         for (int j = 0; j < nblk && !__any_sync(0xffffffffu, *s_abort); ++j) {
             const int st = j & 1;
-            const int64_t off_c = off_n;
-            const int valid_c = valid_n;
-            const float scale_c = scale_n;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_empty[st]), ((j >> 1) & 1) ^ 1))) {
                 *s_abort = 1;
                 break;
             }
             uint8_t* tile = sLat + st * (kMaxChunks * kLChunkBytes);
-            // all of this lane's 16-byte segments of the block, issued back to back
-            uint4 raw[kGatherItems];
-#pragma unroll
-            for (int i = 0; i < kGatherItems; ++i) {
-                const int flat = i * 32 + lane;
-                const int tl = flat / nseg, seg = flat % nseg;
-                const int64_t o = __shfl_sync(0xffffffffu, off_c, tl & 15);
-                const int v = __shfl_sync(0xffffffffu, valid_c, tl & 15);
-                raw[i] = make_uint4(0, 0, 0, 0);
-                if (flat < 16 * nseg && v)
-                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + o + (c_lo * 64 + seg * 16));
-            }
-            // the next block's index -> page -> scale chain runs while those loads fly
-            resolve(j + 1, off_n, valid_n, scale_n);
 #pragma unroll
             for (int i = 0; i < kGatherItems; ++i) {
                 const int flat = i * 32 + lane;
@@ -306,13 +314,18 @@ sparse_mla_tc_kernel(const MlaParams p)
                 *reinterpret_cast<uint4*>(chunk + swizzled_offset(gw * 16 + tl, un + 1, 128)) = hi;
             }
             if (lane < 16) {
-                sScale[st * kNT + gw * 16 + lane] = scale_c;
-                sValid[st * kNT + gw * 16 + lane] = valid_c;
+                sScale[st * kNT + gw * 16 + lane] = scale_a;
+                sValid[st * kNT + gw * 16 + lane] = valid_a;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&lat_full[st]));
+            issue_loads(raw, off_b, valid_b);             // block j + 1 (zeros past the end)
+            off_a = off_b;
+            valid_a = valid_b;
+            scale_a = scale_b;
+            resolve(j + 2, off_b, valid_b, scale_b);
         }
     } else if (warp == kMmaWarp) {
         // ================================ MMA ===================================
@@ -391,10 +404,29 @@ sparse_mla_tc_kernel(const MlaParams p)
         }
     } else {
         // ================================ softmax ===============================
-        const int h = threadIdx.x;                        // head = TMEM lane
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t x_row = smem_u32(sX + h * (kNT * 4));
-        const uint32_t peer_x_row = mapa_shared(x_row, peer);
+        // Two threads per head (= TMEM lane): warps 0-3 take tokens [0, 32) of
+        // every block, warps 9-12 tokens [32, 64); the pair agrees on the block
+        // max through shared memory and a named barrier, and keeps the running
+        // max in lockstep (both see the same sequence of block maxima).
+        const int quarter = warp & 3;
+        const int half = warp >= kSoftWarp1 ? 1 : 0;
+        const int h = quarter * 32 + lane;                // head = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int tcol = half * 32;                       // this thread's tokens within a block
+        // the two warps of this lane quarter meet on pair_bar[quarter] (bounded
+        // waits, so a warp that gives up cannot strand its partner)
+        uint32_t pair_uses = 0;
+        auto pair_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&pair_bar[quarter]));
+            const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pair_bar[quarter]), pair_uses & 1));
+            ++pair_uses;
+            return r;
+        };
+        // the peer's X row of this head: this thread's 32 partial scores go to units
+        // [half*8, half*8 + 8) of it (16-byte units XOR-swizzled by head)
+        const uint32_t peer_x_row = mapa_shared(smem_u32(sX + h * (kNT * 4)), peer);
         const uint32_t peer_x_full = mapa_shared(smem_u32(x_full), peer);
         const uint32_t peer_x_free = mapa_shared(smem_u32(x_free), peer);
         float m_run = -INFINITY, l_run = 0.f;
@@ -411,58 +443,50 @@ sparse_mla_tc_kernel(const MlaParams p)
                 break;
             }
             tc_fence_after_sync();
-            uint32_t ra[32], rb[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_base + sb * kNT, ra);
-            tmem_ld_32x32b_x32(tmem_base + lane_base + sb * kNT + 32, rb);
+            uint32_t ra[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + sb * kNT + tcol, ra);
             tmem_ld_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&s_empty[sb]));
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 32; ++i)
                 ra[i] = __float_as_uint(__uint_as_float(ra[i]) * qback);
-                rb[i] = __float_as_uint(__uint_as_float(rb[i]) * qback);
-            }
 
-            // ---- exchange partial scores with the peer CTA (16-byte units, XOR-swizzled by row)
+            // ---- exchange partial scores with the peer CTA: asynchronous remote
+            // stores whose bytes complete the peer's x_full transaction count
+            if (warp == 0 && lane == 0)
+                mbar_arrive_expect_tx(smem_u32(x_full), static_cast<uint32_t>(128 * kNT * 4));
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(x_free), (j & 1) ^ 1))) {
                 ok = false;
                 break;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                st_cluster_v4(peer_x_row + ((u ^ (h & 7)) << 4), ra[4 * u], ra[4 * u + 1], ra[4 * u + 2], ra[4 * u + 3]);
-#pragma unroll
-            for (int u = 8; u < 16; ++u)
-                st_cluster_v4(peer_x_row + ((u ^ (h & 7)) << 4), rb[4 * u - 32], rb[4 * u - 31], rb[4 * u - 30],
-                              rb[4 * u - 29]);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_remote(peer_x_full);
+                st_async_v4(peer_x_row + (((half * 8 + u) ^ (h & 7)) << 4), ra[4 * u], ra[4 * u + 1], ra[4 * u + 2],
+                            ra[4 * u + 3], peer_x_full);
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(x_full), j & 1))) {
                 ok = false;
                 break;
             }
-            float sco[kNT];
+            float sco[32];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float4 x = *reinterpret_cast<const float4*>(sX + h * (kNT * 4) + ((u ^ (h & 7)) << 4));
-                uint32_t own[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    own[q] = u < 8 ? ra[4 * u + q] : rb[4 * (u - 8) + q];
+            for (int u = 0; u < 8; ++u) {
+                const float4 x = *reinterpret_cast<const float4*>(sX + h * (kNT * 4) + (((half * 8 + u) ^ (h & 7)) << 4));
                 // both CTAs form partial(CTA 0) + partial(CTA 1) in the same order
+                const float o0 = __uint_as_float(ra[4 * u]), o1 = __uint_as_float(ra[4 * u + 1]);
+                const float o2 = __uint_as_float(ra[4 * u + 2]), o3 = __uint_as_float(ra[4 * u + 3]);
                 if (crank == 0) {
-                    sco[4 * u + 0] = __uint_as_float(own[0]) + x.x;
-                    sco[4 * u + 1] = __uint_as_float(own[1]) + x.y;
-                    sco[4 * u + 2] = __uint_as_float(own[2]) + x.z;
-                    sco[4 * u + 3] = __uint_as_float(own[3]) + x.w;
+                    sco[4 * u + 0] = o0 + x.x;
+                    sco[4 * u + 1] = o1 + x.y;
+                    sco[4 * u + 2] = o2 + x.z;
+                    sco[4 * u + 3] = o3 + x.w;
                 } else {
-                    sco[4 * u + 0] = x.x + __uint_as_float(own[0]);
-                    sco[4 * u + 1] = x.y + __uint_as_float(own[1]);
-                    sco[4 * u + 2] = x.z + __uint_as_float(own[2]);
-                    sco[4 * u + 3] = x.w + __uint_as_float(own[3]);
+                    sco[4 * u + 0] = x.x + o0;
+                    sco[4 * u + 1] = x.y + o1;
+                    sco[4 * u + 2] = x.z + o2;
+                    sco[4 * u + 3] = x.w + o3;
                 }
             }
             __syncwarp();
@@ -474,14 +498,21 @@ sparse_mla_tc_kernel(const MlaParams p)
                 ok = false;
                 break;
             }
-            const float* scl = sScale + sb * kNT;
-            const int* vld = sValid + sb * kNT;
-            float m_blk = -INFINITY;
+            const float* scl = sScale + sb * kNT + tcol;
+            const int* vld = sValid + sb * kNT + tcol;
+            float m_half = -INFINITY;
 #pragma unroll
-            for (int t = 0; t < kNT; ++t) {
+            for (int t = 0; t < 32; ++t) {
                 sco[t] = vld[t] ? sco[t] * (scl[t] * p.scale_log2) : -INFINITY;
-                m_blk = fmaxf(m_blk, sco[t]);
+                m_half = fmaxf(m_half, sco[t]);
             }
+            // block max of the head over both halves
+            sMax[half * 128 + h] = m_half;
+            if (!pair_sync()) {
+                ok = false;
+                break;
+            }
+            const float m_blk = fmaxf(sMax[h], sMax[128 + h]);
             // P of the previous block has been consumed (and O is stable) before
             // P is rewritten or O rescaled
             if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(p_empty), (j - 1) & 1))) {
@@ -490,8 +521,10 @@ sparse_mla_tc_kernel(const MlaParams p)
             }
             const float m_new = fmaxf(m_run, m_blk);
             // lazily refreshed running max: a head moves its max only when it grew
-            // by more than 2^8; the O rescale runs for the whole warp (factor 1 on
-            // lanes whose max stays) because TMEM access is warp-collective
+            // by more than 2^8 (both threads of the head decide alike); the O
+            // rescale runs for the whole warp (factor 1 on lanes whose max stays)
+            // because TMEM access is warp-collective, each thread of the pair
+            // scaling its half of the columns
             float f = 1.f;
             if (m_new > m_run + kRescaleLog2) {
                 if (m_run != -INFINITY) {
@@ -505,30 +538,33 @@ sparse_mla_tc_kernel(const MlaParams p)
                 tc_fence_after_sync();
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                    uint32_t o[16];                       // 16 columns at a time: sco[] stays in registers
+                    const uint32_t col = 256 + half * 128 + c * 16;
+                    tmem_ld_32x32b_x16(tmem_base + lane_base + col, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < 16; ++i)
                         o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                    tmem_st_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                    tmem_st_32x32b_x16(tmem_base + lane_base + col, o);
                 }
                 tmem_st_wait();
             }
-            // P (f16, token scale folded in for V) -> row h of the swizzled K-major tile
+            // P (f16, token scale folded in for V) -> row h, units [half*4, half*4 + 4)
+            // of the swizzled K-major tile
+            const float m_use = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                     const int t = 8 * u + 2 * q2;
-                    const float p0 = (m_run == -INFINITY || sco[t] == -INFINITY) ? 0.f : exp2f(sco[t] - m_run);
-                    const float p1 = (m_run == -INFINITY || sco[t + 1] == -INFINITY) ? 0.f : exp2f(sco[t + 1] - m_run);
+                    const float p0 = exp2f(sco[t] - m_use);          // -inf -> 0
+                    const float p1 = exp2f(sco[t + 1] - m_use);
                     l_run += p0 + p1;
                     const __half2 b = __floats2half2_rn(p0 * scl[t], p1 * scl[t + 1]);
                     pk[q2] = *reinterpret_cast<const uint32_t*>(&b);
                 }
-                *reinterpret_cast<uint4*>(sP + swizzled_offset(h, u, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(sP + swizzled_offset(h, half * 4 + u, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -538,16 +574,19 @@ sparse_mla_tc_kernel(const MlaParams p)
         }
         if (!ok)
             *s_abort = 1;
-        // ---- epilogue: O / l -> bf16 out[row][h][crank*256 + v], lse (natural log)
-        const bool have = __all_sync(0xffffffffu, nblk > 0 && ok && mbar_wait(smem_u32(o_done), 0) && !*s_abort);
+        // ---- epilogue: O / l -> bf16 out[row][h][crank*256 + half*128 + v], lse (natural log)
+        sSum[half * 128 + h] = l_run;
+        const bool paired = ok && pair_sync();
+        const float l_tot = sSum[h] + sSum[128 + h];
+        const bool have = __all_sync(0xffffffffu, nblk > 0 && paired && mbar_wait(smem_u32(o_done), 0) && !*s_abort);
         tc_fence_after_sync();
-        const float inv = (have && l_run > 0.f) ? 1.f / l_run : 0.f;
-        __nv_bfloat16* orow = p.out + (static_cast<int64_t>(row) * p.num_heads + h) * 512 + crank * 256;
+        const float inv = (have && l_tot > 0.f) ? 1.f / l_tot : 0.f;
+        __nv_bfloat16* orow = p.out + (static_cast<int64_t>(row) * p.num_heads + h) * 512 + crank * 256 + half * 128;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
             if (have) {                                   // warp-uniform: all lanes load
-                tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + c * 32, o);
+                tmem_ld_32x32b_x32(tmem_base + lane_base + 256 + half * 128 + c * 32, o);
                 tmem_ld_wait();
             }
             if (h < p.num_heads) {
@@ -565,9 +604,9 @@ sparse_mla_tc_kernel(const MlaParams p)
                 }
             }
         }
-        if (crank == 0 && h < p.num_heads)
+        if (crank == 0 && half == 0 && h < p.num_heads)
             p.lse[static_cast<int64_t>(row) * p.num_heads + h] =
-                (have && l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+                (have && l_tot > 0.f) ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
     }
 
     __syncwarp();

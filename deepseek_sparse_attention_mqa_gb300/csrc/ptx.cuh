@@ -330,6 +330,23 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                  : "memory");
 }
 
+// 16-byte asynchronous store into another CTA's shared memory; its bytes
+// complete the transaction count of that CTA's mbarrier (both cluster addresses).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+                 : "memory");
+}
+
+// Named barrier among `count` threads (a multiple of 32) of this CTA; id 0 is
+// __syncthreads'.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
 // prior writes (including remote shared-memory stores) at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
