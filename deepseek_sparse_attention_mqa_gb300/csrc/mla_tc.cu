@@ -390,7 +390,6 @@ sparse_mla_tc_kernel(const MlaParams p)
                     t_idle = 0;
                     continue;
                 }
-                __nanosleep(20);                        // leave issue slots to the warps sharing this SMSP
                 if (t_idle == 0) {
                     t_idle = global_timer_ns();
                 } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
@@ -489,9 +488,12 @@ sparse_mla_tc_kernel(const MlaParams p)
                     sco[4 * u + 3] = x.w + o3;
                 }
             }
+            // X is consumed (its values are in registers): hand it back to the
+            // peer.  A relaxed arrive: a releasing one would also wait for this
+            // thread's st.async to the peer to complete.
             __syncwarp();
             if (lane == 0)
-                mbar_arrive_remote(peer_x_free);
+                mbar_arrive_remote_relaxed(peer_x_free);
 
             // ---- scores in base 2; masked slots are -inf
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_full[sb]), ph))) {
