@@ -131,4 +131,39 @@ struct TileWalk {
     }
 };
 
+// Walks this CTA's super-tiles.  A super-tile is up to R consecutive 128-token
+// tiles of ONE unit, aligned to the unit's first tile; it belongs to the CTA
+// whose tile range [t0, t1) holds its first tile (it may run past t1).  Every
+// role walks the same sequence, so the super-tile ordinal j is the same in all.
+struct SuperWalk {
+    TileWalk w;
+    int R, t1, ts, nt;   // current super-tile: tiles [ts, ts + nt) of unit w.u
+
+    __device__ __forceinline__ void settle()
+    {
+        if (ts >= w.ui.tile_end)
+            ts = w.ui.tile_end;              // the next unit's first tile
+        w.seek(ts);
+        nt = min(R, w.ui.tile_end - ts);
+    }
+    __device__ __forceinline__ void start(const WalkParams& wp, const SchedUnit* units, int total, int t0,
+                                          int t1_, int R_, int u0)
+    {
+        R = R_;
+        t1 = t1_;
+        w.start_at(wp, units, total, t0, u0);
+        const int off = max(0, t0 - w.ui.tile_begin);
+        ts = w.ui.tile_begin + ((off + R - 1) / R) * R;
+        settle();
+    }
+    __device__ __forceinline__ bool valid() const { return ts < t1 && nt > 0; }
+    __device__ __forceinline__ void next()
+    {
+        ts += R;
+        settle();
+    }
+    // first tile of the super-tile inside its unit
+    __device__ __forceinline__ int tile_in_unit() const { return ts - w.ui.tile_begin; }
+};
+
 }  // namespace dsa

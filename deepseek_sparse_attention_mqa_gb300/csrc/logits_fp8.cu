@@ -121,41 +121,6 @@ __host__ __device__ __forceinline__ SmemMap smem_map(int D, int R, int stages, u
     return m;
 }
 
-// Walks this CTA's super-tiles.  A super-tile is up to R consecutive 128-token
-// tiles of ONE unit, aligned to the unit's first tile; it belongs to the CTA
-// whose tile range [t0, t1) holds its first tile (it may run past t1).  Every
-// role walks the same sequence, so the super-tile ordinal j is the same in all.
-struct SuperWalk {
-    TileWalk w;
-    int R, t1, ts, nt;   // current super-tile: tiles [ts, ts + nt) of unit w.u
-
-    __device__ __forceinline__ void settle()
-    {
-        if (ts >= w.ui.tile_end)
-            ts = w.ui.tile_end;              // the next unit's first tile
-        w.seek(ts);
-        nt = min(R, w.ui.tile_end - ts);
-    }
-    __device__ __forceinline__ void start(const WalkParams& wp, const SchedUnit* units, int total, int t0,
-                                          int t1_, int R_, int u0)
-    {
-        R = R_;
-        t1 = t1_;
-        w.start_at(wp, units, total, t0, u0);
-        const int off = max(0, t0 - w.ui.tile_begin);
-        ts = w.ui.tile_begin + ((off + R - 1) / R) * R;
-        settle();
-    }
-    __device__ __forceinline__ bool valid() const { return ts < t1 && nt > 0; }
-    __device__ __forceinline__ void next()
-    {
-        ts += R;
-        settle();
-    }
-    // first tile of the super-tile inside its unit
-    __device__ __forceinline__ int tile_in_unit() const { return ts - w.ui.tile_begin; }
-};
-
 template <int D, int H>
 __global__ void __launch_bounds__(Fp8Roles<H>::kThreads, 1)
 logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -620,11 +585,12 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
 
     __syncwarp();
-    if (threadIdx.x == 0 && *s_abort && p.status)
-        atomicOr(p.status, DSA_DEV_TIMEOUT);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // every role is done: a wait that gave up anywhere in the CTA is visible now
+    if (threadIdx.x == 0 && *s_abort && p.status)
+        atomicOr(p.status, DSA_DEV_TIMEOUT);
     if (warp == kProd)
         tmem_dealloc(tmem_base, p.n_acc * p.R * p.acc_cols);
 }

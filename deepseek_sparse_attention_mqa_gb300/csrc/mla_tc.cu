@@ -612,11 +612,12 @@ sparse_mla_tc_kernel(const MlaParams p)
     }
 
     __syncwarp();
-    if (threadIdx.x == 0 && *s_abort && p.status)
-        atomicOr(p.status, DSA_DEV_TIMEOUT);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // every role is done: a wait that gave up anywhere in the CTA is visible now
+    if (threadIdx.x == 0 && *s_abort && p.status)
+        atomicOr(p.status, DSA_DEV_TIMEOUT);
     if (warp == kMmaWarp)
         tmem_dealloc(tmem_base, kTmemCols);
     cluster_sync();              // no CTA leaves while its peer may still touch its shared memory
