@@ -18,18 +18,26 @@
 // arithmetic, hence identical softmax decisions) and each accumulates its half
 // of O = P V in TMEM, where V is the first 256 dims of its own latent slice.
 //
-//   warps 0-3  softmax: thread = head = TMEM lane.  Exchange partial scores,
-//              scale by token scale * softmax scale, online max / sum in base 2
-//              with a lazily refreshed running max (O in TMEM is rescaled only
-//              when the max grows by more than 2^8), write P (f16, with the
-//              token scale folded in for V; f16 rather than bf16 keeps its
-//              rounding at 2^-12) to shared memory, finally normalise
-//              O and store bf16 out / fp32 lse.
+//   warps 0-3, 9-12  softmax, two threads per head (TMEM lane = head): warps
+//              0-3 take tokens 0-31 of each block, warps 9-12 tokens 32-63.
+//              Each sends its half of the partial scores to the peer CTA with
+//              st.async (completing on the peer's mbarrier), adds the peer's
+//              half, scales by token scale * softmax scale and keeps an online
+//              max / sum in base 2; the two threads of a head combine their
+//              block maxima through shared memory and a two-thread mbarrier.
+//              The running max is refreshed lazily (O in TMEM is rescaled only
+//              when the max grows by more than 2^8).  P is written as f16
+//              (token scale folded in for V; f16 rather than bf16 keeps its
+//              rounding at 2^-12); at the end O is normalised and stored as
+//              bf16 out / fp32 lse.
 //   warps 4-7  gather: per 64-token block, look up each selected token through
-//              the block table, load its FP8 slice, widen to f16 into a 128B-
-//              swizzled K-major tile (zeros for unused slots).
+//              the block table (two blocks ahead), load its FP8 slice (the
+//              next block's loads are issued before this block's widening
+//              stores), widen to f16 into a 128B-swizzled K-major tile (zeros
+//              for unused slots).
 //   warp 8     TMEM allocator + MMA issuer: S = Q K^T (M=128, N=64) and
-//              O += P V (M=128, N=256, V read MN-major from the same tile).
+//              O += P V (M=128, N=256, V read MN-major from the same tile),
+//              each issued as soon as its inputs are ready.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -128,6 +128,29 @@ def test_schedule_buffer_contents():
     assert s[6] == sum(tiles)
 
 
+def test_schedule_reused_across_launches():
+    """One schedule, several stream-ordered logits launches (a captured decode
+    graph replays the logits launch on the buffer its schedule launch filled):
+    every launch reads the schedule only and reproduces the first one's logits
+    bit for bit."""
+    for fmt_case in ("decode", "spec_mxfp4"):
+        case = inputs.make_case(fmt_case, device="cuda", batch=9, seed=21)
+        st = SparseAttentionStep(case, with_mla=False)
+        st.indexer_chunk(0, case.rows)
+        torch.cuda.synchronize()
+        first = st.logits.clone()
+        c = case
+        for rep in range(3):
+            st.logits.fill_(float("nan"))
+            _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
+                            c.batch, c.next_n, 0, c.rows, st.sched, st.logits, st.width, st.status)
+            torch.cuda.synchronize()
+            assert st.device_status() == 0
+            for r in range(c.rows):
+                v = parity.visible(case, r)
+                assert torch.equal(st.logits[r, :v], first[r, :v]), (fmt_case, rep, r)
+
+
 def test_decode_full_size_sampled_rows():
     case = inputs.make_case("decode", device="cuda")
     g, st = gpu_logits(case)
