@@ -9,11 +9,13 @@
 // for a 64-row decode batch); CTA c owns a contiguous slice of the row, keeps it
 // in shared memory as order-preserving uint32 keys, and the cluster cooperates
 // through distributed shared memory with CTA 0 as the meeting point:
-//  1. key range [kmin, kmax] of the row (cluster min/max reduction);
+//  1. key range [kmin, kmax] of the row: each CTA publishes its own, and after
+//     one cluster barrier every CTA reads all of them;
 //  2. 2048 bins over the range by a right shift -- bins uniform in bit-pattern
 //     space, i.e. log scale, so outliers and wide ranges cost nothing; one
 //     histogram round (local histograms added into CTA 0's) finds the bin of
-//     the k-th largest key, refined inside that bin while it is crowded;
+//     the k-th largest key, refined inside that bin while it is crowded; CTA 0
+//     pushes each decision into every CTA's shared memory;
 //  3. every position above that bin is written out directly (cluster-wide
 //     counter); the bin's few elements are appended to CTA 0 as candidates;
 //  4. CTA 0 resolves the candidates exactly by the 64-bit order (key, then lower
@@ -75,14 +77,16 @@ struct TopkShared {
     uint32_t ck[kCandCap];
     int cp[kCandCap];
     int ws[32];
-    int bin, above, in_bin;
+    int bin, above, in_bin;       // histogram decision (pushed by CTA 0)
+    uint32_t rlo, rhi;            // the row's key range
     int nout, ncand;
     int res_above, res_cand;      // this CTA's reserved output / candidate ranges
     uint32_t kmin, kmax;
 };
 
+// two CTAs per SM: a decode batch's clusters (e.g. 64 rows x 4 CTAs) fit in one wave
 template <bool kCached>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             const int32_t* __restrict__ context_lens, int next_n, int row_begin, int k,
             int32_t* __restrict__ idx, int64_t idx_stride, int32_t* __restrict__ count,
@@ -124,23 +128,25 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     const int n = s_hi - s_lo;
 
     // CTA 0's copies of the shared reduction state (cluster addresses)
-    const uint32_t c0_kmin = mapa_shared(smem_u32(&sh.kmin), 0);
-    const uint32_t c0_kmax = mapa_shared(smem_u32(&sh.kmax), 0);
     const uint32_t c0_hist = mapa_shared(smem_u32(&sh.hist[0]), 0);
-    const uint32_t c0_bin = mapa_shared(smem_u32(&sh.bin), 0);
-    const uint32_t c0_above = mapa_shared(smem_u32(&sh.above), 0);
     const uint32_t c0_nout = mapa_shared(smem_u32(&sh.nout), 0);
     const uint32_t c0_ncand = mapa_shared(smem_u32(&sh.ncand), 0);
     const uint32_t c0_ck = mapa_shared(smem_u32(&sh.ck[0]), 0);
     const uint32_t c0_cp = mapa_shared(smem_u32(&sh.cp[0]), 0);
 
+    // Everything another CTA touches remotely is initialised before the first
+    // cluster barrier (the range barrier below), so no barrier is needed here:
+    // this CTA's own range and its first-round histogram, and CTA 0's output
+    // and candidate counters.
     if (tid == 0) {
         sh.kmin = 0xFFFFFFFFu;
         sh.kmax = 0u;
         sh.nout = 0;
         sh.ncand = 0;
     }
-    cluster_sync();                                       // CTA 0's state initialised
+    for (int j = tid; j < kBins; j += kThreads)
+        sh.hist[j] = 0;
+    __syncthreads();
 
     // ---- 1. keys of the slice and the row's key range
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -180,23 +186,44 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     }
     if (lane == 0 && n > 0) {
-        red_min_cluster(c0_kmin, kmin);
-        red_max_cluster(c0_kmax, kmax);
+        atomicMin(&sh.kmin, kmin);
+        atomicMax(&sh.kmax, kmax);
     }
-    cluster_sync();
+    cluster_sync();                                       // every CTA's range and zeroed histogram
+    if (tid < 32) {
+        // lane c reads CTA c's range; the warp reduces them
+        uint32_t a = 0xFFFFFFFFu, z = 0u;
+        if (lane < C) {
+            a = ld_cluster_u32(mapa_shared(smem_u32(&sh.kmin), static_cast<uint32_t>(lane)));
+            z = ld_cluster_u32(mapa_shared(smem_u32(&sh.kmax), static_cast<uint32_t>(lane)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+            z = max(z, __shfl_xor_sync(0xffffffffu, z, o));
+        }
+        if (lane == 0) {
+            sh.rlo = a;
+            sh.rhi = z;
+        }
+    }
+    __syncthreads();
     auto key_at = [&](int j) -> uint32_t {               // j: index within the slice
         return kCached ? s_keys[j] : float_key(__float_as_uint(__ldg(row + s_lo + j)));
     };
-    uint32_t lo = ld_cluster_u32(c0_kmin), hi = ld_cluster_u32(c0_kmax);
+    uint32_t lo = sh.rlo, hi = sh.rhi;
 
     // ---- 2. histogram rounds: the bin of the k-th largest key
     int need = k;                 // still to take from keys in [lo, hi]
-    while (true) {
+    for (int round = 0;; ++round) {
         const uint64_t span = static_cast<uint64_t>(hi) - lo + 1;
         const int shift = max(0, log2_ceil_u64(span) - kBinBits);
-        for (int j = tid; j < kBins; j += kThreads)
-            sh.hist[j] = 0;
-        cluster_sync();                                   // every histogram (CTA 0's too) zeroed
+        if (round > 0) {
+            // (the first round's histograms were zeroed before the range barrier)
+            for (int j = tid; j < kBins; j += kThreads)
+                sh.hist[j] = 0;
+            cluster_sync();                               // every histogram (CTA 0's too) zeroed
+        }
         for (int j = tid; j < n; j += kThreads) {
             const uint32_t key = key_at(j);
             if (key >= lo && key <= hi)
@@ -223,18 +250,23 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if (before + c[q] >= need) {
-                        sh.bin = kBins - 1 - 4 * tid - q;
-                        sh.above = before;
+                        // the decision goes to every CTA of the cluster
+                        const int db = kBins - 1 - 4 * tid - q;
+                        for (int cr = 0; cr < C; ++cr) {
+                            st_cluster_u32(mapa_shared(smem_u32(&sh.bin), cr), static_cast<uint32_t>(db));
+                            st_cluster_u32(mapa_shared(smem_u32(&sh.above), cr), static_cast<uint32_t>(before));
+                            st_cluster_u32(mapa_shared(smem_u32(&sh.in_bin), cr), static_cast<uint32_t>(c[q]));
+                        }
                         break;
                     }
                     before += c[q];
                 }
             }
         }
-        cluster_sync();                                   // decision visible in CTA 0
-        const int bin = static_cast<int>(ld_cluster_u32(c0_bin));
-        need -= static_cast<int>(ld_cluster_u32(c0_above));
-        const int in_bin = static_cast<int>(ld_cluster_u32(c0_hist + 4u * bin));
+        cluster_sync();                                   // decision in every CTA
+        const int bin = sh.bin;
+        need -= sh.above;
+        const int in_bin = sh.in_bin;
         const uint32_t blo = lo + (static_cast<uint32_t>(bin) << shift);
         const uint32_t bhi = static_cast<uint32_t>(
             min(static_cast<uint64_t>(hi), static_cast<uint64_t>(blo) + ((uint64_t(1) << shift) - 1)));
@@ -242,7 +274,6 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         hi = bhi;
         if (in_bin <= kCandCap || shift == 0)
             break;
-        cluster_sync();                                   // everyone read CTA 0's histogram
     }
     const int n_direct = k - need;                        // keys > hi are taken outright
 
@@ -255,9 +286,20 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         n_above += key > hi ? 1 : 0;
         n_cand += (key >= lo && key <= hi) ? 1 : 0;
     }
-    int tot_above, tot_cand;
-    const int off_above = block_incl_scan(n_above, sh.ws, &tot_above) - n_above;
-    const int off_cand = block_incl_scan(n_cand, sh.ws, &tot_cand) - n_cand;
+    int tot_above, tot_cand, off_above, off_cand;
+    if (n < 65536) {
+        // both counts in one scan: above in bits 0-15, candidates in bits 16-31
+        int tot;
+        const int v = n_above | (n_cand << 16);
+        const uint32_t ex = static_cast<uint32_t>(block_incl_scan(v, sh.ws, &tot) - v);
+        off_above = static_cast<int>(ex & 0xFFFFu);
+        off_cand = static_cast<int>(ex >> 16);
+        tot_above = static_cast<int>(static_cast<uint32_t>(tot) & 0xFFFFu);
+        tot_cand = static_cast<int>(static_cast<uint32_t>(tot) >> 16);
+    } else {
+        off_above = block_incl_scan(n_above, sh.ws, &tot_above) - n_above;
+        off_cand = block_incl_scan(n_cand, sh.ws, &tot_cand) - n_cand;
+    }
     if (tid == 0) {
         sh.res_above = tot_above ? static_cast<int>(atom_add_cluster(c0_nout, static_cast<uint32_t>(tot_above))) : 0;
         sh.res_cand = tot_cand ? static_cast<int>(atom_add_cluster(c0_ncand, static_cast<uint32_t>(tot_cand))) : 0;
