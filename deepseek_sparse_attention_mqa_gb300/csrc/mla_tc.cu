@@ -9,7 +9,8 @@
 //
 // GB300 design: one CLUSTER of two CTAs per query row.  The output O
 // (128 heads x 512 fp32) fills a whole TMEM, so it is split by value dims:
-// CTA 0 owns latent dims [0, 256) and CTA 1 owns [256, d_qk); each keeps its
+// CTA c owns latent dims [256 c, 256 c + 256) and, at d_qk 576, half of the
+// rope dims, [512 + 32 c, 544 + 32 c), so both do equal work; each keeps its
 // part of Q resident (f16, swizzled K-major, times a per-head power of two that
 // fits it to f16 range exactly), gathers and widens its part of the selected
 // latent rows (FP8 -> f16, exact) and computes a PARTIAL score
@@ -52,7 +53,7 @@ namespace dsa {
 namespace {
 
 constexpr int kNT = 64;                 // selected tokens per block
-constexpr int kMaxChunks = 5;           // 64-dim chunks per CTA (576 = 4 + 5 chunks)
+constexpr int kMaxChunks = 5;           // 64-dim tile chunks per CTA (4 value chunks + a half-used rope chunk)
 constexpr int kVChunks = 4;             // 256 value dims per CTA
 constexpr int kQChunkBytes = 128 * 128; // 128 heads x 64 f16
 constexpr int kLChunkBytes = kNT * 128; // 64 tokens x 64 f16
@@ -62,7 +63,8 @@ constexpr int kMmaWarp = 8;
 constexpr int kSoftWarp1 = 9;           // softmax warps 0-3 (tokens 0-31) and 9-12 (tokens 32-63)
 constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, O at 256
 constexpr float kRescaleLog2 = 8.f;     // refresh the running max only past 2^8
-constexpr int kGatherItems = (16 * kMaxChunks * 4 + 31) / 32;      // 16-byte segments per gather lane
+constexpr int kMaxSeg = 18;             // 16-byte FP8 segments per token and CTA (256 + 32 dims)
+constexpr int kGatherItems = (16 * kMaxSeg + 31) / 32;      // 16-byte segments per gather lane
 
 struct MlaParams {
     const __nv_bfloat16* q;
@@ -168,9 +170,18 @@ sparse_mla_tc_kernel(const MlaParams p)
     const uint32_t peer = crank ^ 1u;
     const int row = blockIdx.y;
     const int seq = p.seq_of_row ? p.seq_of_row[row] : row / p.next_n;
-    // latent dims of this CTA: chunks [c_lo, c_lo + nchunk) of 64
-    const int c_lo = crank == 0 ? 0 : kVChunks;
-    const int nchunk = crank == 0 ? kVChunks : (p.d_qk / 64 - kVChunks);
+    // Latent dims of this CTA: its value dims [256 c, 256 c + 256) (tile chunks
+    // 0-3, also V for its half of O) and, at d_qk 576, half of the rope dims,
+    // [512 + 32 c, 544 + 32 c) (the first half of tile chunk 4), so that both
+    // CTAs gather and multiply 288 dims per token and neither waits for the
+    // other at the score exchange.
+    const bool rope = p.d_qk == 576;
+    const int nchunk = rope ? kVChunks + 1 : kVChunks;
+    const int nseg = rope ? kMaxSeg : 16;            // 16-byte FP8 segments per token
+    // latent dim of this CTA's 16-dim segment sg (FP8 byte offset in the row)
+    auto seg_dim = [&](int sg) -> int {
+        return sg < 16 ? static_cast<int>(crank) * 256 + sg * 16 : 512 + static_cast<int>(crank) * 32 + (sg - 16) * 16;
+    };
     const int nblk = (p.k + kNT - 1) / kNT;
 
     if (threadIdx.x == 0) {
@@ -211,12 +222,14 @@ sparse_mla_tc_kernel(const MlaParams p)
         // are scaled back by 2^-e in fp32.
         {
             const int h = ct;
-            const __nv_bfloat16* qh =
-                p.q + (static_cast<int64_t>(row) * p.num_heads + h) * p.d_qk + c_lo * 64;
+            // f16 unit u (8 dims) of this CTA's slice: two units per FP8 segment
+            const __nv_bfloat16* qh = p.q + (static_cast<int64_t>(row) * p.num_heads + h) * p.d_qk;
+            const int nunit = 2 * nseg;
+            auto qdim = [&](int u) -> int { return seg_dim(u >> 1) + (u & 1) * 8; };
             float amax = 0.f;
             if (h < p.num_heads)
-                for (int u = 0; u < nchunk * 8; ++u) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(qh + u * 8);
+                for (int u = 0; u < nunit; ++u) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(qh + qdim(u));
                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -232,10 +245,10 @@ sparse_mla_tc_kernel(const MlaParams p)
             }
             sQexp[h] = e;
             const float sc = exp2_int(e);
-            for (int u = 0; u < nchunk * 8; ++u) {
+            for (int u = 0; u < nunit; ++u) {
                 uint4 o = make_uint4(0, 0, 0, 0);
                 if (h < p.num_heads) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(qh + u * 8);
+                    const uint4 v = *reinterpret_cast<const uint4*>(qh + qdim(u));
                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
                     uint32_t r4[4];
 #pragma unroll
@@ -255,7 +268,6 @@ sparse_mla_tc_kernel(const MlaParams p)
             mbar_arrive(smem_u32(q_full));
 
         const int32_t* irow = p.idx + static_cast<int64_t>(row) * p.idx_stride;
-        const int nseg = nchunk * 4;                    // 16-byte FP8 segments per token
         const int gw = warp - kConvWarp0;               // this warp gathers tokens [16 gw, 16 gw + 16) of a block
         // Resolve the warp's 16 tokens of block jb (lane l < 16 owns one): index ->
         // block table -> byte offset of the latent row and its fp32 scale.
@@ -291,7 +303,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                 const int v = __shfl_sync(0xffffffffu, valid, tl & 15);
                 raw[i] = make_uint4(0, 0, 0, 0);
                 if (flat < 16 * nseg && v)
-                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + o + (c_lo * 64 + seg * 16));
+                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + o + seg_dim(seg));
             }
         };
         int64_t off_a, off_b;
@@ -353,8 +365,11 @@ sparse_mla_tc_kernel(const MlaParams p)
                 const uint32_t qa = smem_u32(sQ);
                 const uint32_t kb = smem_u32(sLat + st * (kMaxChunks * kLChunkBytes));
                 for (int ch = 0; ch < nchunk; ++ch) {
+                    const int nks = ch < kVChunks ? 4 : 2;       // the rope chunk holds 32 dims
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
+                        if (ks >= nks)
+                            break;
                         const uint64_t ad = make_smem_desc(qa + ch * kQChunkBytes + ks * 32, 16, 1024, kLayoutSw128);
                         const uint64_t bd = make_smem_desc(kb + ch * kLChunkBytes + ks * 32, 16, 1024, kLayoutSw128);
                         umma_f16(d, ad, bd, idesc_qk, (ch | ks) != 0 ? 1u : 0u);
