@@ -269,31 +269,43 @@ sparse_mla_tc_kernel(const MlaParams p)
 
         const int32_t* irow = p.idx + static_cast<int64_t>(row) * p.idx_stride;
         const int gw = warp - kConvWarp0;               // this warp gathers tokens [16 gw, 16 gw + 16) of a block
-        // Resolve the warp's 16 tokens of block jb (lane l < 16 owns one): index ->
-        // block table -> byte offset of the latent row and its fp32 scale.
-        auto resolve = [&](int jb, int64_t& off, int& valid, float& scale) {
+        // Lane l < 16 owns token gw * 16 + l of every block.  Finding a token's
+        // latent row takes three dependent global loads (index -> block table ->
+        // row and scale), so they are software-pipelined across iterations: while
+        // block j is stored, the latent loads of block j + 1 fly, block j + 2's
+        // row address is formed from the block-table entry loaded one iteration
+        // earlier, block j + 3's block-table entry is loaded and block j + 4's
+        // index.  Each load thus has a whole iteration to land.
+        auto tok_of = [&](int jb) -> int { return jb * kNT + gw * 16 + lane; };
+        auto load_idx = [&](int jb) -> int {       // -1: no token (padding or past k)
+            return (lane < 16 && jb < nblk && tok_of(jb) < p.k) ? irow[tok_of(jb)] : -1;
+        };
+        auto load_page = [&](int sidx) -> int {    // block-table entry of a token (-1 if none)
+            if (sidx < 0)
+                return -1;
+            const int lp = sidx / p.page_kv;
+            return lp < p.max_pages ? p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp] : -1;
+        };
+        // row address of a token from its index and page: latent byte offset and
+        // scale byte offset, or valid = 0 (a selected token with no valid page is
+        // reported and contributes nothing)
+        auto address = [&](int sidx, int pg, int64_t& off, int64_t& soff, int& valid) {
             off = 0;
+            soff = 0;
             valid = 0;
-            scale = 0.f;
-            const int jj = jb * kNT + gw * 16 + lane;
-            if (lane < 16 && jb < nblk && jj < p.k) {
-                const int s = irow[jj];
-                if (s >= 0) {
-                    const int lp = s / p.page_kv;
-                    const int pg = lp < p.max_pages ? p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp] : -1;
-                    if (pg >= 0 && pg < p.num_pages) {
-                        off = pg * p.vps + (s % p.page_kv) * p.vts;
-                        scale = *reinterpret_cast<const float*>(p.scs + pg * p.sps + (s % p.page_kv) * p.sts);
-                        valid = 1;
-                    } else if (p.status) {
-                        atomicOr(p.status, DSA_DEV_BAD_INDEX);
-                    }
-                }
+            if (sidx < 0)
+                return;
+            if (pg >= 0 && pg < p.num_pages) {
+                off = pg * p.vps + (sidx % p.page_kv) * p.vts;
+                soff = pg * p.sps + (sidx % p.page_kv) * p.sts;
+                valid = 1;
+            } else if (p.status) {
+                atomicOr(p.status, DSA_DEV_BAD_INDEX);
             }
         };
-        // The loads of block j + 1 are issued as soon as block j is stored, so they
-        // fly while the indices of block j + 2 are resolved and while the latent
-        // buffer of block j + 1 is waited for.
+        auto load_scale = [&](int64_t soff, int valid) -> float {
+            return valid ? *reinterpret_cast<const float*>(p.scs + soff) : 0.f;
+        };
         auto issue_loads = [&](uint4 (&raw)[kGatherItems], int64_t off, int valid) {
 #pragma unroll
             for (int i = 0; i < kGatherItems; ++i) {
@@ -306,13 +318,17 @@ sparse_mla_tc_kernel(const MlaParams p)
                     raw[i] = *reinterpret_cast<const uint4*>(p.vals + o + seg_dim(seg));
             }
         };
-        int64_t off_a, off_b;
-        int valid_a, valid_b;
-        float scale_a, scale_b;
+        // prologue: indices of blocks 0-3, pages of blocks 0-2, addresses of 0-1
+        int s0 = load_idx(0), s1 = load_idx(1), s2 = load_idx(2), s3 = load_idx(3);
+        const int pg0 = load_page(s0), pg1 = load_page(s1);
+        int pg2 = load_page(s2);
+        int64_t off0, soff0, off1, soff1;
+        int valid0, valid1;
+        address(s0, pg0, off0, soff0, valid0);
+        address(s1, pg1, off1, soff1, valid1);
         uint4 raw[kGatherItems];
-        resolve(0, off_a, valid_a, scale_a);
-        issue_loads(raw, off_a, valid_a);
-        resolve(1, off_b, valid_b, scale_b);
+        issue_loads(raw, off0, valid0);
+        float scale0 = load_scale(soff0, valid0);
         for (int j = 0; j < nblk && !__any_sync(0xffffffffu, *s_abort); ++j) {
             const int st = j & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_empty[st]), ((j >> 1) & 1) ^ 1))) {
@@ -334,18 +350,31 @@ sparse_mla_tc_kernel(const MlaParams p)
                 *reinterpret_cast<uint4*>(chunk + swizzled_offset(gw * 16 + tl, un + 1, 128)) = hi;
             }
             if (lane < 16) {
-                sScale[st * kNT + gw * 16 + lane] = scale_a;
-                sValid[st * kNT + gw * 16 + lane] = valid_a;
+                sScale[st * kNT + gw * 16 + lane] = scale0;
+                sValid[st * kNT + gw * 16 + lane] = valid0;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&lat_full[st]));
-            issue_loads(raw, off_b, valid_b);             // block j + 1 (zeros past the end)
-            off_a = off_b;
-            valid_a = valid_b;
-            scale_a = scale_b;
-            resolve(j + 2, off_b, valid_b, scale_b);
+            // block j + 1: latent loads and its scale (zeros past the end)
+            issue_loads(raw, off1, valid1);
+            const float scale1 = load_scale(soff1, valid1);
+            // block j + 2: row address from the page loaded last iteration
+            int64_t off2, soff2;
+            int valid2;
+            address(s2, pg2, off2, soff2, valid2);
+            // block j + 3: its page; block j + 4: its index
+            const int pg3 = load_page(s3);
+            const int s4 = load_idx(j + 4);
+            valid0 = valid1;
+            scale0 = scale1;
+            off1 = off2;
+            soff1 = soff2;
+            valid1 = valid2;
+            s2 = s3;
+            pg2 = pg3;
+            s3 = s4;
         }
     } else if (warp == kMmaWarp) {
         // ================================ MMA ===================================
