@@ -307,17 +307,19 @@ def load_traffic(kernel, workload):
 
 
 def measure_e2e(st, case, args, pairs, dev):
-    from deepseek_sparse_attention_mqa_gb300 import _abi
-    c = case
-    host = {k: getattr(c, k).cpu().pin_memory() for k in ("q", "weights", "context_lens", "block_table")}
+    """Same metric through the step API with host buffers: every step copies its
+    query-side inputs (one packed pinned arena: q, weights, context lengths,
+    block table) to the device, runs, and reads the top-k indices back."""
+    from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep, StepInputs
+    ins = StepInputs(case, with_mla=False)
+    st = SparseAttentionStep(ins.case(), with_mla=False)
     idx_host = torch.empty(st.idx.shape, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = ins.nbytes
     d2h = idx_host.numel() * 4
     stream = torch.cuda.current_stream()
     steps = max(10, args.steps // 4)
     for _ in range(3):
-        for k, t in host.items():
-            getattr(c, k).copy_(t, non_blocking=True)
+        ins.copy_in(stream)
         st.run()
         idx_host.copy_(st.idx, non_blocking=True)
     torch.cuda.synchronize()
@@ -328,8 +330,7 @@ def measure_e2e(st, case, args, pairs, dev):
     for s in range(steps):
         flush.fill_(float(s))
         e0.record(stream)
-        for k, t in host.items():
-            getattr(c, k).copy_(t, non_blocking=True)
+        ins.copy_in(stream)
         st.run()
         idx_host.copy_(st.idx, non_blocking=True)
         e1.record(stream)

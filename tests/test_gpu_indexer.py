@@ -151,6 +151,35 @@ def test_schedule_reused_across_launches():
                 assert torch.equal(st.logits[r, :v], first[r, :v]), (fmt_case, rep, r)
 
 
+def test_packed_step_inputs_match():
+    """The packed input arena (one host-to-device copy per step) feeds the same
+    kernels with the same bytes: logits and top-k are bit-identical to a step
+    over the separately allocated tensors, also after the host side is
+    rewritten and copied in again."""
+    from deepseek_sparse_attention_mqa_gb300.step import StepInputs
+    for name in ("decode", "spec_mxfp4"):
+        case = inputs.make_case(name, device="cuda", batch=6, seed=5, with_mla=False)
+        st = SparseAttentionStep(case, with_mla=False)
+        st.run()
+        ins = StepInputs(case, with_mla=False)
+        st2 = SparseAttentionStep(ins.case(), with_mla=False)
+        for w in ins.host["weights"], ins.device["weights"]:
+            assert w.shape == case.weights.shape
+        ins.host["weights"].mul_(2.0)                     # a new step's inputs ...
+        ins.copy_in()
+        ins.host["weights"].mul_(0.5)                     # ... and back
+        ins.copy_in()
+        st2.run()
+        torch.cuda.synchronize()
+        assert st2.device_status() == 0 and st.device_status() == 0
+        # the selected set is unique; its order follows the CTAs' output reservations
+        assert torch.equal(st.idx.sort(dim=1).values, st2.idx.sort(dim=1).values)
+        assert torch.equal(st.count, st2.count)
+        for r in range(case.rows):
+            v = parity.visible(case, r)
+            assert torch.equal(st.logits[r, :v], st2.logits[r, :v])
+
+
 def test_decode_full_size_sampled_rows():
     case = inputs.make_case("decode", device="cuda")
     g, st = gpu_logits(case)
