@@ -605,15 +605,24 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
 #pragma unroll
                             for (int q = 0; q < 16; ++q)
                                 dot[q] = 0.f;
+                            // two scale blocks' TMEM loads in flight per wait
 #pragma unroll
-                            for (int bk = 0; bk < NB; ++bk) {
-                                uint32_t r[16];
-                                tmem_ld_32x32b_x16(t_acc0 + static_cast<uint32_t>(m * NB + bk) * p.acc_cols + cb, r);
+                            for (int b0 = 0; b0 < NB; b0 += 2) {
+                                uint32_t r[2][16];
+                                tmem_ld_32x32b_x16(t_acc0 + static_cast<uint32_t>(m * NB + b0) * p.acc_cols + cb, r[0]);
+                                if (b0 + 1 < NB)
+                                    tmem_ld_32x32b_x16(t_acc0 + static_cast<uint32_t>(m * NB + b0 + 1) * p.acc_cols + cb,
+                                                       r[1]);
                                 tmem_ld_wait();
-                                const float* sq = sqS + bk * p.w_cols + cb;
 #pragma unroll
-                                for (int q = 0; q < 16; ++q)
-                                    dot[q] = fmaf(sq[q] * sk[bk], __uint_as_float(r[q]), dot[q]);
+                                for (int u = 0; u < 2; ++u) {
+                                    if (b0 + u < NB) {
+                                        const float* sq = sqS + (b0 + u) * p.w_cols + cb;
+#pragma unroll
+                                        for (int q = 0; q < 16; ++q)
+                                            dot[q] = fmaf(sq[q] * sk[b0 + u], __uint_as_float(r[u][q]), dot[q]);
+                                    }
+                                }
                             }
                             float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
