@@ -202,10 +202,13 @@ def run_ours(args, rank, world, local):
         e = ev[s]
         e[0].record(stream)
         for ci, (rb, re) in enumerate(chunks):
-            _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status)
+            inline = st.inline[(rb, re)]          # no schedule launch: the logits kernel builds the units
+            if not inline:
+                _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status)
             e[3 * ci + 1].record(stream)
             _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
-                            c.batch, c.next_n, rb, re, st.sched, st.logits, st.width, st.status)
+                            c.batch, c.next_n, rb, re, None if inline else st.sched, st.logits, st.width,
+                            st.status)
             e[3 * ci + 2].record(stream)
             st.topk_chunk(rb, re)
             e[3 * ci + 3].record(stream)
@@ -271,7 +274,7 @@ def run_ours(args, rank, world, local):
                           "logits": round(statistics.mean(logits_ms), 5),
                           "topk": round(statistics.mean(topk_ms), 5), "chunks": nck},
             "roofline": roof,
-            "gpu_launches": 3 * nck * args.steps,
+            "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clocks,
             "e2e": e2e,
             "full_step": full,

@@ -148,11 +148,29 @@ def build_schedule(context_lens, batch, next_n, num_heads, row_begin, row_end, s
 
 def mqa_logits(q, q_scales, fmt, weights, num_heads, cache: PagedCache, context_lens, batch,
                next_n, row_begin, row_end, sched, logits, logits_width, status=None, stream=None):
+    """indexer_mqa_logits_paged; ``sched=None`` lets the kernel build the units of
+    a call with at most INLINE_UNITS units itself (no schedule launch)."""
     _check(lib().indexer_mqa_logits_paged(
         _ptr(q), _ptr(q_scales), int(fmt), _ptr(weights), num_heads, ctypes.byref(cache),
         _ptr(context_lens), batch, next_n, row_begin, row_end, _ptr(sched),
-        sched.numel() * sched.element_size(), _ptr(logits), logits.stride(0), int(logits_width),
-        _ptr(status), _stream(stream)), "indexer_mqa_logits_paged")
+        0 if sched is None else sched.numel() * sched.element_size(), _ptr(logits), logits.stride(0),
+        int(logits_width), _ptr(status), _stream(stream)), "indexer_mqa_logits_paged")
+
+
+INLINE_UNITS = 256      # kInlineUnits of the library
+
+
+def units_of(batch, next_n, num_heads, row_begin, row_end) -> int:
+    """Work units of a logits call (rows of one sequence sharing an MMA)."""
+    if row_end <= row_begin:
+        return 0
+    g = max(1, min(next_n, 256 // num_heads))
+    total = 0
+    b0, b1 = row_begin // next_n, (row_end - 1) // next_n
+    for b in range(b0, min(b1, batch - 1) + 1):
+        lo, hi = max(b * next_n, row_begin), min((b + 1) * next_n, row_end)
+        total += (hi - lo + g - 1) // g
+    return total
 
 
 def mqa_logits_noalloc(q, q_scales, fmt, weights, num_heads, cache: PagedCache, context_lens,

@@ -230,14 +230,16 @@ dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_f
     // units of at most 128 columns (rows x heads) in the 512 TMEM columns
     if (q_fmt == DSA_KV_MXFP4 && D == 128 && unit_rows(next_n, num_heads) * num_heads > 128)
         return DSA_ERR_UNSUPPORTED;
-    if (!q || !aligned16(q) || !weights || !aligned16(weights) || !logits || !sched || !aligned16(sched) ||
+    if (!q || !aligned16(q) || !weights || !aligned16(weights) || !logits || (sched && !aligned16(sched)) ||
         (batch > 0 && !context_lens))
         return DSA_ERR_INVALID_ARG;
     if (logits_width < 0 || logits_row_stride < logits_width)
         return DSA_ERR_INVALID_ARG;
     const int G = unit_rows(next_n, num_heads);
     const int64_t units = count_units(batch, next_n, G, row_begin, row_end);
-    if (sched_bytes < static_cast<size_t>(sched_bytes_for_units(units)))
+    if (sched && sched_bytes < static_cast<size_t>(sched_bytes_for_units(units)))
+        return DSA_ERR_CAPACITY;
+    if (!sched && units > kInlineUnits)      // the kernels build at most kInlineUnits units themselves
         return DSA_ERR_CAPACITY;
     if (row_end == row_begin)
         return DSA_OK;

@@ -12,6 +12,9 @@ namespace dsa {
 constexpr int kTileTokens = 128;
 // Largest MMA N (rows x heads per work unit).
 constexpr int kMaxUnitCols = 256;
+// Largest unit count for which a logits launch without a schedule buffer builds
+// the unit records itself (in shared memory, in every CTA).
+constexpr int kInlineUnits = 256;
 
 // Visible length of draft row i of a sequence of context length L with next_n
 // new tokens: clamp(L - next_n + i + 1, 0, L) ("SM120 FP8 paged MQA page 32",
@@ -84,6 +87,32 @@ __host__ __device__ __forceinline__ int64_t count_units(int batch, int next_n, i
         }
     }
     return total;
+}
+
+// Unit u -> (sequence, first absolute row, rows) for rows [row_begin, row_end).
+__device__ __forceinline__ void unit_rows_of(int u, int next_n, int G, int row_begin, int row_end,
+                                             int* seq, int* first_row, int* nrows)
+{
+    const int b0 = row_begin / next_n;
+    const int lo0 = row_begin;
+    const int hi0 = min((b0 + 1) * next_n, row_end);
+    const int u_first = (hi0 - lo0 + G - 1) / G;
+    const int U = (next_n + G - 1) / G;  // units of a sequence fully inside the range
+    int b, lo, hi, j;
+    if (u < u_first) {
+        b = b0;
+        lo = lo0;
+        hi = hi0;
+        j = u;
+    } else {
+        b = b0 + 1 + (u - u_first) / U;
+        j = (u - u_first) % U;
+        lo = b * next_n;
+        hi = min((b + 1) * next_n, row_end);
+    }
+    *seq = b;
+    *first_row = lo + j * G;
+    *nrows = min(G, hi - *first_row);
 }
 
 // Order-preserving map of an fp32 bit pattern to uint32 (larger float -> larger

@@ -166,4 +166,76 @@ struct SuperWalk {
     __device__ __forceinline__ int tile_in_unit() const { return ts - w.ui.tile_begin; }
 };
 
+// ------------------------------------------------------------ inline schedule
+//
+// A logits launch without a schedule buffer builds the unit records itself, in
+// shared memory, when there are at most kInlineUnits units (a decode batch of up
+// to 256 sequences): every CTA computes the same records from the context
+// lengths in its prologue, which costs about what reading a prebuilt schedule
+// costs and saves the schedule kernel's launch.  ("Add fp4 indexer for dsv4",
+// commit notes: with a prebuilt schedule buffer the scoring kernel skips its own
+// build.)  kInlineUnits is in common.cuh.
+constexpr uint32_t kInlineScratchBytes = 160;   // 33 ints of scan scratch, 16-byte multiple
+
+// All threads of the CTA call this (blockDim.x >= num_units, blockDim.x <= 1024).
+// Writes records [0, num_units) to `su` exactly as the schedule kernel does and
+// returns the total number of 128-token tiles.
+__device__ __forceinline__ int build_inline_units(SchedUnit* su, int* scratch, const int32_t* context_lens,
+                                                  int batch, int next_n, int G, int row_begin, int row_end,
+                                                  int num_units, int32_t* status)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = static_cast<int>(blockDim.x + 31) >> 5;
+    int seq = 0, first_row = 0, nrows = 0, tiles = 0, vis = 0, ctx = 0;
+    if (tid < num_units) {
+        unit_rows_of(tid, next_n, G, row_begin, row_end, &seq, &first_row, &nrows);
+        if (seq < batch && nrows > 0) {
+            const int L = context_lens[seq];
+            ctx = L < 0 ? 0 : L;
+            vis = visible_len(ctx, next_n, first_row + nrows - 1 - seq * next_n);
+            tiles = (vis + kTileTokens - 1) / kTileTokens;
+        } else if (status) {
+            atomicOr(status, DSA_DEV_SCHEDULE);
+        }
+    }
+    // block-wide exclusive scan of the tile counts
+    int incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        scratch[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o)
+                t += v;
+        }
+        scratch[lane] = t;                     // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = (warp > 0 ? scratch[warp - 1] : 0) + incl - tiles;
+    if (tid < num_units) {
+        SchedUnit r;
+        r.first_row = first_row;
+        r.nrows = nrows;
+        r.seq = seq;
+        r.tile_begin = excl;
+        r.tile_end = excl + tiles;
+        r.vis_max = vis;
+        r.ctx_len = ctx;
+        r.pad = 0;
+        su[tid] = r;
+    }
+    const int total = scratch[nw - 1];
+    __syncthreads();
+    return total;
+}
+
 }  // namespace dsa

@@ -66,7 +66,9 @@ struct Fp8Roles {
 };
 
 struct LogitsParams {
-    const int32_t* sched;
+    const int32_t* sched;       // prebuilt schedule, or null: the CTAs build the units themselves
+    int batch;
+    int inline_units;           // units built in shared memory (0 with a prebuilt schedule)
     const int32_t* context_lens;
     const int32_t* block_table;
     int64_t bt_stride;
@@ -105,11 +107,11 @@ struct Fp8Tile {
 
 // Shared memory map (offsets from a 1024-aligned base).
 struct SmemMap {
-    uint32_t k_off, q_off, sc_off, w_off, ks_off, pc_off, bar_off, misc_off, total;
+    uint32_t k_off, q_off, sc_off, w_off, ks_off, pc_off, bar_off, misc_off, units_off, total;
 };
 
 __host__ __device__ __forceinline__ SmemMap smem_map(int D, int R, int stages, uint32_t q_buf_bytes, int w_cols,
-                                                     int epi_warps)
+                                                     int epi_warps, int inline_units)
 {
     SmemMap m;
     m.k_off = 0;
@@ -120,7 +122,8 @@ __host__ __device__ __forceinline__ SmemMap smem_map(int D, int R, int stages, u
     m.pc_off = m.ks_off + epi_warps * R * 32 * 4;            // token scales per epilogue warp
     m.bar_off = m.pc_off + kProd * kPageCache * 4;
     m.misc_off = m.bar_off + (2 * kMaxStages + 2 * kMaxAcc + 4 + kMma) * 8;
-    m.total = m.misc_off + 16;
+    m.units_off = m.misc_off + 16;               // inline schedule: records, then scan scratch
+    m.total = m.units_off + (inline_units > 0 ? inline_units * 32 + kInlineScratchBytes : 0);
     return m;
 }
 
@@ -134,7 +137,7 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemMap mp = smem_map(D, p.R, p.stages, p.q_buf_bytes, p.w_cols, kEpiWarps);
+    const SmemMap mp = smem_map(D, p.R, p.stages, p.q_buf_bytes, p.w_cols, kEpiWarps, p.inline_units);
     const uint32_t stage_bytes = static_cast<uint32_t>(p.R) * T::kBlockBytes;
     const int stage_tokens = p.R * kTileTokens;
     uint8_t* sK = smem + mp.k_off;
@@ -157,16 +160,28 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- schedule header (uniform over the CTA, checked before any allocation)
-    const int32_t* hdr = p.sched;
-    const SchedUnit* units = reinterpret_cast<const SchedUnit*>(p.sched + kSchedHeaderWords);
-    if (hdr[0] != kSchedMagic || hdr[1] != p.num_units || hdr[2] != p.rows_per_unit ||
-        hdr[3] != p.row_begin || hdr[4] != p.row_end || hdr[5] != p.next_n) {
-        if (threadIdx.x == 0 && p.status)
-            atomicOr(p.status, DSA_DEV_SCHEDULE);
-        return;
+    // ---- the schedule: a prebuilt buffer (its header checked, uniformly over the
+    // CTA, before any allocation) or the units built here in shared memory
+    const SchedUnit* units;
+    int total_tiles;
+    if (p.sched) {
+        const int32_t* hdr = p.sched;
+        units = reinterpret_cast<const SchedUnit*>(p.sched + kSchedHeaderWords);
+        if (hdr[0] != kSchedMagic || hdr[1] != p.num_units || hdr[2] != p.rows_per_unit ||
+            hdr[3] != p.row_begin || hdr[4] != p.row_end || hdr[5] != p.next_n) {
+            if (threadIdx.x == 0 && p.status)
+                atomicOr(p.status, DSA_DEV_SCHEDULE);
+            return;
+        }
+        total_tiles = hdr[6];
+    } else {
+        SchedUnit* su = reinterpret_cast<SchedUnit*>(smem + mp.units_off);
+        int* scratch = reinterpret_cast<int*>(smem + mp.units_off + p.inline_units * 32);
+        total_tiles = build_inline_units(su, scratch, p.context_lens, p.batch, p.next_n, p.rows_per_unit,
+                                         p.row_begin, p.row_end, p.num_units,
+                                         blockIdx.x == 0 ? p.status : nullptr);
+        units = su;
     }
-    const int total_tiles = hdr[6];
     const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total_tiles) / gridDim.x);
     const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total_tiles) / gridDim.x);
     if (t0 >= t1 || p.num_units == 0)
@@ -672,15 +687,19 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     const int budget = std::min(dev.max_smem_optin, 227 * 1024) - 1024;
     constexpr int kEpiWarps = Fp8Roles<H>::kEpiWarps;
     int stages = (kMaxStages / step) * step;
-    while (stages > step && static_cast<int>(smem_map(D, R, stages, q_buf_bytes, w_cols, kEpiWarps).total) > budget)
+    const int inline_units = a.sched ? 0 : a.num_units;
+    while (stages > step &&
+           static_cast<int>(smem_map(D, R, stages, q_buf_bytes, w_cols, kEpiWarps, inline_units).total) > budget)
         stages -= step;
-    const SmemMap mp = smem_map(D, R, stages, q_buf_bytes, w_cols, kEpiWarps);
+    const SmemMap mp = smem_map(D, R, stages, q_buf_bytes, w_cols, kEpiWarps, inline_units);
     if (static_cast<int>(mp.total) > budget || n_acc % lcm2(kMma, n_grp) != 0)
         return DSA_ERR_UNSUPPORTED;
     const int smem_bytes = static_cast<int>(mp.total) + 1024;
 
     LogitsParams p;
     p.sched = a.sched;
+    p.batch = a.batch;
+    p.inline_units = inline_units;
     p.context_lens = a.context_lens;
     p.block_table = k->block_table;
     p.bt_stride = k->bt_row_stride;

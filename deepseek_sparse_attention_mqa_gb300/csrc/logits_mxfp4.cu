@@ -61,7 +61,10 @@ constexpr int kMaxR = 4;
 constexpr int kPageCache = 128;
 
 struct Mx4Params {
-    const int32_t* sched;
+    const int32_t* sched;       // prebuilt schedule, or null: the CTAs build the units themselves
+    const int32_t* context_lens;
+    int batch;
+    int inline_units;           // units built in shared memory (0 with a prebuilt schedule)
     const int32_t* block_table;
     int64_t bt_stride;
     int max_pages;
@@ -104,12 +107,12 @@ struct Mx4Layout {
 };
 
 struct Mx4Smem {
-    uint32_t raw_k, raw_sc, conv_k, conv_sc, q, w, sq, ks, qraw, wraw, pc, bar, misc, total;
+    uint32_t raw_k, raw_sc, conv_k, conv_sc, q, w, sq, ks, qraw, wraw, pc, bar, misc, units, total;
 };
 
 template <int D>
 __host__ __device__ __forceinline__ Mx4Smem mx4_smem(int R, int raw_stages, int conv_stages, uint32_t q_buf_bytes,
-                                                     int w_cols)
+                                                     int w_cols, int inline_units)
 {
     using Lt = Mx4Layout<D>;
     Mx4Smem m;
@@ -126,7 +129,8 @@ __host__ __device__ __forceinline__ Mx4Smem mx4_smem(int R, int raw_stages, int 
     m.pc = m.wraw + 2 * w_cols * 4;                                 // fp32 weights of the next units
     m.bar = m.pc + kProd * kPageCache * 4;
     m.misc = m.bar + (2 * kMaxRaw + 2 * kMaxConv + 2 * kMaxAcc + 4 + kMma + 2) * 8;
-    m.total = m.misc + 16;
+    m.units = m.misc + 16;                                          // inline schedule: records, scan scratch
+    m.total = m.units + (inline_units > 0 ? inline_units * 32 + kInlineScratchBytes : 0);
     return m;
 }
 
@@ -173,7 +177,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Mx4Smem mp = mx4_smem<D>(p.R, p.raw_stages, p.conv_stages, p.q_buf_bytes, p.w_cols);
+    const Mx4Smem mp = mx4_smem<D>(p.R, p.raw_stages, p.conv_stages, p.q_buf_bytes, p.w_cols, p.inline_units);
     const int R = p.R;
     const int st_tokens = R * kTileTokens;
     uint8_t* sRawK = smem + mp.raw_k;
@@ -201,15 +205,28 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
     volatile int* s_u0 = reinterpret_cast<volatile int*>(smem + mp.misc + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int32_t* hdr = p.sched;
-    const SchedUnit* units = reinterpret_cast<const SchedUnit*>(p.sched + kSchedHeaderWords);
-    if (hdr[0] != kSchedMagic || hdr[1] != p.num_units || hdr[2] != p.rows_per_unit ||
-        hdr[3] != p.row_begin || hdr[4] != p.row_end || hdr[5] != p.next_n) {
-        if (threadIdx.x == 0 && p.status)
-            atomicOr(p.status, DSA_DEV_SCHEDULE);
-        return;
+    // the schedule: a prebuilt buffer (header checked uniformly over the CTA) or
+    // the units built here in shared memory
+    const SchedUnit* units;
+    int total_tiles;
+    if (p.sched) {
+        const int32_t* hdr = p.sched;
+        units = reinterpret_cast<const SchedUnit*>(p.sched + kSchedHeaderWords);
+        if (hdr[0] != kSchedMagic || hdr[1] != p.num_units || hdr[2] != p.rows_per_unit ||
+            hdr[3] != p.row_begin || hdr[4] != p.row_end || hdr[5] != p.next_n) {
+            if (threadIdx.x == 0 && p.status)
+                atomicOr(p.status, DSA_DEV_SCHEDULE);
+            return;
+        }
+        total_tiles = hdr[6];
+    } else {
+        SchedUnit* su = reinterpret_cast<SchedUnit*>(smem + mp.units);
+        int* scratch = reinterpret_cast<int*>(smem + mp.units + p.inline_units * 32);
+        total_tiles = build_inline_units(su, scratch, p.context_lens, p.batch, p.next_n, p.rows_per_unit,
+                                         p.row_begin, p.row_end, p.num_units,
+                                         blockIdx.x == 0 ? p.status : nullptr);
+        units = su;
     }
-    const int total_tiles = hdr[6];
     const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total_tiles) / gridDim.x);
     const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total_tiles) / gridDim.x);
     if (t0 >= t1 || p.num_units == 0)
@@ -699,8 +716,9 @@ dsa_status launch_mx4_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     const int budget = std::min(dev.max_smem_optin, 227 * 1024) - 1024;
     const int cstep = std::max(n_mma, n_grp);
     int raw_stages = 8, conv_stages = 4;
+    const int inline_units = a.sched ? 0 : a.num_units;
     auto fits = [&](int rs, int cs) {
-        return static_cast<int>(mx4_smem<D>(R, rs, cs, q_buf_bytes, w_cols).total) <= budget;
+        return static_cast<int>(mx4_smem<D>(R, rs, cs, q_buf_bytes, w_cols, inline_units).total) <= budget;
     };
     while (!fits(raw_stages, conv_stages) && raw_stages > 2)
         raw_stages -= 2;
@@ -708,7 +726,8 @@ dsa_status launch_mx4_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
         conv_stages -= cstep;
     if (!fits(raw_stages, conv_stages))
         return DSA_ERR_UNSUPPORTED;
-    const int smem_bytes = static_cast<int>(mx4_smem<D>(R, raw_stages, conv_stages, q_buf_bytes, w_cols).total) + 1024;
+    const int smem_bytes =
+        static_cast<int>(mx4_smem<D>(R, raw_stages, conv_stages, q_buf_bytes, w_cols, inline_units).total) + 1024;
 
     CUtensorMap tm_k;
     {
@@ -724,6 +743,9 @@ dsa_status launch_mx4_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     }
     Mx4Params p;
     p.sched = a.sched;
+    p.context_lens = a.context_lens;
+    p.batch = a.batch;
+    p.inline_units = inline_units;
     p.block_table = k->block_table;
     p.bt_stride = k->bt_row_stride;
     p.max_pages = k->max_pages_per_seq;

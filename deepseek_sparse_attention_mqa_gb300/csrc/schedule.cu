@@ -21,32 +21,6 @@ namespace {
 
 constexpr int kSchedThreads = 1024;
 
-// Unit u -> (sequence, first absolute row, rows) for rows [row_begin, row_end).
-__device__ __forceinline__ void unit_rows_of(int u, int next_n, int G, int row_begin, int row_end,
-                                             int* seq, int* first_row, int* nrows)
-{
-    const int b0 = row_begin / next_n;
-    const int lo0 = row_begin;
-    const int hi0 = min((b0 + 1) * next_n, row_end);
-    const int u_first = (hi0 - lo0 + G - 1) / G;
-    const int U = (next_n + G - 1) / G;  // units of a sequence fully inside the range
-    int b, lo, hi, j;
-    if (u < u_first) {
-        b = b0;
-        lo = lo0;
-        hi = hi0;
-        j = u;
-    } else {
-        b = b0 + 1 + (u - u_first) / U;
-        j = (u - u_first) % U;
-        lo = b * next_n;
-        hi = min((b + 1) * next_n, row_end);
-    }
-    *seq = b;
-    *first_row = lo + j * G;
-    *nrows = min(G, hi - *first_row);
-}
-
 __global__ void __launch_bounds__(kSchedThreads)
 build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int next_n, int G,
                       int row_begin, int row_end, int num_units, int32_t* __restrict__ sched,

@@ -66,7 +66,7 @@ class StepInputs:
 
 class SparseAttentionStep:
     def __init__(self, case: Case, with_mla: bool = True, budget_bytes: int = LOGITS_BUDGET_BYTES,
-                 rows_per_chunk: int | None = None):
+                 rows_per_chunk: int | None = None, inline_schedule: bool | None = None):
         dev = case.q.device
         assert dev.type == "cuda", "SparseAttentionStep needs the case on a CUDA device"
         self.case = case
@@ -82,6 +82,11 @@ class SparseAttentionStep:
         self.kcache = _abi.make_cache(kc.fmt, kc.head_dim, kc.page_kv, kc.num_pages, kc.values,
                                       kc.val_page_stride, kc.val_token_stride, kc.scales,
                                       kc.sc_page_stride, kc.sc_token_stride, c.block_table)
+        # a chunk of at most INLINE_UNITS units needs no schedule launch: the logits
+        # kernel builds its units itself (inline_schedule=False forces the buffer)
+        self.inline = {(rb, re): (inline_schedule is not False and
+                                  _abi.units_of(c.batch, c.next_n, c.num_heads, rb, re) <= _abi.INLINE_UNITS)
+                       for rb, re in self.chunks}
         sb = max(_abi.schedule_bytes(c.batch, c.next_n, c.num_heads, rb, re) for rb, re in self.chunks)
         self.sched = torch.empty((sb + 15) // 16 * 4, dtype=torch.int32, device=dev)
         self.logits = torch.empty((self.rows_per_chunk, max(1, self.width)), dtype=torch.float32,
@@ -106,11 +111,13 @@ class SparseAttentionStep:
     # ------------------------------------------------------------------ stages
     def indexer_chunk(self, rb: int, re: int, stream=None):
         c = self.case
-        _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, self.sched,
-                            self.status, stream)
+        inline = self.inline.get((rb, re), False)
+        if not inline:
+            _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, self.sched,
+                                self.status, stream)
         _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, self.kcache,
-                        c.context_lens, c.batch, c.next_n, rb, re, self.sched, self.logits,
-                        self.width, self.status, stream)
+                        c.context_lens, c.batch, c.next_n, rb, re, None if inline else self.sched,
+                        self.logits, self.width, self.status, stream)
 
     def topk_chunk(self, rb: int, re: int, stream=None):
         c = self.case
@@ -131,7 +138,7 @@ class SparseAttentionStep:
             self.mla(stream)
 
     def launches_per_step(self) -> int:
-        n = sum(3 for rb, re in self.chunks if re > rb)
+        n = sum(2 if self.inline.get((rb, re), False) else 3 for rb, re in self.chunks if re > rb)
         return n + (1 if self.with_mla else 0)
 
     def device_status(self) -> int:

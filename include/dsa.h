@@ -150,7 +150,10 @@ DSA_API dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int b
  * k:        the paged indexer K cache; FP8 caches carry k_scale per token,
  *           MXFP4 caches carry block scales only (k_scale = 1).
  * sched:    built by dsa_indexer_build_schedule() with the same batch, next_n,
- *           num_heads, row_begin, row_end (and current context_lens).
+ *           num_heads, row_begin, row_end (and current context_lens); or NULL
+ *           (sched_bytes ignored) for calls of at most 256 work units, whose
+ *           units the kernel then builds itself from context_lens (one launch
+ *           instead of two; larger calls without a schedule get DSA_ERR_CAPACITY).
  * logits:   fp32, row (r - row_begin) at logits + (r-row_begin)*logits_row_stride
  *           (ELEMENTS); logits_width = columns available per row.  A decode
  *           step under graph capture keeps a fixed width; a prefill sizes it to

@@ -110,3 +110,25 @@ def test_host_validation_rejects_before_any_gpu_call(L):
                                fake, fake, None, 0, None, None) == 2
     # device status read needs pointers
     assert L.dsa_get_device_status(None, None, None) == 1
+
+
+def test_inline_schedule_unit_limit_and_count():
+    """The Python unit count the step uses to choose the inline schedule agrees
+    with the library's schedule sizing, and a call without a schedule buffer over
+    256 work units is refused on the host before any pointer is touched."""
+    import ctypes
+    from deepseek_sparse_attention_mqa_gb300 import _abi
+    L = _abi.lib()
+    for args in [(64, 1, 64, 0, 64), (5, 3, 64, 0, 15), (1, 16384, 64, 0, 8192), (3, 4, 128, 2, 10),
+                 (128, 2, 32, 0, 256), (7, 3, 16, 4, 19), (300, 1, 64, 0, 300)]:
+        assert L.dsa_indexer_schedule_bytes(*args) == 32 + 32 * _abi.units_of(*args)
+    fake = ctypes.c_void_p(0x1000)
+    c = _abi.PagedCache()
+    c.fmt, c.head_dim, c.page_kv, c.num_pages = 0, 128, 64, 2000
+    c.values, c.scales, c.block_table = 0x1000, 0x2000, 0x3000
+    c.val_page_stride, c.val_token_stride = 64 * 128, 128
+    c.sc_page_stride, c.sc_token_stride = 256, 4
+    c.bt_row_stride, c.max_pages_per_seq = 2000, 2000
+    st = L.indexer_mqa_logits_paged(fake, None, 0, fake, 64, ctypes.byref(c), fake, 300, 1, 0, 300,
+                                    None, 0, fake, 4096, 4096, None, None)
+    assert st == _abi.DSA_ERR_CAPACITY

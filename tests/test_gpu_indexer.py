@@ -109,7 +109,7 @@ def test_prefill_chunked_causal():
 def test_schedule_buffer_contents():
     case = inputs.make_case("decode", device="cuda", lens=[0, 129, 5000, 128], next_n=2,
                             num_heads=64, width=5000, seed=9)
-    st = SparseAttentionStep(case, with_mla=False)
+    st = SparseAttentionStep(case, with_mla=False, inline_schedule=False)
     st.indexer_chunk(0, case.rows)
     torch.cuda.synchronize()
     s = st.sched.cpu().numpy()
@@ -135,7 +135,7 @@ def test_schedule_reused_across_launches():
     bit for bit."""
     for fmt_case in ("decode", "spec_mxfp4"):
         case = inputs.make_case(fmt_case, device="cuda", batch=9, seed=21)
-        st = SparseAttentionStep(case, with_mla=False)
+        st = SparseAttentionStep(case, with_mla=False, inline_schedule=False)
         st.indexer_chunk(0, case.rows)
         torch.cuda.synchronize()
         first = st.logits.clone()
@@ -149,6 +149,33 @@ def test_schedule_reused_across_launches():
             for r in range(c.rows):
                 v = parity.visible(case, r)
                 assert torch.equal(st.logits[r, :v], first[r, :v]), (fmt_case, rep, r)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("decode", dict(lens=[0, 1, 127, 128, 129, 4000, 70], width=4000)),
+    ("decode", dict(lens=[5, 300, 2049], next_n=3, num_heads=16, head_dim=64, page_kv=32, width=2100)),
+    ("decode", dict(lens=[900, 33], next_n=3, num_heads=128, width=900)),
+    ("decode", dict(batch=256, width=32768)),
+    ("spec_mxfp4", dict(batch=40)),
+])
+def test_inline_schedule_matches_prebuilt(name, over):
+    """Without a schedule buffer the logits kernel builds its units itself (one
+    launch instead of two); the logits are bit-identical to a launch on a
+    schedule built by the schedule kernel, up to the 256-unit limit."""
+    case = inputs.make_case(name, device="cuda", seed=41, with_mla=False, **over)
+    ref = SparseAttentionStep(case, with_mla=False, inline_schedule=False)
+    got = SparseAttentionStep(case, with_mla=False)
+    assert all(got.inline.values()) and not any(ref.inline.values())
+    assert got.launches_per_step() == 2 and ref.launches_per_step() == 3
+    for st in (ref, got):
+        st.logits.fill_(float("nan"))
+        st.indexer_chunk(0, case.rows)
+    torch.cuda.synchronize()
+    assert ref.device_status() == 0 and got.device_status() == 0
+    for r in range(case.rows):
+        v = parity.visible(case, r)
+        assert torch.equal(ref.logits[r, :v], got.logits[r, :v]), r
+        assert torch.isnan(got.logits[r, v:]).all(), r
 
 
 def test_packed_step_inputs_match():
