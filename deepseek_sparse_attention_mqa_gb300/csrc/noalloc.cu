@@ -71,6 +71,11 @@ extern "C" DSA_API dsa_status indexer_mqa_logits_paged_noalloc(
         return DSA_ERR_INVALID_ARG;
     if (need > kNoallocSchedBytes)
         return DSA_ERR_CAPACITY;             // too many work units for the fixed array
+    // small calls: the logits kernel builds its units itself (one launch, the array untouched)
+    if (need <= static_cast<size_t>(sched_bytes_for_units(kInlineUnits)))
+        return indexer_mqa_logits_paged(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n,
+                                        row_begin, row_end, nullptr, 0, logits, logits_row_stride, logits_width,
+                                        status_dev, stream);
     void* sched = nullptr;
     dsa_status st = scratch_address(&sched);
     if (st != DSA_OK)

@@ -75,6 +75,19 @@ def test_two_calls_in_a_row_match_the_regular_entry_point():
         check_same(case, ref, got)
 
 
+def test_over_256_units_use_the_fixed_array():
+    # 300 sequences: more units than the logits kernel builds itself, so the
+    # schedule goes through the library's fixed array; then a small call (inline
+    # schedule) and the large one again
+    big = inputs.make_case("decode", device="cuda", lens=[(i * 37) % 600 + 1 for i in range(300)], width=640,
+                           seed=74)
+    small = inputs.make_case("decode", device="cuda", lens=[700, 3], width=704, seed=75)
+    assert _abi.units_of(big.batch, big.next_n, big.num_heads, 0, big.rows) > _abi.INLINE_UNITS
+    for case in (big, small, big):
+        ref, st = regular_logits(case)
+        check_same(case, ref, noalloc_logits(case, st))
+
+
 def test_mxfp4_through_the_noalloc_entry_point():
     case = inputs.make_case("spec_mxfp4", device="cuda", lens=[0, 1, 33, 700, 64, 2049],
                             width=2048 + 64, seed=73)
