@@ -24,7 +24,7 @@
  *  - The indexer score itself (DeepSeek sparse attention, lightning indexer):
  *        logit[r, s] = k_scale[s] * sum_h w[r, h] * relu( sum_d q[r, h, d] * k[s, d] )
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - visible length of draft row i of a sequence with context length L and
  *    next_n rows: clamp(L - next_n + i + 1, 0, L) (context length includes the
  *    next_n new tokens, bound inclusive);
