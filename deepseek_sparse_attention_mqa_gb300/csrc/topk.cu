@@ -19,8 +19,9 @@
 //  3. every position above that bin is written out directly (cluster-wide
 //     counter); the bin's few elements are appended to CTA 0 as candidates;
 //  4. CTA 0 resolves the candidates exactly by the 64-bit order (key, then lower
-//     position), the same order as a full sort with ties broken by position,
-//     with a parallel radix selection (11-bit digits, block-wide scans).
+//     position), the same order as a full sort with ties broken by position:
+//     by ranking each candidate against the others when there are at most 256,
+//     else with a parallel radix selection (11-bit digits, block-wide scans).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -34,6 +35,7 @@ constexpr int kThreads = 512;
 constexpr int kBins = 2048;
 constexpr int kBinBits = 11;
 constexpr int kCandCap = 4096;      // threshold-bin candidates collected in CTA 0
+constexpr int kRankSelectMax = 256; // up to this many candidates are selected by direct ranking
 constexpr int kSliceCap = 16384;    // keys per CTA kept in shared memory (64 KB)
 constexpr int kMaxCluster = 8;
 
@@ -330,12 +332,25 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     // histogram; it stops as soon as the chosen digit's bin holds exactly the
     // number still needed (then every candidate matching the prefix is in).
     const int cand_total = sh.ncand;
-    if (cand_total <= kCandCap) {
+    auto cand_order = [&](int j) -> uint64_t {
+        return (static_cast<uint64_t>(sh.ck[j] - lo) << 32) |
+               static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(sh.cp[j]));
+    };
+    if (cand_total <= kRankSelectMax) {
+        // Few candidates (the usual case: the threshold bin of a decode row holds
+        // tens of keys): each thread ranks one candidate against all of them by
+        // the same 64-bit order (unique: positions differ), and the `need` best
+        // go straight to their slots -- no radix rounds, no block barriers.
+        for (int t = tid; t < cand_total; t += kThreads) {
+            const uint64_t ot = cand_order(t);
+            int rank = 0;
+            for (int j = 0; j < cand_total; ++j)
+                rank += cand_order(j) > ot ? 1 : 0;
+            if (rank < need)
+                out[n_direct + rank] = sh.cp[t];
+        }
+    } else if (cand_total <= kCandCap) {
         const int key_bits = log2_ceil_u64(static_cast<uint64_t>(hi - lo) + 1);
-        auto cand_order = [&](int j) -> uint64_t {
-            return (static_cast<uint64_t>(sh.ck[j] - lo) << 32) |
-                   static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(sh.cp[j]));
-        };
         uint64_t prefix = 0;
         int rem = need;
         int top = 32 + key_bits;                          // bits [0, top) still undecided
