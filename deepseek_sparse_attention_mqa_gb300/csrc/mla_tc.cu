@@ -11,9 +11,10 @@
 // (128 heads x 512 fp32) fills a whole TMEM, so it is split by value dims:
 // CTA c owns latent dims [256 c, 256 c + 256) and, at d_qk 576, half of the
 // rope dims, [512 + 32 c, 544 + 32 c), so both do equal work; each keeps its
-// part of Q resident (f16, swizzled K-major, times a per-head power of two that
-// fits it to f16 range exactly), gathers and widens its part of the selected
-// latent rows (FP8 -> f16, exact) and computes a PARTIAL score
+// part of Q resident (f16, times a per-head power of two that fits it to f16
+// range exactly: the 256 value dims in TMEM as the A operand of the QK MMA,
+// the rope dims in a swizzled K-major shared-memory tile), gathers and widens
+// its part of the selected latent rows (FP8 -> f16, exact) and computes a PARTIAL score
 // S_c = Q_c K_c^T on the tensor cores.  The two partials are exchanged through
 // distributed shared memory, so both CTAs hold the same S = S_0 + S_1 (identical
 // arithmetic, hence identical softmax decisions) and each accumulates its half
@@ -31,8 +32,9 @@
 //              (token scale folded in for V; f16 rather than bf16 keeps its
 //              rounding at 2^-12); at the end O is normalised and stored as
 //              bf16 out / fp32 lse.
-//   warps 4-7  gather: per 64-token block, look up each selected token through
-//              the block table (two blocks ahead), load its FP8 slice (the
+//   warps 4-7  gather, three latent tiles in flight: per 64-token block, look
+//              up each selected token through the block table (two blocks
+//              ahead), load its FP8 slice (the
 //              next block's loads are issued before this block's widening
 //              stores), widen to f16 into a 128B-swizzled K-major tile (zeros
 //              for unused slots).
@@ -61,7 +63,9 @@ constexpr int kThreads = 416;           // 13 warps
 constexpr int kConvWarp0 = 4;           // gather warps 4-7
 constexpr int kMmaWarp = 8;
 constexpr int kSoftWarp1 = 9;           // softmax warps 0-3 (tokens 0-31) and 9-12 (tokens 32-63)
-constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, O at 256
+constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, Q (value dims, f16 pairs) at 128, O at 256
+constexpr uint32_t kQCol = 128;
+constexpr int kLatBufs = 3;             // latent tiles (with their scales and valid flags) in flight
 constexpr float kRescaleLog2 = 8.f;     // refresh the running max only past 2^8
 constexpr int kMaxSeg = 18;             // 16-byte FP8 segments per token and CTA (256 + 32 dims)
 constexpr int kGatherItems = (16 * kMaxSeg + 31) / 32;      // 16-byte segments per gather lane
@@ -98,12 +102,12 @@ __host__ __device__ constexpr MlaSmem mla_smem()
 {
     MlaSmem m{};
     m.q = 0;
-    m.lat = m.q + kMaxChunks * kQChunkBytes;
-    m.p = m.lat + 2 * kMaxChunks * kLChunkBytes;
+    m.lat = m.q + kQChunkBytes;                      // the rope chunk of Q (value dims are in TMEM)
+    m.p = m.lat + kLatBufs * kMaxChunks * kLChunkBytes;
     m.x = m.p + 128 * 128;
     m.scale = m.x + 128 * kNT * 4;
-    m.valid = m.scale + 2 * kNT * 4;
-    m.qexp = m.valid + 2 * kNT * 4;
+    m.valid = m.scale + kLatBufs * kNT * 4;
+    m.qexp = m.valid + kLatBufs * kNT * 4;
     m.red = m.qexp + 128 * 4;
     m.bar = m.red + 2 * 2 * 128 * 4;
     m.misc = m.bar + 24 * 8;
@@ -152,16 +156,16 @@ sparse_mla_tc_kernel(const MlaParams p)
     float* sSum = sMax + 2 * 128;                                  // [2][128] final sum per half
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + mp.bar);
     uint64_t* q_full = bars + 0;
-    uint64_t* lat_full = bars + 1;   // [2]
-    uint64_t* lat_empty = bars + 3;  // [2]
-    uint64_t* s_full = bars + 5;     // [2]
-    uint64_t* s_empty = bars + 7;    // [2]
-    uint64_t* x_full = bars + 9;     // peer's partial scores arrived in sX
-    uint64_t* x_free = bars + 10;    // peer consumed what this CTA wrote
-    uint64_t* p_full = bars + 11;
-    uint64_t* p_empty = bars + 12;
-    uint64_t* o_done = bars + 13;
-    uint64_t* pair_bar = bars + 14;  // [4] the two softmax warps of a lane quarter
+    uint64_t* lat_full = bars + 1;   // [kLatBufs]
+    uint64_t* lat_empty = bars + 4;  // [kLatBufs]
+    uint64_t* s_full = bars + 7;     // [2]
+    uint64_t* s_empty = bars + 9;    // [2]
+    uint64_t* x_full = bars + 11;    // peer's partial scores arrived in sX
+    uint64_t* x_free = bars + 12;    // peer consumed what this CTA wrote
+    uint64_t* p_full = bars + 13;
+    uint64_t* p_empty = bars + 14;
+    uint64_t* o_done = bars + 15;
+    uint64_t* pair_bar = bars + 16;  // [4] the two softmax warps of a lane quarter
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc + 4);
 
@@ -186,9 +190,11 @@ sparse_mla_tc_kernel(const MlaParams p)
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(q_full), 4);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kLatBufs; ++i) {
             mbar_init(smem_u32(&lat_full[i]), 4);
             mbar_init(smem_u32(&lat_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
             mbar_init(smem_u32(&s_empty[i]), 8);
         }
@@ -245,7 +251,7 @@ sparse_mla_tc_kernel(const MlaParams p)
             }
             sQexp[h] = e;
             const float sc = exp2_int(e);
-            for (int u = 0; u < nunit; ++u) {
+            auto conv = [&](int u) -> uint4 {              // 8 dims of unit u, f16 x 2^e
                 uint4 o = make_uint4(0, 0, 0, 0);
                 if (h < p.num_heads) {
                     const uint4 v = *reinterpret_cast<const uint4*>(qh + qdim(u));
@@ -259,10 +265,31 @@ sparse_mla_tc_kernel(const MlaParams p)
                     }
                     o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
                 }
-                *reinterpret_cast<uint4*>(sQ + (u >> 3) * kQChunkBytes + swizzled_offset(h, u & 7, 128)) = o;
+                return o;
+            };
+            // the 256 value dims go to TMEM lane h (this warp's lane quarter),
+            // columns [kQCol, kQCol + 128): 32 columns (8 units) per store
+            const uint32_t q_lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+#pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+                uint32_t wv[32];
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const uint4 o = conv(8 * r + b);
+                    wv[4 * b] = o.x;
+                    wv[4 * b + 1] = o.y;
+                    wv[4 * b + 2] = o.z;
+                    wv[4 * b + 3] = o.w;
+                }
+                tmem_st_32x32b_x32(tmem_base + q_lane + kQCol + 32 * r, wv);
             }
+            tmem_st_wait();
+            // the rope dims (d_qk 576) go to the shared-memory chunk
+            for (int u = 32; u < nunit; ++u)
+                *reinterpret_cast<uint4*>(sQ + swizzled_offset(h, u - 32, 128)) = conv(u);
         }
         fence_proxy_async_smem();
+        tc_fence_before_sync();
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(q_full));
@@ -330,8 +357,8 @@ sparse_mla_tc_kernel(const MlaParams p)
         issue_loads(raw, off0, valid0);
         float scale0 = load_scale(soff0, valid0);
         for (int j = 0; j < nblk && !__any_sync(0xffffffffu, *s_abort); ++j) {
-            const int st = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_empty[st]), ((j >> 1) & 1) ^ 1))) {
+            const int st = j % kLatBufs;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_empty[st]), ((j / kLatBufs) & 1) ^ 1))) {
                 *s_abort = 1;
                 break;
             }
@@ -392,16 +419,21 @@ sparse_mla_tc_kernel(const MlaParams p)
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(st * kNT);
                 const uint32_t qa = smem_u32(sQ);
-                const uint32_t kb = smem_u32(sLat + st * (kMaxChunks * kLChunkBytes));
+                const uint32_t kb = smem_u32(sLat + (j % kLatBufs) * (kMaxChunks * kLChunkBytes));
                 for (int ch = 0; ch < nchunk; ++ch) {
                     const int nks = ch < kVChunks ? 4 : 2;       // the rope chunk holds 32 dims
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         if (ks >= nks)
                             break;
-                        const uint64_t ad = make_smem_desc(qa + ch * kQChunkBytes + ks * 32, 16, 1024, kLayoutSw128);
                         const uint64_t bd = make_smem_desc(kb + ch * kLChunkBytes + ks * 32, 16, 1024, kLayoutSw128);
-                        umma_f16(d, ad, bd, idesc_qk, (ch | ks) != 0 ? 1u : 0u);
+                        if (ch < kVChunks) {
+                            // value dims: A = Q from TMEM (16 K elements = 8 columns per step)
+                            umma_f16_ts(d, tmem_base + kQCol + ch * 32 + ks * 8, bd, idesc_qk, (ch | ks) != 0 ? 1u : 0u);
+                        } else {
+                            const uint64_t ad = make_smem_desc(qa + ks * 32, 16, 1024, kLayoutSw128);
+                            umma_f16(d, ad, bd, idesc_qk, 1u);
+                        }
                     }
                 }
                 umma_commit(smem_u32(&s_full[st]));
@@ -413,7 +445,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                 // 8-token groups 1 KB apart = SBO)
                 const uint32_t d = tmem_base + 256;
                 const uint32_t pa = smem_u32(sP);
-                const uint32_t vb = smem_u32(sLat + (j & 1) * (kMaxChunks * kLChunkBytes));
+                const uint32_t vb = smem_u32(sLat + (j % kLatBufs) * (kMaxChunks * kLChunkBytes));
 #pragma unroll
                 for (int ks = 0; ks < kNT / 16; ++ks) {
                     const uint64_t ad = make_smem_desc(pa + ks * 32, 16, 1024, kLayoutSw128);
@@ -421,14 +453,14 @@ sparse_mla_tc_kernel(const MlaParams p)
                     umma_f16(d, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(smem_u32(p_empty));
-                umma_commit(smem_u32(&lat_empty[j & 1]));
+                umma_commit(smem_u32(&lat_empty[j % kLatBufs]));
             };
             int jq = 0, jp = 0;                         // next QK / PV block to issue
             uint64_t t_idle = 0;
             while (ok && jp < nblk && !*s_abort) {
                 bool progress = false;
                 // QK(jq): its latent block is gathered and S buffer jq & 1 was read
-                if (jq < nblk && mbar_test_wait(smem_u32(&lat_full[jq & 1]), (jq >> 1) & 1) &&
+                if (jq < nblk && mbar_test_wait(smem_u32(&lat_full[jq % kLatBufs]), (jq / kLatBufs) & 1) &&
                     mbar_test_wait(smem_u32(&s_empty[jq & 1]), ((jq >> 1) & 1) ^ 1)) {
                     issue_qk(jq++);
                     progress = true;
@@ -548,12 +580,13 @@ sparse_mla_tc_kernel(const MlaParams p)
                 mbar_arrive_remote_relaxed(peer_x_free);
 
             // ---- scores in base 2; masked slots are -inf
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_full[sb]), ph))) {
+            const int lb = j % kLatBufs;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_full[lb]), (j / kLatBufs) & 1))) {
                 ok = false;
                 break;
             }
-            const float* scl = sScale + sb * kNT + tcol;
-            const int* vld = sValid + sb * kNT + tcol;
+            const float* scl = sScale + lb * kNT + tcol;
+            const int* vld = sValid + lb * kNT + tcol;
             float m_half = -INFINITY;
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
