@@ -115,6 +115,19 @@ __host__ __device__ constexpr MlaSmem mla_smem()
     return m;
 }
 
+// tcgen05.mma kind::f16 with the A operand in tensor memory (lane = row of A,
+// two 16-bit K elements per 32-bit column; one K step of 16 = 8 columns).
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // 16 e4m3 bytes -> 16 f16 (exact: every e4m3 value is an f16 value).
 __device__ __forceinline__ void e4m3x16_to_f16x16(const uint4 v, uint4& lo, uint4& hi)
 {
