@@ -7,18 +7,19 @@
 // straddles two non-contiguous pages (BLOCK_KV = min(PAGE_KV, 64)), several
 // TMA warps each owning a KV group, 2-3 stages to fit SM120's 99 KiB.
 //
-// GB300 design (one persistent CTA per SM, warp-specialised).  Every role walks
-// the CTA's 128-token tiles in order; tile j (CTA-local ordinal) lives in stage
-// j % stages and accumulator j % n_acc.  Each role is split over several warps
-// that take tiles round-robin, because on this part a single thread's chain of
-// barrier waits, copy or MMA issues and commits per tile costs more than the
-// tile's HBM time:
-//   warps 0-3   TMA producers (tile j -> warp j % 4): per tile, one 3-D box per
-//               physical page (2 at page 64, 4 at page 32, one lane each) into a
-//               128B/64B/32B-swizzled K-major stage, and the per-token fp32
-//               scales with one 16-byte cp.async per lane; warp 0 also loads
-//               each unit's q rows ([rows x heads, D], K-major).
-//   warps 4-5   single-thread tcgen05.mma issuers (tile j -> warp j % 2),
+// GB300 design (one persistent CTA per SM, warp-specialised).  The CTA takes an
+// equal share of the 128-token tiles and walks it in super-tiles: up to R
+// consecutive tiles of one unit (R = 4 at D = 128 and 64 heads, so a stage holds
+// up to 64 KB of K and two super-tile accumulators fit in TMEM).  Super-tile j
+// (CTA-local ordinal) lives in stage j % stages and accumulator j % n_acc.  Each
+// role is split over several warps, because on this part a single thread's chain
+// of barrier waits, copy or MMA issues and commits costs more than a tile's HBM
+// time:
+//   warps 0-3   TMA producers, all on every super-tile: one 3-D box per physical
+//               page (lane i of warp w copies page w + 4i) into a 128B/64B/32B-
+//               swizzled K-major stage, and the per-token fp32 scales with one
+//               16-byte cp.async per lane.
+//   warps 4-5   single-thread tcgen05.mma issuers (super-tile j -> warp j % 2),
 //               kind::f8f6f4: D[128 tokens x N] += K_tile[128 x D] * Q[N x D]^T,
 //               N = rows x heads; each TMEM lane is one token and each column
 //               one (row, head).  Warp 4 also owns the TMEM allocation.
@@ -29,8 +30,10 @@
 //               head-weighting / k_scale reduction is thread-local (no
 //               shuffles, rows of a unit past its last row skipped), and each
 //               warp stores 32 consecutive logits per row.
-//   Up to eight TMEM accumulators let the epilogues of earlier tiles overlap the
-//   MMAs of later ones; the stage ring keeps K bytes in flight.
+//   Up to eight TMEM accumulators let the epilogues of earlier super-tiles
+//   overlap the MMAs of later ones; the stage ring keeps K bytes in flight.
+//   Without a schedule buffer (at most kInlineUnits units) every CTA first
+//   builds the unit records in shared memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
