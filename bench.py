@@ -155,6 +155,22 @@ def logits_algorithmic_bytes(case):
     return kv + q + w + out + bt
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values of `x` (the job takes as long as its
+    slowest replica); the value itself on one rank."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(pairs_per_replica: float, world: int, ms_per_step: float) -> float:
+    """K-tokens scored per second over all replicas, each scoring the same
+    workload in `ms_per_step` (the max over ranks)."""
+    return pairs_per_replica * world / (ms_per_step * 1e-3) / 1e3
+
+
 def run_ours(args, rank, world, local):
     from deepseek_sparse_attention_mqa_gb300 import _abi, build, inputs
     from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
@@ -220,13 +236,9 @@ def run_ours(args, rank, world, local):
     sched_ms = [sum((e[3 * ci] if ci else e[0]).elapsed_time(e[3 * ci + 1]) for ci in range(nck)) for e in ev]
     logits_ms = [sum(e[3 * ci + 1].elapsed_time(e[3 * ci + 2]) for ci in range(nck)) for e in ev]
     topk_ms = [sum(e[3 * ci + 2].elapsed_time(e[3 * ci + 3]) for ci in range(nck)) for e in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = pairs * world / (ms_per_step * 1e-3) / 1e3
+    value = whole_job_value(pairs, world, ms_per_step)
 
     clocks = sampler.summary(t_begin, t_end) if sampler else None
     if sampler:
