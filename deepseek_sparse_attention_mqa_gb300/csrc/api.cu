@@ -166,7 +166,7 @@ const char* dsa_status_string(dsa_status s)
 
 int dsa_last_cuda_error(void) { return g_last_cuda_error; }
 
-int dsa_version(void) { return 100; }
+int dsa_version(void) { return 101; }
 
 size_t dsa_indexer_schedule_bytes(int batch, int next_n, int num_heads, int row_begin, int row_end)
 {

@@ -103,7 +103,8 @@ DSA_API const char* dsa_status_string(dsa_status status);
 /* cudaError_t of the last failed CUDA call made by this thread (0 = none). */
 DSA_API int dsa_last_cuda_error(void);
 
-/* Library ABI version (major*100 + minor). */
+/* Library ABI version (major*100 + minor).  1.01: indexer_mqa_logits_paged
+ * accepts sched = NULL for calls of at most 256 work units. */
 DSA_API int dsa_version(void);
 
 /*
