@@ -14,6 +14,9 @@ paged MQA logits + top-k (3 libdsa launches).  Reported:
                inside the timed region (the K cache is device-resident state);
 * roofline     the logits kernel: algorithmic bytes per launch / its event time
                vs the measured HBM copy bandwidth;
+* spec_mxfp4, prefill  the speculative/varlen MXFP4 and the causal prefill
+               indexer configurations timed the same way (their own value,
+               kernel times and roofline: HBM for MXFP4, FP8 tensor for prefill);
 * full_step    the whole graph-captured step of the full decode workload
                (indexer + top-k + sparse MLA, 128 heads 576/512) in us/step,
                with each stage also timed alone and the sparse MLA's tensor
@@ -47,6 +50,14 @@ METRIC = "indexer K-tokens scored/s & HBM GB/s (%roofline); sparse-attn decode Â
 UNIT = "K-tokens/s"
 WORKLOAD = ("decode indexer + top-k: batch 64, next_n 1, 64 heads, head_dim 128, page 64, "
             "FP8 e4m3 K cache with fp32 token scale, lens U[4096,32768], 2x shuffled pool, top-k 2048")
+WORKLOADS = {
+    "decode": WORKLOAD,
+    "spec_mxfp4": ("speculative/varlen indexer + top-k: batch 128, next_n 2, 32 heads, head_dim 64, "
+                   "page 32, MXFP4 K cache and q in a padded-stride layout, lens log-uniform in "
+                   "[0, 65536] with empty/partial-page edge lengths, top-k 512"),
+    "prefill": ("prefill indexer + top-k: one causal sequence of 16384 tokens, 64 heads, head_dim 128, "
+                "page 64, FP8 e4m3, logits width 16384, two 8192-row chunks (512 MiB budget), top-k 2048"),
+}
 
 
 def dist_env():
@@ -171,6 +182,109 @@ def whole_job_value(pairs_per_replica: float, world: int, ms_per_step: float) ->
     return pairs_per_replica * world / (ms_per_step * 1e-3) / 1e3
 
 
+class L2Flush:
+    """Evicts L2 (129 MB) between timed steps by READING a 384 MiB buffer (a
+    reduction into one preallocated word): no dirty lines are left behind to be
+    written back inside the next timed kernel.  At ~60 us of GPU time per flush
+    it also keeps the GPU queue ahead of the host, so events time kernels, not
+    host launch gaps."""
+
+    BYTES = 384 * 2 ** 20
+
+    def __init__(self, dev):
+        self.buf = torch.ones(self.BYTES // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def __call__(self, step=0):
+        torch.sum(self.buf, dim=0, out=self.acc)
+
+
+def time_indexer_steps(st, steps, flush, stream, fused=False):
+    """Event-timed indexer steps (schedule if any, logits, top-k per chunk), L2
+    flushed before each; returns per-step lists of ms."""
+    from deepseek_sparse_attention_mqa_gb300 import _abi
+    c = st.case
+    chunks = [(rb, re) for rb, re in st.chunks if re > rb]
+    nck = len(chunks)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * nck + 1)] for _ in range(steps)]
+    for s in range(steps):
+        flush(s)
+        e = ev[s]
+        e[0].record(stream)
+        for ci, (rb, re) in enumerate(chunks):
+            inline = st.inline[(rb, re)]          # no schedule launch: the logits kernel builds the units
+            if not inline:
+                _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status)
+            e[3 * ci + 1].record(stream)
+            _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
+                            c.batch, c.next_n, rb, re, None if inline else st.sched, st.logits, st.width,
+                            st.status)
+            e[3 * ci + 2].record(stream)
+            st.topk_chunk(rb, re)
+            e[3 * ci + 3].record(stream)
+    torch.cuda.synchronize()
+    return {
+        "step": [e[0].elapsed_time(e[-1]) for e in ev],
+        "schedule": [sum((e[3 * ci] if ci else e[0]).elapsed_time(e[3 * ci + 1]) for ci in range(nck)) for e in ev],
+        "logits": [sum(e[3 * ci + 1].elapsed_time(e[3 * ci + 2]) for ci in range(nck)) for e in ev],
+        "topk": [sum(e[3 * ci + 2].elapsed_time(e[3 * ci + 3]) for ci in range(nck)) for e in ev],
+        "chunks": nck,
+    }
+
+
+def logits_roofline(case, workload, logits_ms_per_launch, nck):
+    """Roofline of the logits kernel: HBM bytes for the decode-type workloads,
+    FP8 tensor flops for the prefill (compute-bound) workload."""
+    from deepseek_sparse_attention_mqa_gb300 import inputs
+    hbm, bf16, _, src = measured_peaks()
+    pairs = scored_pairs(case)
+    if workload == "prefill":
+        # FP8 MMA work per launch (one chunk): 2 * pairs * heads * head_dim
+        flops = 2.0 * pairs * case.num_heads * case.head_dim / nck
+        achieved = flops / (logits_ms_per_launch * 1e-3) / 1e12
+        fp8_peak = 2.0 * bf16                             # nominal fp8 : bf16 = 2 : 1
+        return {"kernel": "logits_fp8 (indexer_mqa_logits_paged), per chunk launch", "bound": "tensor",
+                "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / fp8_peak, 4),
+                "peak_source": src + " bf16 burst x 2 (nominal fp8/bf16 ratio)",
+                "algorithmic_flops": flops, "traffic": load_traffic("logits_fp8", workload)}
+    lg_bytes = logits_algorithmic_bytes(case) / nck
+    achieved = lg_bytes / (logits_ms_per_launch * 1e-3) / 1e9
+    kname = "logits_fp8" if case.fmt == inputs.FMT_FP8 else "logits_mxfp4"
+    return {"kernel": kname + " (indexer_mqa_logits_paged)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_source": src,
+            "algorithmic_bytes": lg_bytes, "traffic": load_traffic(kname, workload)}
+
+
+def measure_indexer_config(workload, dev, steps, flush):
+    """One indexer configuration timed on its own (spec_mxfp4, prefill): the
+    configuration's value, per-kernel times and the logits roofline."""
+    from deepseek_sparse_attention_mqa_gb300 import inputs
+    from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
+    case = inputs.make_case(workload, device=dev)
+    st = SparseAttentionStep(case, with_mla=False)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        st.run()
+    torch.cuda.synchronize()
+    status = st.device_status()
+    t = time_indexer_steps(st, steps, flush, stream)
+    pairs = scored_pairs(case)
+    ms = statistics.mean(t["step"])
+    nck = t["chunks"]
+    res = {"workload": WORKLOADS[workload], "value": round(pairs / (ms * 1e-3) / 1e3, 1), "unit": UNIT,
+           "ms_per_step": round(ms, 5), "steps": steps, "scored_pairs_per_step": pairs,
+           "kernel_ms": {"schedule": round(statistics.mean(t["schedule"]), 5),
+                         "logits": round(statistics.mean(t["logits"]), 5),
+                         "topk": round(statistics.mean(t["topk"]), 5), "chunks": nck},
+           "roofline": logits_roofline(case, workload, statistics.mean(t["logits"]) / nck, nck),
+           "gpu_launches_per_step": st.launches_per_step(), "device_status": status}
+    del st, case
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local):
     from deepseek_sparse_attention_mqa_gb300 import _abi, build, inputs
     from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
@@ -189,10 +303,7 @@ def run_ours(args, rank, world, local):
     case = inputs.make_case(args.workload, device=dev)
     st = SparseAttentionStep(case, with_mla=False)
     pairs = scored_pairs(case)
-    # 1 GiB write between steps: evicts L2 (129 MB) and, at ~170 us of GPU time,
-    # keeps the GPU queue ahead of the host so that events time kernels, not
-    # host-side launch gaps
-    flush = torch.empty(int(2 ** 30) // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -202,9 +313,6 @@ def run_ours(args, rank, world, local):
     if status != 0:
         raise RuntimeError("device status %#x after warm-up" % status)
 
-    chunks = [(rb, re) for rb, re in st.chunks if re > rb]
-    nck = len(chunks)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * nck + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.wait_first()
@@ -212,31 +320,12 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_begin = time.time()
-    c = st.case
-    for s in range(args.steps):
-        flush.fill_(float(s))                    # evict L2 between steps
-        e = ev[s]
-        e[0].record(stream)
-        for ci, (rb, re) in enumerate(chunks):
-            inline = st.inline[(rb, re)]          # no schedule launch: the logits kernel builds the units
-            if not inline:
-                _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status)
-            e[3 * ci + 1].record(stream)
-            _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
-                            c.batch, c.next_n, rb, re, None if inline else st.sched, st.logits, st.width,
-                            st.status)
-            e[3 * ci + 2].record(stream)
-            st.topk_chunk(rb, re)
-            e[3 * ci + 3].record(stream)
-    torch.cuda.synchronize()
+    t = time_indexer_steps(st, args.steps, flush, stream)
     t_end = time.time()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
-    sched_ms = [sum((e[3 * ci] if ci else e[0]).elapsed_time(e[3 * ci + 1]) for ci in range(nck)) for e in ev]
-    logits_ms = [sum(e[3 * ci + 1].elapsed_time(e[3 * ci + 2]) for ci in range(nck)) for e in ev]
-    topk_ms = [sum(e[3 * ci + 2].elapsed_time(e[3 * ci + 3]) for ci in range(nck)) for e in ev]
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    nck = t["chunks"]
+    total_ms = max_over_ranks(sum(t["step"]), world, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_value(pairs, world, ms_per_step)
 
@@ -244,54 +333,41 @@ def run_ours(args, rank, world, local):
     if sampler:
         sampler.stop()
 
-    # ---- end to end through the public step API, host buffers
-    e2e = None
-    if rank == 0:
-        e2e = measure_e2e(st, case, args, pairs, dev)
-
     result = None
     if rank == 0:
-        hbm, bf16, bf16s, src = measured_peaks()
-        lg_ms = statistics.mean(logits_ms) / nck            # per launch
-        if args.workload == "prefill":
-            # FP8 MMA work per launch (one chunk): 2 * pairs * heads * head_dim
-            flops = 2.0 * pairs * case.num_heads * case.head_dim / nck
-            achieved = flops / (lg_ms * 1e-3) / 1e12
-            fp8_peak = 2.0 * bf16                             # nominal fp8 : bf16 = 2 : 1
-            roof = {"kernel": "logits_fp8 (indexer_mqa_logits_paged), per chunk launch", "bound": "tensor",
-                    "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(achieved / fp8_peak, 4),
-                    "peak_source": src + " bf16 burst x 2 (nominal fp8/bf16 ratio)",
-                    "algorithmic_flops": flops, "traffic": load_traffic("logits_fp8", args.workload)}
-        else:
-            lg_bytes = logits_algorithmic_bytes(case) / nck
-            achieved = lg_bytes / (lg_ms * 1e-3) / 1e9
-            kname = "logits_fp8" if case.fmt == inputs.FMT_FP8 else "logits_mxfp4"
-            roof = {"kernel": kname + " (indexer_mqa_logits_paged)", "bound": "hbm",
-                    "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(achieved / hbm, 4), "peak_source": src,
-                    "algorithmic_bytes": lg_bytes, "traffic": load_traffic(kname, args.workload)}
-        full = None if args.skip_full_step else measure_full_step(dev, args)
-        full64 = None if args.skip_full_step else measure_full_step(dev, args, "full_step_h64")
+        # the same steps with the former flush (a 1 GiB WRITE), once, for comparison:
+        # its dirty lines are written back inside the timed logits kernel
+        wbuf = torch.empty(int(2 ** 30) // 4, dtype=torch.float32, device=dev)
+        tw = time_indexer_steps(st, max(10, min(200, args.steps)), lambda s: wbuf.fill_(float(s)), stream)
+        del wbuf
+        e2e = measure_e2e(st, case, args, pairs, dev)
+        roof = logits_roofline(case, args.workload, statistics.mean(t["logits"]) / nck, nck)
         result = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3" if case.fmt == inputs.FMT_FP8 else "e2m1", "data": "synthetic",
-            "config": {"workload": WORKLOAD if args.workload == "decode" else args.workload, "batch": case.batch, "next_n": case.next_n,
-                       "heads": case.num_heads, "head_dim": case.head_dim, "page_kv": case.page_kv,
-                       "topk": case.topk, "scored_pairs_per_step": pairs, "seed": case.meta["seed"],
-                       "l2": "flushed between steps (1 GiB write)", "parallelism": "replicas"},
-            "kernel_ms": {"schedule": round(statistics.mean(sched_ms), 5),
-                          "logits": round(statistics.mean(logits_ms), 5),
-                          "topk": round(statistics.mean(topk_ms), 5), "chunks": nck},
+            "config": {"workload": WORKLOADS.get(args.workload, args.workload), "batch": case.batch,
+                       "next_n": case.next_n, "heads": case.num_heads, "head_dim": case.head_dim,
+                       "page_kv": case.page_kv, "topk": case.topk, "scored_pairs_per_step": pairs,
+                       "seed": case.meta["seed"], "l2": "flushed between steps (384 MiB read)",
+                       "parallelism": "replicas"},
+            "kernel_ms": {"schedule": round(statistics.mean(t["schedule"]), 5),
+                          "logits": round(statistics.mean(t["logits"]), 5),
+                          "topk": round(statistics.mean(t["topk"]), 5), "chunks": nck,
+                          "logits_after_write_flush": round(statistics.mean(tw["logits"]), 5)},
             "roofline": roof,
             "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clocks,
             "e2e": e2e,
-            "full_step": full,
-            "full_step_indexer_h64": full64,
         }
+        if args.workload == "decode" and not args.skip_configs:
+            n_sub = max(10, min(200, args.steps))
+            result["spec_mxfp4"] = measure_indexer_config("spec_mxfp4", dev, n_sub, flush)
+            result["prefill"] = measure_indexer_config("prefill", dev, max(5, min(20, args.steps)), flush)
+        if not args.skip_full_step:
+            result["full_step"] = measure_full_step(dev, args, flush)
+            result["full_step_indexer_h64"] = measure_full_step(dev, args, flush, "full_step_h64")
         if not args.skip_cpu:
             result["cpu_baseline"] = cpu_baseline(case, pairs)
     if world > 1:
@@ -340,10 +416,10 @@ def measure_e2e(st, case, args, pairs, dev):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    flush = torch.empty(int(256 * 2 ** 20) // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     tot = 0.0
     for s in range(steps):
-        flush.fill_(float(s))
+        flush(s)
         e0.record(stream)
         ins.copy_in(stream)
         st.run()
@@ -356,7 +432,7 @@ def measure_e2e(st, case, args, pairs, dev):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
-def measure_full_step(dev, args, workload="full_step"):
+def measure_full_step(dev, args, flush, workload="full_step"):
     """Full decode step (indexer, top-k, sparse MLA 128 heads 576/512 on an FP8
     latent, lens U[8192,131072], top-k 2048) captured in one CUDA graph; us/step
     over replays, L2 flushed.  Also times each stage alone (eager launches,
@@ -375,12 +451,11 @@ def measure_full_step(dev, args, workload="full_step"):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         st.run()
-    flush = torch.empty(int(256 * 2 ** 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     times = []
     n = max(20, min(200, args.steps // 10))
     for i in range(n + 3):
-        flush.fill_(float(i))
+        flush(i)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -393,7 +468,7 @@ def measure_full_step(dev, args, workload="full_step"):
     stage = {"indexer": [], "topk": [], "mla": []}
     (rb, re), = [(a, b) for a, b in st.chunks if b > a]
     for i in range(n):
-        flush.fill_(float(i))
+        flush(i)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         ev[0].record(stream)
         st.indexer_chunk(rb, re)
@@ -428,10 +503,9 @@ def cpu_baseline(case, pairs, mac_budget=12e9):
     contiguous block of rows of the same workload (all rows when they fit the
     multiply-accumulate budget, ~10-30 s of CPU work)."""
     import oracle
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import parity
+    from oracle.cases import oracle_cache, visible
     per_pair = case.num_heads * case.head_dim
-    vis = [parity.visible(case, r) for r in range(case.rows)]
+    vis = [visible(case, r) for r in range(case.rows)]
     if sum(vis) * per_pair <= mac_budget:
         rb, re = 0, case.rows
     else:
@@ -442,7 +516,7 @@ def cpu_baseline(case, pairs, mac_budget=12e9):
             acc += vis[re] * per_pair
             re += 1
         re = max(re, rb + 1)
-    cache, _ = parity.oracle_cache(case.kcache, case.block_table)
+    cache, _ = oracle_cache(case.kcache, case.block_table)
     ctx = case.context_lens.cpu()
     t0 = time.time()
     if case.q_scales is None:
@@ -468,11 +542,10 @@ def run_reference(args, rank, world):
         return None
     import oracle
     from deepseek_sparse_attention_mqa_gb300 import inputs
+    from oracle.cases import oracle_cache
     oracle.build()
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import parity
     case = inputs.make_case(args.workload, device="cpu")
-    cache, _ = parity.oracle_cache(case.kcache, case.block_table)
+    cache, _ = oracle_cache(case.kcache, case.block_table)
     q, w = case.q, case.weights
     n = case.next_n
     cap = 4096
@@ -518,6 +591,7 @@ def main():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-full-step", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

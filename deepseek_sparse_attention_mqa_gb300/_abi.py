@@ -22,7 +22,7 @@ EXPORTS = (
     "dsa_status_string", "dsa_last_cuda_error", "dsa_version", "dsa_indexer_schedule_bytes",
     "dsa_indexer_build_schedule", "indexer_mqa_logits_paged", "dsa_topk_workspace_bytes",
     "indexer_topk", "dsa_sparse_mla_workspace_bytes", "sparse_mla_decode", "dsa_get_device_status",
-    "indexer_mqa_logits_paged_noalloc",
+    "indexer_mqa_logits_paged_noalloc", "dsa_wait_selftest",
 )
 
 
@@ -96,6 +96,8 @@ def lib():
         L.sparse_mla_decode.argtypes = [_vp, _i, _i, _i, _i, ctypes.c_float,
                                         ctypes.POINTER(PagedCache), _vp, _i, _vp, _i64, _i, _vp,
                                         _vp, _vp, _sz, _vp, _vp]
+        L.dsa_wait_selftest.restype = _i
+        L.dsa_wait_selftest.argtypes = [_vp, ctypes.c_int32, _i, _vp, _vp]
         L.dsa_get_device_status.restype = _i
         L.dsa_get_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
         _lib = L
@@ -216,3 +218,10 @@ def device_status(status, stream=None) -> int:
     _check(lib().dsa_get_device_status(_ptr(status), ctypes.byref(v), _stream(stream)),
            "dsa_get_device_status")
     return int(v.value)
+
+
+def wait_selftest(flag, expect, limit_us, status, stream=None):
+    """dsa_wait_selftest: a bounded wait on a barrier arrived on only if
+    flag[0] == expect; a wait that runs out sets DEV_TIMEOUT in status."""
+    _check(lib().dsa_wait_selftest(_ptr(flag), int(expect), int(limit_us), _ptr(status),
+                                   _stream(stream)), "dsa_wait_selftest")

@@ -146,6 +146,49 @@ static dsa_status check_cache(const dsa_paged_cache* c, bool need_scales)
     return DSA_OK;
 }
 
+// Every host-side check of a logits call except those on the schedule buffer:
+// the same for indexer_mqa_logits_paged and its allocation-free variant, so
+// that both reject a bad call before enqueueing anything.  On success *units is
+// the call's work-unit count.
+dsa_status validate_logits_call(const void* q, const void* q_scales, int q_fmt, const float* weights,
+                                int num_heads, const dsa_paged_cache* k, const int32_t* context_lens, int batch,
+                                int next_n, int row_begin, int row_end, const float* logits,
+                                int64_t logits_row_stride, int logits_width, int64_t* units)
+{
+    if (!row_range_ok(batch, next_n, row_begin, row_end) || !k)
+        return DSA_ERR_INVALID_ARG;
+    if (!heads_supported(num_heads))
+        return DSA_ERR_UNSUPPORTED;
+    if (q_fmt != k->fmt || (q_fmt != DSA_KV_FP8_E4M3 && q_fmt != DSA_KV_MXFP4))
+        return DSA_ERR_UNSUPPORTED;
+    const int D = k->head_dim;
+    if (D != 32 && D != 64 && D != 128)
+        return DSA_ERR_UNSUPPORTED;
+    dsa_status st = check_cache(k, true);
+    if (st != DSA_OK)
+        return st;
+    if (q_fmt == DSA_KV_FP8_E4M3) {
+        if (k->val_token_stride != D || k->sc_token_stride != 4 || k->val_page_stride < int64_t(k->page_kv) * D ||
+            k->sc_page_stride < int64_t(k->page_kv) * 4)
+            return DSA_ERR_INVALID_ARG;
+    } else {
+        if (k->val_token_stride != D / 2 || k->sc_token_stride != D / 32 ||
+            k->val_page_stride < int64_t(k->page_kv) * (D / 2) || k->sc_page_stride < int64_t(k->page_kv) * (D / 32) ||
+            !q_scales)
+            return DSA_ERR_INVALID_ARG;
+    }
+    // MXFP4 keeps one TMEM accumulator per 32-element block: head_dim 128 fits
+    // units of at most 128 columns (rows x heads) in the 512 TMEM columns
+    if (q_fmt == DSA_KV_MXFP4 && D == 128 && unit_rows(next_n, num_heads) * num_heads > 128)
+        return DSA_ERR_UNSUPPORTED;
+    if (!q || !aligned16(q) || !weights || !aligned16(weights) || !logits || (batch > 0 && !context_lens))
+        return DSA_ERR_INVALID_ARG;
+    if (logits_width < 0 || logits_row_stride < logits_width)
+        return DSA_ERR_INVALID_ARG;
+    *units = count_units(batch, next_n, unit_rows(next_n, num_heads), row_begin, row_end);
+    return DSA_OK;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -204,39 +247,13 @@ dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_f
                                     size_t sched_bytes, float* logits, int64_t logits_row_stride,
                                     int logits_width, int32_t* status_dev, void* stream)
 {
-    if (!row_range_ok(batch, next_n, row_begin, row_end) || !k)
-        return DSA_ERR_INVALID_ARG;
-    if (!heads_supported(num_heads))
-        return DSA_ERR_UNSUPPORTED;
-    if (q_fmt != k->fmt || (q_fmt != DSA_KV_FP8_E4M3 && q_fmt != DSA_KV_MXFP4))
-        return DSA_ERR_UNSUPPORTED;
-    const int D = k->head_dim;
-    if (D != 32 && D != 64 && D != 128)
-        return DSA_ERR_UNSUPPORTED;
-    dsa_status st = check_cache(k, true);
+    int64_t units = 0;
+    dsa_status st = validate_logits_call(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n,
+                                         row_begin, row_end, logits, logits_row_stride, logits_width, &units);
     if (st != DSA_OK)
         return st;
-    if (q_fmt == DSA_KV_FP8_E4M3) {
-        if (k->val_token_stride != D || k->sc_token_stride != 4 || k->val_page_stride < int64_t(k->page_kv) * D ||
-            k->sc_page_stride < int64_t(k->page_kv) * 4)
-            return DSA_ERR_INVALID_ARG;
-    } else {
-        if (k->val_token_stride != D / 2 || k->sc_token_stride != D / 32 ||
-            k->val_page_stride < int64_t(k->page_kv) * (D / 2) || k->sc_page_stride < int64_t(k->page_kv) * (D / 32) ||
-            !q_scales)
-            return DSA_ERR_INVALID_ARG;
-    }
-    // MXFP4 keeps one TMEM accumulator per 32-element block: head_dim 128 fits
-    // units of at most 128 columns (rows x heads) in the 512 TMEM columns
-    if (q_fmt == DSA_KV_MXFP4 && D == 128 && unit_rows(next_n, num_heads) * num_heads > 128)
-        return DSA_ERR_UNSUPPORTED;
-    if (!q || !aligned16(q) || !weights || !aligned16(weights) || !logits || (sched && !aligned16(sched)) ||
-        (batch > 0 && !context_lens))
+    if (sched && !aligned16(sched))
         return DSA_ERR_INVALID_ARG;
-    if (logits_width < 0 || logits_row_stride < logits_width)
-        return DSA_ERR_INVALID_ARG;
-    const int G = unit_rows(next_n, num_heads);
-    const int64_t units = count_units(batch, next_n, G, row_begin, row_end);
     if (sched && sched_bytes < static_cast<size_t>(sched_bytes_for_units(units)))
         return DSA_ERR_CAPACITY;
     if (!sched && units > kInlineUnits)      // the kernels build at most kInlineUnits units themselves
@@ -258,7 +275,7 @@ dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_f
     a.next_n = next_n;
     a.row_begin = row_begin;
     a.row_end = row_end;
-    a.rows_per_unit = G;
+    a.rows_per_unit = unit_rows(next_n, num_heads);
     a.num_units = static_cast<int>(units);
     a.sched = static_cast<const int32_t*>(sched);
     a.logits = logits;

@@ -31,6 +31,13 @@ dsa_status encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, c
                         const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                         CUtensorMapSwizzle swizzle);
 
+// Host checks of a logits call shared by its entry points (api.cu); *units
+// receives the call's work-unit count.
+dsa_status validate_logits_call(const void* q, const void* q_scales, int q_fmt, const float* weights,
+                                int num_heads, const dsa_paged_cache* k, const int32_t* context_lens, int batch,
+                                int next_n, int row_begin, int row_end, const float* logits,
+                                int64_t logits_row_stride, int logits_width, int64_t* units);
+
 // Launchers implemented in the kernel translation units.
 dsa_status launch_build_schedule(const int32_t* context_lens, int batch, int next_n,
                                  int rows_per_unit, int row_begin, int row_end, int num_units,

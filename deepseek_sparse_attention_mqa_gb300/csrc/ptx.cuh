@@ -82,8 +82,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed, at most kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Wait until the phase with the given parity has completed, at most limit_ns.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -92,9 +92,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity))
                 return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs)
+        if (global_timer_ns() - t0 > limit_ns)
             return false;
     }
+}
+
+// Wait until the phase with the given parity has completed, at most kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------------------- TMA

@@ -188,8 +188,10 @@ DSA_API dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales,
  *    next_n * num_heads <= 256; ceil(rows / (256 / num_heads)) for prefill);
  *    larger calls return DSA_ERR_CAPACITY and enqueue nothing.
  *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any stream
- *    capture.
+ *    device and CUDA context, with that device current; again after a device
+ *    reset); make that first call before any stream capture.
+ *  - Every host check of indexer_mqa_logits_paged() runs before anything is
+ *    enqueued, so a rejected call leaves the array as it was.
  *  - All calls share the one array: calls whose work overlaps on the GPU (other
  *    streams, other host threads) race on it and must be serialised by the
  *    caller.  Nothing needs clearing between calls: each call rewrites every
@@ -255,6 +257,20 @@ DSA_API dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads
                              int64_t idx_row_stride, int k, void* out_bf16, float* lse,
                              void* workspace, size_t ws_bytes, int32_t* status_dev,
                              void* stream);
+
+/*
+ * Self-test of the bounded waits (no counterpart on the pages; it checks a
+ * property of this library).  Every on-chip wait in libdsa's kernels gives up
+ * after a time limit and reports DSA_DEV_TIMEOUT instead of hanging.  This call
+ * runs the same wait on a condition the caller controls: one thread waits, at
+ * most limit_us microseconds, on a barrier that is arrived on only if
+ * *flag == expect when the kernel reads it.  If the wait runs out it ORs
+ * DSA_DEV_TIMEOUT into *status_dev and the kernel returns normally.
+ * flag, status_dev: device int32 words.  1 <= limit_us <= 2,000,000.
+ * Errors: INVALID_ARG, UNSUPPORTED (wrong GPU), CUDA.
+ */
+DSA_API dsa_status dsa_wait_selftest(const int32_t* flag, int32_t expect, int limit_us,
+                                     int32_t* status_dev, void* stream);
 
 /*
  * Opt-in, SYNCHRONISING read of a device status word: waits for `stream`,

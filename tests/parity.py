@@ -19,39 +19,9 @@ MLA_OUT_ATOL = 1e-2
 MLA_LSE_ATOL = 1e-3
 
 
-def oracle_cache(paged, block_table, seqs=None):
-    """oracle.PagedBytes from a (possibly device-resident) inputs.Paged.  With
-    ``seqs`` only those sequences' pages are copied (renumbered), which keeps
-    full-size workloads cheap to check on sampled rows."""
-    bt = block_table.detach().cpu()
-    if seqs is None:
-        vals = paged.values.detach().cpu()
-        scs = None if paged.scales is None else paged.scales.detach().cpu()
-        return oracle.PagedBytes(vals, paged.val_page_stride, paged.val_token_stride, scs,
-                                 paged.sc_page_stride, paged.sc_token_stride, bt, paged.page_kv,
-                                 paged.num_pages), list(range(bt.shape[0]))
-    seqs = list(seqs)
-    phys = []
-    new_bt = torch.full((len(seqs), bt.shape[1]), -1, dtype=torch.int32)
-    for j, b in enumerate(seqs):
-        row = bt[b]
-        for lp in range(row.shape[0]):
-            p = int(row[lp])
-            if p < 0:
-                continue
-            new_bt[j, lp] = len(phys)
-            phys.append(p)
-    idx = torch.tensor(phys if phys else [0], dtype=torch.long, device=paged.values.device)
-    vals = paged.values.index_select(0, idx).cpu()
-    scs = None if paged.scales is None else paged.scales.index_select(0, idx).cpu()
-    return oracle.PagedBytes(vals, paged.val_page_stride, paged.val_token_stride, scs,
-                             paged.sc_page_stride, paged.sc_token_stride, new_bt, paged.page_kv,
-                             max(1, len(phys))), seqs
-
-
-def visible(case, r):
-    b, i = divmod(r, case.next_n)
-    return oracle.visible(int(case.context_lens[b]), case.next_n, i)
+# the workload -> oracle adapters live beside the oracle (the benchmark's CPU
+# legs use them too); re-exported here for the tests
+from oracle.cases import oracle_cache, visible  # noqa: E402,F401
 
 
 def check_logits(gpu_rows, ref_rows, vis, scale=None, what="logits"):

@@ -132,3 +132,23 @@ def test_inline_schedule_unit_limit_and_count():
     st = L.indexer_mqa_logits_paged(fake, None, 0, fake, 64, ctypes.byref(c), fake, 300, 1, 0, 300,
                                     None, 0, fake, 4096, 4096, None, None)
     assert st == _abi.DSA_ERR_CAPACITY
+
+
+def test_noalloc_rejects_before_touching_the_fixed_array():
+    """A call above 256 units with a bad argument is refused by the same host
+    checks as the regular entry point, before the fixed array's address is
+    looked up or its schedule build enqueued: with no GPU here, any CUDA call
+    would have come back as DSA_ERR_CUDA instead."""
+    L = _abi.lib()
+    fake = ctypes.c_void_p(0x1000)
+    c = _abi.PagedCache()
+    c.fmt, c.head_dim, c.page_kv, c.num_pages = 0, 128, 64, 2000
+    c.values, c.scales, c.block_table = 0x1000, 0x2000, 0x3000
+    c.val_page_stride, c.val_token_stride = 64 * 128, 128
+    c.sc_page_stride, c.sc_token_stride = 256, 4
+    c.bt_row_stride, c.max_pages_per_seq = 2000, 2000
+    call = lambda H, w, width: L.indexer_mqa_logits_paged_noalloc(
+        fake, None, 0, w, H, ctypes.byref(c), fake, 300, 1, 0, 300, fake, 4096, width, None, None)
+    assert call(48, fake, 4096) == _abi.DSA_ERR_UNSUPPORTED            # head count
+    assert call(64, ctypes.c_void_p(0x1004), 4096) == _abi.DSA_ERR_INVALID_ARG  # misaligned weights
+    assert call(64, fake, 8192) == _abi.DSA_ERR_INVALID_ARG            # row stride < width

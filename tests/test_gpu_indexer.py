@@ -208,17 +208,61 @@ def test_packed_step_inputs_match():
 
 
 def test_decode_full_size_sampled_rows():
+    """The decode workload at full size in the launch configuration the bench
+    times (inline schedule, 64 rows x 32768, top-k 2048 on 4-CTA clusters):
+    logits and the top-k of the kernel's own logits on sampled rows."""
     case = inputs.make_case("decode", device="cuda")
-    g, st = gpu_logits(case)
+    st = SparseAttentionStep(case, with_mla=False)
+    assert all(st.inline.values()) and st.launches_per_step() == 2
+    st.logits.fill_(float("nan"))
+    st.run()
+    torch.cuda.synchronize()
     assert st.device_status() == 0
     sample = [0, 17, 40, 63]
     q = case.q.cpu()
     w = case.weights.cpu()
     ctx = case.context_lens.cpu()
+    idx = st.idx.cpu().numpy()
     for r in sample:
         cache, _ = parity.oracle_cache(case.kcache, case.block_table, seqs=[r])
         o = oracle.logits_fp8(q[r:r + 1], w[r:r + 1], cache, ctx[r:r + 1], 1, width=case.width)
-        parity.check_logits([g[r]], [o[0]], [parity.visible(case, r)])
+        vis = parity.visible(case, r)
+        parity.check_logits([st.logits[r].cpu().numpy()], [o[0]], [vis])
+        scale = float(np.max(np.abs(o[0, :vis])))
+        parity.check_topk_tolerant(idx[r:r + 1], [o[0]], [vis], case.topk, scale)
+
+
+def test_prefill_full_size_both_chunks():
+    """The prefill workload at full size as the bench runs it: 16384 causal rows
+    in two 8192-row chunks (2048 work units each, so a prebuilt schedule per
+    chunk and persistent CTAs walking many units), logits width 16384, top-k
+    2048 on 1-CTA clusters.  Sampled rows of each chunk -- its first rows, the
+    rows on both sides of the chunk boundary and the last row -- are compared
+    with the oracle: logits element by element, entries past the row's window
+    untouched, and the top-k of the kernel's own logits."""
+    case = inputs.make_case("prefill", device="cuda")
+    st = SparseAttentionStep(case, with_mla=False)
+    assert st.chunks == [(0, 8192), (8192, 16384)]
+    assert not any(st.inline.values())
+    q, w = case.q.cpu(), case.weights.cpu()
+    ctx = case.context_lens.cpu()
+    cache, _ = parity.oracle_cache(case.kcache, case.block_table)
+    samples = [[0, 1, 127, 128, 3001, 8190, 8191], [8192, 8193, 12345, 16382, 16383]]
+    for (rb, re), rows in zip(st.chunks, samples):
+        st.logits.fill_(float("nan"))
+        st.indexer_chunk(rb, re)
+        st.topk_chunk(rb, re)
+        torch.cuda.synchronize()
+        assert st.device_status() == 0
+        for r in rows:
+            o = oracle.logits_fp8(q, w, cache, ctx, case.next_n, r, r + 1, width=case.width)[0]
+            vis = parity.visible(case, r)
+            assert vis == r + 1
+            g = st.logits[r - rb].cpu().numpy()
+            parity.check_logits([g], [o], [vis])
+            assert np.all(np.isnan(g[vis:])), "row %d written past its window" % r
+            scale = float(np.max(np.abs(o[:vis])))
+            parity.check_topk_tolerant(st.idx[r:r + 1].cpu().numpy(), [o], [vis], case.topk, scale)
 
 
 def test_bad_block_table_entry_sets_status():

@@ -72,6 +72,52 @@ def test_graph_replay_with_changing_lengths():
         check_indexer_rows(case, st, list(range(case.rows)), np.array(new, np.int32))
 
 
+def check_mla_rows(case, st, rows):
+    """MLA output of sampled rows on the GPU's own top-k selection vs the oracle."""
+    cache, _ = parity.oracle_cache(case.latent, case.block_table, seqs=rows)
+    idx = st.idx.cpu().numpy()
+    for j, r in enumerate(rows):
+        o, l = oracle.sparse_mla(case.q_mla[r:r + 1].cpu(), case.softmax_scale, oracle.FMT_FP8,
+                                 cache, idx[r:r + 1], case.d_v, seq_of_row=[j])
+        parity.check_mla(st.out[r:r + 1], st.lse[r:r + 1], o, l)
+
+
+def test_full_step_graph_with_mla_replayed_with_changing_lengths():
+    """The full decode step at full size (indexer 4 heads x 32, lens up to
+    131072, top-k 2048, sparse MLA 128 heads 576/512 on the FP8 latent) captured
+    once in ONE CUDA graph with the MLA stage, then replayed after the context
+    lengths change: every replay recomputes the work from the new lengths (no
+    stale windows), and sampled rows' logits, top-k and MLA output match the
+    oracle.  The new lengths include an empty history, rows shorter than k and
+    rows exactly at k."""
+    case = inputs.make_case("full_step", device="cuda")
+    st = SparseAttentionStep(case, with_mla=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        st.run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        st.run()
+    torch.cuda.synchronize()
+    orig = case.context_lens.cpu().numpy().copy()
+    shrunk = orig // 2
+    shrunk[:6] = [0, 1, 2047, 2048, 2049, 8192]
+    rows = [0, 1, 2, 3, 4, 5, 31, 63]
+    for new in (orig, shrunk, orig):
+        case.context_lens.copy_(torch.from_numpy(np.ascontiguousarray(new, np.int32)))
+        st.logits.fill_(float("nan"))
+        st.out.fill_(float("nan"))
+        st.idx.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert st.device_status() == 0
+        check_indexer_rows(case, st, rows, new)
+        check_mla_rows(case, st, rows)
+
+
 def test_full_step_full_size_sampled_rows():
     case = inputs.make_case("full_step", device="cuda")
     st = SparseAttentionStep(case, with_mla=True)

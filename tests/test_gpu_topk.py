@@ -55,6 +55,44 @@ def test_same_logits_exact(width, k):
     assert sorted(idx[5].tolist()) == list(range(k))
 
 
+def topk_cluster_size(rows, width, sm_count):
+    """The cluster size the library's top-k launch picks (CTAs per row): enough
+    that the widest slice fits in shared memory, then enough to cover ~1.5x the
+    SMs, at most 8."""
+    C = 1
+    while C < 8 and -(-width // C) > 16384:
+        C *= 2
+    while C < 8 and rows * C * 2 < 3 * sm_count:
+        C *= 2
+    return C
+
+
+@pytest.mark.parametrize("rows,width,k,expect_c", [
+    (64, 32768, 2048, 4),      # the decode workload's launch: 64 rows x 32768
+    (256, 65536, 512, 4),      # the speculative workload's launch: 128 x 2 rows x 65536
+    (320, 16384, 2048, 1),     # a prefill chunk's launch shape: >= 304 rows x 16384
+])
+def test_workload_launch_shapes_exact(rows, width, k, expect_c):
+    """Same logits on both sides at the row counts and widths the real workloads
+    launch with, so the cluster sizes they run at (4 CTAs per row for decode and
+    speculative decode, 1 for prefill chunks) are compared with the oracle's
+    full sort: identical index sets, ties to the lower position."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert topk_cluster_size(rows, width, sms) == expect_c
+    g = torch.Generator().manual_seed(rows + width + k)
+    lens = torch.randint(k // 2, width + 1, (rows,), generator=g).tolist()
+    lens[:6] = [0, 1, k, k + 1, width, width - 1]
+    logits = torch.randn((rows, width), generator=g)
+    logits[2::7] = torch.round(logits[2::7] * 4)         # rows full of exact ties
+    logits[3::11, ::3] = 2.5                             # a heavy tie at the top
+    idx, cnt, st = run_topk(logits, lens, 1, k, width)
+    assert st == 0
+    ref_idx, ref_cnt = oracle.topk(logits.double().numpy(), lens, 1, k)
+    assert list(cnt) == list(ref_cnt)
+    parity.check_topk_same_input(idx, ref_idx, lens, k)
+
+
 def test_next_n_windows():
     g = torch.Generator().manual_seed(2)
     lens = [10, 3000]

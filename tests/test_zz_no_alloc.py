@@ -18,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import parity
 from deepseek_sparse_attention_mqa_gb300 import _abi, build, inputs
 from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
@@ -31,6 +32,7 @@ def _setup():
         pytest.skip("no CUDA device")
     build.build()
     _abi.lib()
+    oracle.build()
 
 
 def regular_logits(case):
@@ -86,6 +88,34 @@ def test_over_256_units_use_the_fixed_array():
     for case in (big, small, big):
         ref, st = regular_logits(case)
         check_same(case, ref, noalloc_logits(case, st))
+
+
+def check_oracle(case, got):
+    """The allocation-free call's logits against the fp64 oracle."""
+    cache, _ = parity.oracle_cache(case.kcache, case.block_table)
+    ref = oracle.logits_fp8(case.q.cpu(), case.weights.cpu(), cache, case.context_lens.cpu(),
+                            case.next_n, width=case.width)
+    vis = [parity.visible(case, r) for r in range(case.rows)]
+    parity.check_logits(list(got), list(ref), vis)
+
+
+def test_fixed_array_rebuilt_when_the_call_changes():
+    # three calls above 256 units back to back, all through the fixed array: 300
+    # sequences, then 400 shorter ones with next_n 2 and another head count (so
+    # other unit sizes and tile counts), then the first call again.  A schedule
+    # left over from the previous call (skipped or partly rebuilt) would send
+    # each call's work to the wrong rows and tokens.
+    a = inputs.make_case("decode", device="cuda", lens=[(i * 37) % 600 + 1 for i in range(300)],
+                         num_heads=16, head_dim=64, width=640, seed=76)
+    b = inputs.make_case("decode", device="cuda", lens=[(i * 13) % 150 for i in range(400)],
+                         next_n=2, num_heads=32, head_dim=64, page_kv=32, width=160, seed=77)
+    for case in (a, b):
+        assert _abi.units_of(case.batch, case.next_n, case.num_heads, 0, case.rows) > _abi.INLINE_UNITS
+    for case in (a, b, a):
+        ref, st = regular_logits(case)
+        got = noalloc_logits(case, st)
+        check_same(case, ref, got)
+        check_oracle(case, got)
 
 
 def test_mxfp4_through_the_noalloc_entry_point():
