@@ -20,6 +20,10 @@ and the passages they follow:
 * ``topk`` -- full sort, descending logit, ties by ascending index, -1 padding.
 * ``sparse_mla`` -- softmax attention over the selected latent tokens with an
   fp32-style LSE output ("Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels").
+* ``encode_e4m3 / encode_e2m1 / quantize_scatter`` -- writing new K rows into
+  the paged FP8 (per-token fp32 scale) or MXFP4 (ue8m0 per 32 elements) cache
+  through a slot mapping ("feat(deepseek_v4): Add fp4 indexer for dsv4": the FP4
+  indexer's cache scatter beside its logits kernel; OCP MX v1.0 block scaling).
 
 Parity pins: tests/test_oracle_*.py.  No function here is "parity unpinned".
 """
@@ -96,6 +100,14 @@ def _load():
             _c_u16p, _int, _int, _int, _int, ctypes.c_double, _int, _c_u8p, _i64, _i64,
             _c_u8p, _i64, _i64, _c_i32p, _i64, _int, _int, _int, _c_i32p, _int,
             _c_i32p, _i64, _int, _c_f64p, _c_f64p]
+        lib.dsa_oracle_encode_e4m3.restype = ctypes.c_uint8
+        lib.dsa_oracle_encode_e4m3.argtypes = [ctypes.c_float]
+        lib.dsa_oracle_encode_e2m1.restype = ctypes.c_uint8
+        lib.dsa_oracle_encode_e2m1.argtypes = [ctypes.c_float]
+        lib.dsa_oracle_quantize_scatter.restype = _int
+        lib.dsa_oracle_quantize_scatter.argtypes = [
+            ctypes.c_void_p, _int, _i64, _int, _int, ctypes.POINTER(ctypes.c_int64), _int,
+            _c_u8p, _i64, _i64, _c_u8p, _i64, _i64, _int, _int]
         lib.dsa_oracle_threads.restype = _int
         lib.dsa_oracle_threads.argtypes = []
         _lib = lib
@@ -264,3 +276,35 @@ def sparse_mla(q_bf16, softmax_scale, fmt, cache: PagedBytes, idx, d_v, seq_of_r
         _ptr(ix, ctypes.c_int32), k, k, _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
     _check(rc, "sparse_mla")
     return out, lse
+
+
+def encode_e4m3(v: float) -> int:
+    """Nearest e4m3 code to the float32 value v (ties to even, saturating)."""
+    return int(_load().dsa_oracle_encode_e4m3(float(v)))
+
+
+def encode_e2m1(v: float) -> int:
+    """Nearest e2m1 code (4 bits) to the float32 value v (ties to even, saturating)."""
+    return int(_load().dsa_oracle_encode_e2m1(float(v)))
+
+
+def quantize_scatter(k, slots, fmt, cache: PagedBytes):
+    """Quantise rows of new K (fp32 array, or torch bf16 / fp32 tensor) and write
+    them into ``cache`` (its values / scales byte buffers are updated in place)
+    at the physical slots ``slots`` (int64, page * page_kv + row; < 0 skipped).
+    fmt: 0 = FP8 e4m3 + fp32 token scale, 1 = MXFP4 (e2m1 + ue8m0 per 32)."""
+    lib = _load()
+    is_bf16 = hasattr(k, "dtype") and str(k.dtype) == "torch.bfloat16"
+    if is_bf16:
+        arr = _np(k.view(__import__("torch").int16), np.uint16)
+    else:
+        arr = _np(k, np.float32)
+    n, D = arr.shape
+    sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int64).reshape(-1))
+    assert sl.shape[0] == n
+    rc = lib.dsa_oracle_quantize_scatter(
+        arr.ctypes.data_as(ctypes.c_void_p), 1 if is_bf16 else 0, D, n, D,
+        sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), int(fmt),
+        _ptr(cache.values, ctypes.c_uint8), cache.vps, cache.vts,
+        _ptr(cache.scales, ctypes.c_uint8), cache.sps, cache.sts, cache.page_kv, cache.num_pages)
+    _check(rc, "quantize_scatter")

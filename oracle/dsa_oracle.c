@@ -414,6 +414,163 @@ int dsa_oracle_sparse_mla(const uint16_t* q, int rows, int Hq, int d_qk, int d_v
     return err;
 }
 
+/* --------------------------------------------- K-cache quantise / scatter */
+
+/* Round-half-to-even of a non-negative double to an integer (the doubles met
+ * here are exact multiples of 2^-k with small magnitude, so this is exact). */
+static double round_half_even(double a)
+{
+    double f = floor(a), d = a - f;
+    if (d > 0.5)
+        return f + 1.0;
+    if (d < 0.5)
+        return f;
+    return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+/* Nearest OCP E4M3 ("fn") code to the float v, ties to the even code,
+ * saturating to +-448 (no NaN produced for finite v); the sign bit is v's sign
+ * bit (so a negative value that rounds to zero gives 0x80).  Each step follows
+ * the format: subnormals are multiples of 2^-9 below 2^-6; a normal binade
+ * [2^E, 2^(E+1)) holds 8 values spaced 2^(E-3). */
+uint8_t dsa_oracle_encode_e4m3(float v)
+{
+    uint32_t u;
+    double a;
+    uint8_t sign, code;
+    memcpy(&u, &v, sizeof u);
+    sign = (uint8_t)((u >> 31) << 7);
+    a = fabs((double)v);
+    if (a >= 448.0) {
+        code = 0x7E;
+    } else if (a < ldexp(1.0, -6)) {
+        double m = round_half_even(a / ldexp(1.0, -9));        /* 0 .. 8 */
+        code = (uint8_t)m;                                     /* m = 8 is 2^-6: code 0x08 */
+    } else {
+        int E;
+        double q;
+        frexp(a, &E);                                          /* a = f * 2^E, f in [0.5, 1) */
+        E -= 1;                                                /* a in [2^E, 2^(E+1)) */
+        q = round_half_even(a / ldexp(1.0, E - 3));            /* 8 .. 16 */
+        if (q >= 16.0) {
+            q = 8.0;
+            E += 1;
+        }
+        if (E > 8 || (E == 8 && q > 14.0))
+            code = 0x7E;                                       /* beyond 448: saturate */
+        else
+            code = (uint8_t)(((E + 7) << 3) | ((int)q - 8));
+    }
+    return (uint8_t)(sign | code);
+}
+
+/* Nearest OCP E2M1 code (4 bits) to the float v, ties to the even code,
+ * saturating to +-6; the sign bit (bit 3) is v's sign bit.  Grid: 0, 0.5, 1,
+ * 1.5 (spacing 0.5), 2, 3 (spacing 1), 4, 6 (spacing 2). */
+uint8_t dsa_oracle_encode_e2m1(float v)
+{
+    uint32_t u;
+    double a;
+    uint8_t sign, code;
+    memcpy(&u, &v, sizeof u);
+    sign = (uint8_t)((u >> 31) << 3);
+    a = fabs((double)v);
+    if (a >= 6.0)
+        code = 7;
+    else if (a < 2.0)
+        code = (uint8_t)round_half_even(a * 2.0);              /* 0 .. 4 (4 = 2.0) */
+    else if (a < 4.0)
+        code = (uint8_t)(round_half_even(a) + 2.0);            /* 2, 3, 4 -> codes 4, 5, 6 */
+    else
+        code = (uint8_t)(round_half_even(a / 2.0) + 4.0);      /* 2, 3 -> codes 6, 7 */
+    return (uint8_t)(sign | code);
+}
+
+/* Writes new K rows into a paged cache through a slot mapping (slot = physical
+ * page * page_kv + row; slots < 0 are skipped), quantising each row:
+ *  - FP8 (fmt 0): per token, amax = max_d |x_d| (fp32), scale = amax / 448 in
+ *    fp32 (1 when amax = 0), code_d = e4m3(x_d / scale) with the division in
+ *    fp32; the fp32 scale is stored beside the token.
+ *  - MXFP4 (fmt 1): per 32-element block, amax (fp32), shared exponent
+ *    e = floor(log2 amax) - 2 clamped to [-127, 127] (-127 when amax = 0),
+ *    stored as the ue8m0 byte e + 127; element codes e2m1(x_d * 2^-e), packed
+ *    two per byte with the even element in the low nibble.
+ * k:  [n_tokens] rows of D values, fp32 (k_is_bf16 = 0) or bf16 bits, row
+ *     stride k_stride ELEMENTS.  Returns ORACLE_ERR_PAGE if a slot's page is
+ *     outside [0, num_pages) (that token is skipped). */
+int dsa_oracle_quantize_scatter(const void* k, int k_is_bf16, int64_t k_stride, int n_tokens, int D,
+                                const int64_t* slots, int fmt, uint8_t* vals, int64_t vps, int64_t vts,
+                                uint8_t* scales, int64_t sps, int64_t sts, int page_kv, int num_pages)
+{
+    int err = ORACLE_OK;
+    long t;
+    if (n_tokens < 0 || D <= 0 || page_kv <= 0 || (fmt != 0 && fmt != 1) || (fmt == 1 && D % 32 != 0))
+        return ORACLE_ERR_ARG;
+    for (t = 0; t < n_tokens; ++t) {
+        int64_t slot = slots[t], page, row;
+        float x[4096];
+        uint8_t *vrow, *srow;
+        int d;
+        if (slot < 0)
+            continue;
+        page = slot / page_kv;
+        row = slot % page_kv;
+        if (page >= num_pages || D > 4096) {
+            err = ORACLE_ERR_PAGE;
+            continue;
+        }
+        for (d = 0; d < D; ++d) {
+            if (k_is_bf16) {
+                uint16_t bits = ((const uint16_t*)k)[t * k_stride + d];
+                x[d] = (float)dsa_oracle_bf16(bits);
+            } else {
+                x[d] = ((const float*)k)[t * k_stride + d];
+            }
+        }
+        vrow = vals + page * vps + row * vts;
+        srow = scales + page * sps + row * sts;
+        if (fmt == 0) {
+            float amax = 0.0f, scale;
+            for (d = 0; d < D; ++d)
+                if (fabsf(x[d]) > amax)
+                    amax = fabsf(x[d]);
+            scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+            for (d = 0; d < D; ++d) {
+                float q = x[d] / scale;
+                vrow[d] = dsa_oracle_encode_e4m3(q);
+            }
+            memcpy(srow, &scale, sizeof scale);
+        } else {
+            int blk;
+            for (blk = 0; blk < D / 32; ++blk) {
+                float amax = 0.0f;
+                int e;
+                for (d = 32 * blk; d < 32 * blk + 32; ++d)
+                    if (fabsf(x[d]) > amax)
+                        amax = fabsf(x[d]);
+                if (amax > 0.0f) {
+                    int E;
+                    frexpf(amax, &E);                  /* amax = f * 2^E, f in [0.5, 1) */
+                    e = (E - 1) - 2;
+                } else {
+                    e = -127;
+                }
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+                srow[blk] = (uint8_t)(e + 127);
+                for (d = 32 * blk; d < 32 * blk + 32; d += 2) {
+                    uint8_t lo = dsa_oracle_encode_e2m1((float)ldexp((double)x[d], -e));
+                    uint8_t hi = dsa_oracle_encode_e2m1((float)ldexp((double)x[d + 1], -e));
+                    vrow[d / 2] = (uint8_t)(lo | (hi << 4));
+                }
+            }
+        }
+    }
+    return err;
+}
+
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
 int dsa_oracle_threads(void)
 {
