@@ -22,8 +22,9 @@ EXPORTS = (
     "dsa_status_string", "dsa_last_cuda_error", "dsa_version", "dsa_indexer_schedule_bytes",
     "dsa_indexer_build_schedule", "indexer_mqa_logits_paged", "dsa_topk_workspace_bytes",
     "indexer_topk", "dsa_sparse_mla_workspace_bytes", "sparse_mla_decode", "dsa_get_device_status",
-    "indexer_mqa_logits_paged_noalloc", "dsa_wait_selftest",
+    "indexer_mqa_logits_paged_noalloc", "dsa_wait_selftest", "dsa_kv_quantize_scatter",
 )
+DTYPE_F32, DTYPE_BF16 = 0, 1
 
 
 class DSAError(RuntimeError):
@@ -96,6 +97,8 @@ def lib():
         L.sparse_mla_decode.argtypes = [_vp, _i, _i, _i, _i, ctypes.c_float,
                                         ctypes.POINTER(PagedCache), _vp, _i, _vp, _i64, _i, _vp,
                                         _vp, _vp, _sz, _vp, _vp]
+        L.dsa_kv_quantize_scatter.restype = _i
+        L.dsa_kv_quantize_scatter.argtypes = [_vp, _i, _i64, _i, _vp, ctypes.POINTER(PagedCache), _vp, _vp]
         L.dsa_wait_selftest.restype = _i
         L.dsa_wait_selftest.argtypes = [_vp, ctypes.c_int32, _i, _vp, _vp]
         L.dsa_get_device_status.restype = _i
@@ -225,3 +228,15 @@ def wait_selftest(flag, expect, limit_us, status, stream=None):
     flag[0] == expect; a wait that runs out sets DEV_TIMEOUT in status."""
     _check(lib().dsa_wait_selftest(_ptr(flag), int(expect), int(limit_us), _ptr(status),
                                    _stream(stream)), "dsa_wait_selftest")
+
+
+def kv_quantize_scatter(k_new, slot_mapping, cache: PagedCache, status=None, stream=None):
+    """dsa_kv_quantize_scatter: quantise rows of k_new ([n, D] float32 or
+    bfloat16 device tensor) into `cache` at slot_mapping ([n] int64)."""
+    import torch
+    dt = DTYPE_BF16 if k_new.dtype == torch.bfloat16 else DTYPE_F32
+    if k_new.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("k_new must be float32 or bfloat16")
+    _check(lib().dsa_kv_quantize_scatter(
+        _ptr(k_new), dt, k_new.stride(0) if k_new.dim() == 2 else k_new.shape[-1], k_new.shape[0],
+        _ptr(slot_mapping), ctypes.byref(cache), _ptr(status), _stream(stream)), "dsa_kv_quantize_scatter")

@@ -397,6 +397,47 @@ dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads, int d_
     return launch_sparse_mla_simt(a, static_cast<cudaStream_t>(stream));
 }
 
+dsa_status dsa_kv_quantize_scatter(const void* k_new, int k_dtype, int64_t k_row_stride, int n_tokens,
+                                   const int64_t* slot_mapping, const dsa_paged_cache* cache, int32_t* status_dev,
+                                   void* stream)
+{
+    if (!cache || n_tokens < 0 || (k_dtype != DSA_DTYPE_F32 && k_dtype != DSA_DTYPE_BF16))
+        return DSA_ERR_INVALID_ARG;
+    const int D = cache->head_dim;
+    const int64_t esize = k_dtype == DSA_DTYPE_BF16 ? 2 : 4;
+    if (cache->fmt == DSA_KV_FP8_E4M3) {
+        if (D < 8 || D % 8 != 0 || D > 4096)
+            return DSA_ERR_UNSUPPORTED;
+        if (cache->val_token_stride < D || cache->val_token_stride % 8 != 0 || cache->val_page_stride % 8 != 0 ||
+            cache->sc_token_stride < 4 || cache->sc_token_stride % 4 != 0 || cache->sc_page_stride % 4 != 0)
+            return DSA_ERR_INVALID_ARG;
+    } else if (cache->fmt == DSA_KV_MXFP4) {
+        if (D < 32 || D % 32 != 0 || D > 4096)
+            return DSA_ERR_UNSUPPORTED;
+        if (cache->val_token_stride < D / 2 || cache->val_token_stride % 4 != 0 || cache->val_page_stride % 4 != 0 ||
+            cache->sc_token_stride < D / 32)
+            return DSA_ERR_INVALID_ARG;
+    } else {
+        return DSA_ERR_UNSUPPORTED;
+    }
+    if (cache->page_kv < 1 || cache->num_pages < 1 || !cache->values || !cache->scales ||
+        (reinterpret_cast<uintptr_t>(cache->values) & 7u) != 0 ||
+        (reinterpret_cast<uintptr_t>(cache->scales) & 3u) != 0 ||
+        static_cast<int64_t>(cache->page_kv) * cache->val_token_stride > cache->val_page_stride ||
+        static_cast<int64_t>(cache->page_kv) * cache->sc_token_stride > cache->sc_page_stride)
+        return DSA_ERR_INVALID_ARG;
+    if (n_tokens == 0)
+        return DSA_OK;
+    if (!k_new || !slot_mapping || !aligned16(k_new) || k_row_stride < D || (k_row_stride * esize) % 16 != 0)
+        return DSA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    const dsa_status st = current_device(&dev);
+    if (st != DSA_OK)
+        return st;
+    return launch_kv_scatter(k_new, k_dtype == DSA_DTYPE_BF16, k_row_stride, n_tokens, slot_mapping, cache,
+                             status_dev, static_cast<cudaStream_t>(stream));
+}
+
 dsa_status dsa_get_device_status(const int32_t* status_dev, int32_t* host_out, void* stream)
 {
     if (!status_dev || !host_out)

@@ -82,6 +82,9 @@ struct TopkArgs {
 };
 dsa_status launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
+dsa_status launch_kv_scatter(const void* k, bool bf16, int64_t k_stride, int n_tokens, const int64_t* slots,
+                             const dsa_paged_cache* c, int32_t* status, cudaStream_t stream);
+
 struct MlaArgs {
     const void* q;
     int rows;

@@ -60,6 +60,10 @@ typedef enum {
     DSA_KV_BF16 = 2      /* bf16 values, no scale */
 } dsa_format;
 
+/* Element types of unquantised inputs. */
+#define DSA_DTYPE_F32 0
+#define DSA_DTYPE_BF16 1
+
 /* Bits OR-ed into the caller's device status word. */
 #define DSA_DEV_BAD_PAGE 0x1  /* block_table entry outside [0, num_pages): access skipped */
 #define DSA_DEV_WIDTH 0x2     /* visible length > logits_width: clipped to the width */
@@ -257,6 +261,39 @@ DSA_API dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads
                              int64_t idx_row_stride, int k, void* out_bf16, float* lse,
                              void* workspace, size_t ws_bytes, int32_t* status_dev,
                              void* stream);
+
+/*
+ * K-cache quantise / scatter ("feat(deepseek_v4): Add fp4 indexer for dsv4",
+ * commit notes: the FP4 indexer's scatter kernel beside its mqa-logits kernel,
+ * writing new tokens' K into the paged cache).  Token t's row of new K is
+ * quantised and written to physical slot s = slot_mapping[t] of `cache`, i.e.
+ * page s / page_kv, row s % page_kv (slots < 0 are padding and skipped; a page
+ * >= num_pages sets DSA_DEV_BAD_PAGE and the token is skipped):
+ *  - DSA_KV_FP8_E4M3: scale = amax / 448 over the token's head_dim values (fp32
+ *    division; 1 for an all-zero row), codes e4m3(x / scale) (fp32 division,
+ *    round to nearest, ties to even, saturating at +-448); the fp32 scale is
+ *    stored at the token's scale slot.
+ *  - DSA_KV_MXFP4 (OCP MX v1.0): per 32-element block, e = floor(log2 amax) - 2
+ *    clamped to [-127, 127] (-127 for a zero block) stored as the ue8m0 byte
+ *    e + 127, codes e2m1(x * 2^-e) (ties to even, saturating at +-6), two per
+ *    byte with the even element in the low nibble.
+ * The sign bit of every code is the sign bit of the value it encodes.
+ *
+ * k_new:    [n_tokens, k_row_stride] fp32 (k_dtype DSA_DTYPE_F32) or bf16
+ *           (DSA_DTYPE_BF16); 16-byte aligned, row stride in ELEMENTS with
+ *           stride * element size a multiple of 16.
+ * slot_mapping: device int64 [n_tokens].
+ * cache:    FP8 (head_dim % 8 == 0) or MXFP4 (head_dim % 32 == 0), head_dim <=
+ *           4096; its values and scales are WRITTEN (only the addressed token
+ *           rows); block_table is not used.  FP8: values 8-byte aligned, value
+ *           strides multiples of 8, scale strides multiples of 4.  MXFP4: value
+ *           strides multiples of 4.  Two tokens mapped to one slot race.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+DSA_API dsa_status dsa_kv_quantize_scatter(const void* k_new, int k_dtype, int64_t k_row_stride,
+                                           int n_tokens, const int64_t* slot_mapping,
+                                           const dsa_paged_cache* cache, int32_t* status_dev,
+                                           void* stream);
 
 /*
  * Self-test of the bounded waits (no counterpart on the pages; it checks a
