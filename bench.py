@@ -4,7 +4,8 @@
 Default workload (the decode indexer + top-k configuration): batch 64, next_n 1,
 64 indexer heads, head_dim 128, page 64, context lengths U[4096, 32768] in a 2x
 oversized shuffled FP8 pool, top-k 2048.  One step = device schedule build +
-paged MQA logits + top-k (3 libdsa launches).  Reported:
+paged MQA logits + top-k (2 libdsa launches; the fused single-launch
+indexer_score_topk is timed beside it, --fused makes it the headline).  Reported:
 
 * value        K-tokens scored/s (sum of visible lengths / step time / 1e3),
                inputs resident in HBM, L2 flushed between steps, CUDA events;
@@ -199,9 +200,11 @@ class L2Flush:
         torch.sum(self.buf, dim=0, out=self.acc)
 
 
-def time_indexer_steps(st, steps, flush, stream, fused=False):
-    """Event-timed indexer steps (schedule if any, logits, top-k per chunk), L2
-    flushed before each; returns per-step lists of ms."""
+def time_indexer_steps(st, steps, flush, stream):
+    """Event-timed indexer steps, L2 flushed before each; per chunk: the
+    schedule launch (chunks of more than 256 units), then either the logits and
+    top-k launches or (st.fused) the one fused score + top-k launch.  Returns
+    per-step lists of ms ("logits" is the fused launch when fused, "topk" 0)."""
     from deepseek_sparse_attention_mqa_gb300 import _abi
     c = st.case
     chunks = [(rb, re) for rb, re in st.chunks if re > rb]
@@ -216,11 +219,17 @@ def time_indexer_steps(st, steps, flush, stream, fused=False):
             if not inline:
                 _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status)
             e[3 * ci + 1].record(stream)
-            _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
-                            c.batch, c.next_n, rb, re, None if inline else st.sched, st.logits, st.width,
-                            st.status)
-            e[3 * ci + 2].record(stream)
-            st.topk_chunk(rb, re)
+            if st.fused:
+                _abi.score_topk(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
+                                c.batch, c.next_n, rb, re, None if inline else st.sched, st.logits, st.width,
+                                c.topk, st.idx[rb:re], st.count[rb:re], st.fused_ws, st.status)
+                e[3 * ci + 2].record(stream)
+            else:
+                _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,
+                                c.batch, c.next_n, rb, re, None if inline else st.sched, st.logits, st.width,
+                                st.status)
+                e[3 * ci + 2].record(stream)
+                st.topk_chunk(rb, re)
             e[3 * ci + 3].record(stream)
     torch.cuda.synchronize()
     return {
@@ -232,38 +241,54 @@ def time_indexer_steps(st, steps, flush, stream, fused=False):
     }
 
 
-def logits_roofline(case, workload, logits_ms_per_launch, nck):
-    """Roofline of the logits kernel: HBM bytes for the decode-type workloads,
-    FP8 tensor flops for the prefill (compute-bound) workload."""
+def kernel_ms_summary(t, fused, extra=None):
+    d = {"schedule": round(statistics.mean(t["schedule"]), 5), "chunks": t["chunks"]}
+    if fused:
+        d["score_topk"] = round(statistics.mean(t["logits"]), 5)
+    else:
+        d["logits"] = round(statistics.mean(t["logits"]), 5)
+        d["topk"] = round(statistics.mean(t["topk"]), 5)
+    d.update(extra or {})
+    return d
+
+
+def logits_roofline(case, workload, logits_ms_per_launch, nck, fused=False):
+    """Roofline of the logits kernel (fused: the score + top-k kernel): HBM
+    bytes for the decode-type workloads (the fused kernel also writes the index
+    rows), FP8 tensor flops for the prefill (compute-bound) workload."""
     from deepseek_sparse_attention_mqa_gb300 import inputs
     hbm, bf16, _, src = measured_peaks()
     pairs = scored_pairs(case)
+    base = "logits_fp8" if case.fmt == inputs.FMT_FP8 else "logits_mxfp4"
+    kname = base + (" + fused top-k (indexer_score_topk)" if fused else " (indexer_mqa_logits_paged)")
+    tkey = base + ("_fused" if fused else "")
     if workload == "prefill":
         # FP8 MMA work per launch (one chunk): 2 * pairs * heads * head_dim
         flops = 2.0 * pairs * case.num_heads * case.head_dim / nck
         achieved = flops / (logits_ms_per_launch * 1e-3) / 1e12
         fp8_peak = 2.0 * bf16                             # nominal fp8 : bf16 = 2 : 1
-        return {"kernel": "logits_fp8 (indexer_mqa_logits_paged), per chunk launch", "bound": "tensor",
+        return {"kernel": kname + ", per chunk launch", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp8_peak, 4),
                 "peak_source": src + " bf16 burst x 2 (nominal fp8/bf16 ratio)",
-                "algorithmic_flops": flops, "traffic": load_traffic("logits_fp8", workload)}
-    lg_bytes = logits_algorithmic_bytes(case) / nck
+                "algorithmic_flops": flops, "traffic": load_traffic(tkey, workload)}
+    lg_bytes = (logits_algorithmic_bytes(case) + (case.rows * case.topk * 4 if fused else 0)) / nck
     achieved = lg_bytes / (logits_ms_per_launch * 1e-3) / 1e9
-    kname = "logits_fp8" if case.fmt == inputs.FMT_FP8 else "logits_mxfp4"
-    return {"kernel": kname + " (indexer_mqa_logits_paged)", "bound": "hbm",
+    return {"kernel": kname, "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_source": src,
-            "algorithmic_bytes": lg_bytes, "traffic": load_traffic(kname, workload)}
+            "algorithmic_bytes": lg_bytes, "traffic": load_traffic(tkey, workload)}
 
 
-def measure_indexer_config(workload, dev, steps, flush):
-    """One indexer configuration timed on its own (spec_mxfp4, prefill): the
-    configuration's value, per-kernel times and the logits roofline."""
+def measure_indexer_config(workload, dev, steps, flush, fused=True, case=None):
+    """One indexer configuration timed on its own: the configuration's value,
+    per-kernel times and the roofline of its dominant kernel."""
     from deepseek_sparse_attention_mqa_gb300 import inputs
     from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
-    case = inputs.make_case(workload, device=dev)
-    st = SparseAttentionStep(case, with_mla=False)
+    own = case is None
+    if own:
+        case = inputs.make_case(workload, device=dev)
+    st = SparseAttentionStep(case, with_mla=False, fused=fused)
     stream = torch.cuda.current_stream()
     for _ in range(3):
         st.run()
@@ -273,15 +298,16 @@ def measure_indexer_config(workload, dev, steps, flush):
     pairs = scored_pairs(case)
     ms = statistics.mean(t["step"])
     nck = t["chunks"]
-    res = {"workload": WORKLOADS[workload], "value": round(pairs / (ms * 1e-3) / 1e3, 1), "unit": UNIT,
+    res = {"workload": WORKLOADS.get(workload, workload), "fused": fused,
+           "value": round(pairs / (ms * 1e-3) / 1e3, 1), "unit": UNIT,
            "ms_per_step": round(ms, 5), "steps": steps, "scored_pairs_per_step": pairs,
-           "kernel_ms": {"schedule": round(statistics.mean(t["schedule"]), 5),
-                         "logits": round(statistics.mean(t["logits"]), 5),
-                         "topk": round(statistics.mean(t["topk"]), 5), "chunks": nck},
-           "roofline": logits_roofline(case, workload, statistics.mean(t["logits"]) / nck, nck),
+           "kernel_ms": kernel_ms_summary(t, fused),
+           "roofline": logits_roofline(case, workload, statistics.mean(t["logits"]) / nck, nck, fused),
            "gpu_launches_per_step": st.launches_per_step(), "device_status": status}
-    del st, case
-    torch.cuda.empty_cache()
+    del st
+    if own:
+        del case
+        torch.cuda.empty_cache()
     return res
 
 
@@ -301,7 +327,8 @@ def run_ours(args, rank, world, local):
     _abi.lib()
 
     case = inputs.make_case(args.workload, device=dev)
-    st = SparseAttentionStep(case, with_mla=False)
+    fused = args.fused
+    st = SparseAttentionStep(case, with_mla=False, fused=fused)
     pairs = scored_pairs(case)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
@@ -335,13 +362,14 @@ def run_ours(args, rank, world, local):
 
     result = None
     if rank == 0:
+        n_side = max(10, min(200, args.steps))
         # the same steps with the former flush (a 1 GiB WRITE), once, for comparison:
-        # its dirty lines are written back inside the timed logits kernel
+        # its dirty lines are written back inside the timed kernel
         wbuf = torch.empty(int(2 ** 30) // 4, dtype=torch.float32, device=dev)
-        tw = time_indexer_steps(st, max(10, min(200, args.steps)), lambda s: wbuf.fill_(float(s)), stream)
+        tw = time_indexer_steps(st, n_side, lambda s: wbuf.fill_(float(s)), stream)
         del wbuf
         e2e = measure_e2e(st, case, args, pairs, dev)
-        roof = logits_roofline(case, args.workload, statistics.mean(t["logits"]) / nck, nck)
+        roof = logits_roofline(case, args.workload, statistics.mean(t["logits"]) / nck, nck, fused)
         result = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -352,22 +380,25 @@ def run_ours(args, rank, world, local):
                        "page_kv": case.page_kv, "topk": case.topk, "scored_pairs_per_step": pairs,
                        "seed": case.meta["seed"], "l2": "flushed between steps (384 MiB read)",
                        "parallelism": "replicas"},
-            "kernel_ms": {"schedule": round(statistics.mean(t["schedule"]), 5),
-                          "logits": round(statistics.mean(t["logits"]), 5),
-                          "topk": round(statistics.mean(t["topk"]), 5), "chunks": nck,
-                          "logits_after_write_flush": round(statistics.mean(tw["logits"]), 5)},
+            "kernel_ms": kernel_ms_summary(t, fused, {"first_kernel_after_write_flush":
+                                                      round(statistics.mean(tw["logits"]), 5)}),
+            "fused_score_topk": fused,
             "roofline": roof,
             "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clocks,
             "e2e": e2e,
         }
+        # the same workload with the other top-k arrangement (separate launches
+        # when the headline is fused, and vice versa)
+        result["unfused" if fused else "fused"] = measure_indexer_config(args.workload, dev, n_side, flush,
+                                                                         not fused, case)
         if args.workload == "decode" and not args.skip_configs:
-            n_sub = max(10, min(200, args.steps))
-            result["spec_mxfp4"] = measure_indexer_config("spec_mxfp4", dev, n_sub, flush)
-            result["prefill"] = measure_indexer_config("prefill", dev, max(5, min(20, args.steps)), flush)
+            result["spec_mxfp4"] = measure_indexer_config("spec_mxfp4", dev, n_side, flush, fused)
+            result["prefill"] = measure_indexer_config("prefill", dev, max(5, min(20, args.steps)), flush,
+                                                       False)
         if not args.skip_full_step:
-            result["full_step"] = measure_full_step(dev, args, flush)
-            result["full_step_indexer_h64"] = measure_full_step(dev, args, flush, "full_step_h64")
+            result["full_step"] = measure_full_step(dev, args, flush, fused=fused)
+            result["full_step_indexer_h64"] = measure_full_step(dev, args, flush, "full_step_h64", fused=fused)
         if not args.skip_cpu:
             result["cpu_baseline"] = cpu_baseline(case, pairs)
     if world > 1:
@@ -403,7 +434,7 @@ def measure_e2e(st, case, args, pairs, dev):
     block table) to the device, runs, and reads the top-k indices back."""
     from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep, StepInputs
     ins = StepInputs(case, with_mla=False)
-    st = SparseAttentionStep(ins.case(), with_mla=False)
+    st = SparseAttentionStep(ins.case(), with_mla=False, fused=st.fused)
     idx_host = torch.empty(st.idx.shape, dtype=torch.int32).pin_memory()
     h2d = ins.nbytes
     d2h = idx_host.numel() * 4
@@ -432,7 +463,7 @@ def measure_e2e(st, case, args, pairs, dev):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
-def measure_full_step(dev, args, flush, workload="full_step"):
+def measure_full_step(dev, args, flush, workload="full_step", fused=True):
     """Full decode step (indexer, top-k, sparse MLA 128 heads 576/512 on an FP8
     latent, lens U[8192,131072], top-k 2048) captured in one CUDA graph; us/step
     over replays, L2 flushed.  Also times each stage alone (eager launches,
@@ -440,7 +471,7 @@ def measure_full_step(dev, args, flush, workload="full_step"):
     from deepseek_sparse_attention_mqa_gb300 import inputs
     from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
     case = inputs.make_case(workload, device=dev)
-    st = SparseAttentionStep(case, with_mla=True)
+    st = SparseAttentionStep(case, with_mla=True, fused=fused)
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -465,21 +496,29 @@ def measure_full_step(dev, args, flush, workload="full_step"):
         if i >= 3:
             times.append(e0.elapsed_time(e1) * 1e3)
     # per-stage device time, eager (one chunk: decode rows fit the logits budget)
-    stage = {"indexer": [], "topk": [], "mla": []}
+    stage = {"indexer": [], "topk": [], "mla": []} if not fused else {"score_topk": [], "mla": []}
     (rb, re), = [(a, b) for a, b in st.chunks if b > a]
     for i in range(n):
         flush(i)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         ev[0].record(stream)
-        st.indexer_chunk(rb, re)
-        ev[1].record(stream)
-        st.topk_chunk(rb, re)
-        ev[2].record(stream)
+        if fused:
+            st.score_topk_chunk(rb, re)
+            ev[1].record(stream)
+            ev[2].record(stream)
+        else:
+            st.indexer_chunk(rb, re)
+            ev[1].record(stream)
+            st.topk_chunk(rb, re)
+            ev[2].record(stream)
         st.mla()
         ev[3].record(stream)
         ev[3].synchronize()
-        stage["indexer"].append(ev[0].elapsed_time(ev[1]) * 1e3)
-        stage["topk"].append(ev[1].elapsed_time(ev[2]) * 1e3)
+        if fused:
+            stage["score_topk"].append(ev[0].elapsed_time(ev[1]) * 1e3)
+        else:
+            stage["indexer"].append(ev[0].elapsed_time(ev[1]) * 1e3)
+            stage["topk"].append(ev[1].elapsed_time(ev[2]) * 1e3)
         stage["mla"].append(ev[2].elapsed_time(ev[3]) * 1e3)
     status = st.device_status()
     # sparse MLA tensor work: QK^T over d_qk and PV over d_v for every (row, head, selected token)
@@ -488,7 +527,7 @@ def measure_full_step(dev, args, flush, workload="full_step"):
     _, bf16, _, src = measured_peaks()
     return {"workload": "full sparse-attention decode step: batch 64, indexer %d heads x %d FP8 page 64, "
                         "lens U[8192,131072], top-k 2048, sparse MLA 128 heads q/k 576 v 512 FP8 latent"
-                        % (case.num_heads, case.head_dim),
+                        % (case.num_heads, case.head_dim), "fused_score_topk": fused,
             "us_per_step_median": round(statistics.median(times), 2),
             "us_per_step_mean": round(statistics.mean(times), 2), "replays": n,
             "stage_us_median": {k: round(statistics.median(v), 2) for k, v in stage.items()},
@@ -592,6 +631,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-full-step", action="store_true")
     ap.add_argument("--skip-configs", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="headline step with the fused score + top-k launch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

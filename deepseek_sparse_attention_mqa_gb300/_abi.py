@@ -23,6 +23,7 @@ EXPORTS = (
     "dsa_indexer_build_schedule", "indexer_mqa_logits_paged", "dsa_topk_workspace_bytes",
     "indexer_topk", "dsa_sparse_mla_workspace_bytes", "sparse_mla_decode", "dsa_get_device_status",
     "indexer_mqa_logits_paged_noalloc", "dsa_wait_selftest", "dsa_kv_quantize_scatter",
+    "dsa_score_topk_workspace_bytes", "indexer_score_topk",
 )
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
@@ -97,6 +98,12 @@ def lib():
         L.sparse_mla_decode.argtypes = [_vp, _i, _i, _i, _i, ctypes.c_float,
                                         ctypes.POINTER(PagedCache), _vp, _i, _vp, _i64, _i, _vp,
                                         _vp, _vp, _sz, _vp, _vp]
+        L.dsa_score_topk_workspace_bytes.restype = _sz
+        L.dsa_score_topk_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+        L.indexer_score_topk.restype = _i
+        L.indexer_score_topk.argtypes = [
+            _vp, _vp, _i, _vp, _i, ctypes.POINTER(PagedCache), _vp, _i, _i, _i, _i, _vp, _sz,
+            _vp, _i64, _i, _i, _vp, _i64, _vp, _vp, _sz, _vp, _vp]
         L.dsa_kv_quantize_scatter.restype = _i
         L.dsa_kv_quantize_scatter.argtypes = [_vp, _i, _i64, _i, _vp, ctypes.POINTER(PagedCache), _vp, _vp]
         L.dsa_wait_selftest.restype = _i
@@ -163,6 +170,23 @@ def mqa_logits(q, q_scales, fmt, weights, num_heads, cache: PagedCache, context_
 
 
 INLINE_UNITS = 256      # kInlineUnits of the library
+
+
+def score_topk_workspace_bytes(batch, next_n, num_heads, row_begin, row_end) -> int:
+    return int(lib().dsa_score_topk_workspace_bytes(batch, next_n, num_heads, row_begin, row_end))
+
+
+def score_topk(q, q_scales, fmt, weights, num_heads, cache: PagedCache, context_lens, batch, next_n,
+               row_begin, row_end, sched, logits, logits_width, k, idx, count, workspace, status=None,
+               stream=None):
+    """indexer_score_topk: logits and the per-row top-k in one launch.
+    ``workspace`` must be zero before the first call (the call leaves it zero)."""
+    _check(lib().indexer_score_topk(
+        _ptr(q), _ptr(q_scales), int(fmt), _ptr(weights), num_heads, ctypes.byref(cache),
+        _ptr(context_lens), batch, next_n, row_begin, row_end, _ptr(sched),
+        0 if sched is None else sched.numel() * sched.element_size(), _ptr(logits), logits.stride(0),
+        int(logits_width), int(k), _ptr(idx), idx.stride(0), _ptr(count), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)), "indexer_score_topk")
 
 
 def units_of(batch, next_n, num_heads, row_begin, row_end) -> int:

@@ -209,7 +209,7 @@ const char* dsa_status_string(dsa_status s)
 
 int dsa_last_cuda_error(void) { return g_last_cuda_error; }
 
-int dsa_version(void) { return 101; }
+int dsa_version(void) { return 102; }
 
 size_t dsa_indexer_schedule_bytes(int batch, int next_n, int num_heads, int row_begin, int row_end)
 {
@@ -241,27 +241,16 @@ dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int batch, in
                                  static_cast<int32_t*>(sched), status_dev, static_cast<cudaStream_t>(stream));
 }
 
-dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_fmt, const float* weights,
-                                    int num_heads, const dsa_paged_cache* k, const int32_t* context_lens,
-                                    int batch, int next_n, int row_begin, int row_end, const void* sched,
-                                    size_t sched_bytes, float* logits, int64_t logits_row_stride,
-                                    int logits_width, int32_t* status_dev, void* stream)
+// The logits launch shared by indexer_mqa_logits_paged and indexer_score_topk
+// (topk.k = 0: logits only); the call has passed validate_logits_call.
+static dsa_status launch_logits_call(const void* q, const void* q_scales, int q_fmt, const float* weights,
+                                     int num_heads, const dsa_paged_cache* k, const int32_t* context_lens, int batch,
+                                     int next_n, int row_begin, int row_end, int64_t units, const void* sched,
+                                     float* logits, int64_t logits_row_stride, int logits_width,
+                                     const FusedTopk& topk, int32_t* status_dev, void* stream)
 {
-    int64_t units = 0;
-    dsa_status st = validate_logits_call(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n,
-                                         row_begin, row_end, logits, logits_row_stride, logits_width, &units);
-    if (st != DSA_OK)
-        return st;
-    if (sched && !aligned16(sched))
-        return DSA_ERR_INVALID_ARG;
-    if (sched && sched_bytes < static_cast<size_t>(sched_bytes_for_units(units)))
-        return DSA_ERR_CAPACITY;
-    if (!sched && units > kInlineUnits)      // the kernels build at most kInlineUnits units themselves
-        return DSA_ERR_CAPACITY;
-    if (row_end == row_begin)
-        return DSA_OK;
     DeviceInfo dev;
-    st = current_device(&dev);
+    const dsa_status st = current_device(&dev);
     if (st != DSA_OK)
         return st;
     LogitsArgs a;
@@ -282,9 +271,77 @@ dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_f
     a.logits_row_stride = logits_row_stride;
     a.logits_width = logits_width;
     a.status = status_dev;
+    a.topk = topk;
     if (q_fmt == DSA_KV_FP8_E4M3)
         return launch_logits_fp8(a, dev, static_cast<cudaStream_t>(stream));
     return launch_logits_mxfp4(a, dev, static_cast<cudaStream_t>(stream));
+}
+
+dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales, int q_fmt, const float* weights,
+                                    int num_heads, const dsa_paged_cache* k, const int32_t* context_lens,
+                                    int batch, int next_n, int row_begin, int row_end, const void* sched,
+                                    size_t sched_bytes, float* logits, int64_t logits_row_stride,
+                                    int logits_width, int32_t* status_dev, void* stream)
+{
+    int64_t units = 0;
+    dsa_status st = validate_logits_call(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n,
+                                         row_begin, row_end, logits, logits_row_stride, logits_width, &units);
+    if (st != DSA_OK)
+        return st;
+    if (sched && !aligned16(sched))
+        return DSA_ERR_INVALID_ARG;
+    if (sched && sched_bytes < static_cast<size_t>(sched_bytes_for_units(units)))
+        return DSA_ERR_CAPACITY;
+    if (!sched && units > kInlineUnits)      // the kernels build at most kInlineUnits units themselves
+        return DSA_ERR_CAPACITY;
+    if (row_end == row_begin)
+        return DSA_OK;
+    const FusedTopk none{0, nullptr, 0, nullptr, nullptr};
+    return launch_logits_call(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n, row_begin,
+                              row_end, units, sched, logits, logits_row_stride, logits_width, none, status_dev,
+                              stream);
+}
+
+size_t dsa_score_topk_workspace_bytes(int batch, int next_n, int num_heads, int row_begin, int row_end)
+{
+    if (!row_range_ok(batch, next_n, row_begin, row_end) || num_heads < 1 || num_heads > kMaxUnitCols)
+        return 0;
+    const int64_t units = count_units(batch, next_n, unit_rows(next_n, num_heads), row_begin, row_end);
+    return static_cast<size_t>((units * 4 + 15) / 16 * 16 + 16);
+}
+
+dsa_status indexer_score_topk(const void* q, const void* q_scales, int q_fmt, const float* weights, int num_heads,
+                              const dsa_paged_cache* k, const int32_t* context_lens, int batch, int next_n,
+                              int row_begin, int row_end, const void* sched, size_t sched_bytes, float* logits,
+                              int64_t logits_row_stride, int logits_width, int topk, int32_t* idx,
+                              int64_t idx_row_stride, int32_t* count, void* workspace, size_t ws_bytes,
+                              int32_t* status_dev, void* stream)
+{
+    int64_t units = 0;
+    dsa_status st = validate_logits_call(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n,
+                                         row_begin, row_end, logits, logits_row_stride, logits_width, &units);
+    if (st != DSA_OK)
+        return st;
+    if (topk < 1 || topk > 16384)
+        return DSA_ERR_UNSUPPORTED;
+    if (!idx || idx_row_stride < topk || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+        return DSA_ERR_INVALID_ARG;
+    // the selection streams logits rows with 16-byte loads
+    if (!aligned16(logits) || logits_row_stride % 4 != 0)
+        return DSA_ERR_INVALID_ARG;
+    if (sched && !aligned16(sched))
+        return DSA_ERR_INVALID_ARG;
+    if (sched && sched_bytes < static_cast<size_t>(sched_bytes_for_units(units)))
+        return DSA_ERR_CAPACITY;
+    if (!sched && units > kInlineUnits)
+        return DSA_ERR_CAPACITY;
+    if (ws_bytes < dsa_score_topk_workspace_bytes(batch, next_n, num_heads, row_begin, row_end))
+        return DSA_ERR_CAPACITY;
+    if (row_end == row_begin)
+        return DSA_OK;
+    const FusedTopk f{topk, idx, idx_row_stride, count, static_cast<int32_t*>(workspace)};
+    return launch_logits_call(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n, row_begin,
+                              row_end, units, sched, logits, logits_row_stride, logits_width, f, status_dev, stream);
 }
 
 size_t dsa_topk_workspace_bytes(int rows, int logits_width, int k)

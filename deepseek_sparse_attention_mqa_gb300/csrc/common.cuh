@@ -115,6 +115,15 @@ __device__ __forceinline__ void unit_rows_of(int u, int next_n, int G, int row_b
     *nrows = min(G, hi - *first_row);
 }
 
+// Top-k outputs of a fused indexer score + top-k launch (k = 0: logits only).
+struct FusedTopk {
+    int k;
+    int32_t* idx;           // [rows, idx_stride] int32, row r - row_begin
+    int64_t idx_stride;     // elements
+    int32_t* count;         // nullable, [rows]
+    int32_t* counters;      // [num_units] int32 workspace: zero on entry, zero again on exit
+};
+
 // Order-preserving map of an fp32 bit pattern to uint32 (larger float -> larger
 // key).  -0 is mapped like +0 so that equal values get equal keys.
 __host__ __device__ __forceinline__ uint32_t float_key(uint32_t bits)

@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "../../include/dsa.h"
+#include "common.cuh"
 
 namespace dsa {
 
@@ -61,6 +62,7 @@ struct LogitsArgs {
     int64_t logits_row_stride;
     int logits_width;
     int32_t* status;
+    FusedTopk topk;             // k = 0: logits only
 };
 dsa_status launch_logits_fp8(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 dsa_status launch_logits_mxfp4(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_t stream);

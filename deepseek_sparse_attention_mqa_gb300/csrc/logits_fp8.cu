@@ -40,6 +40,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "fused_topk.cuh"
 #include "host.h"
 #include "logits_common.cuh"
 #include "ptx.cuh"
@@ -98,6 +99,7 @@ struct LogitsParams {
     int n_acc;          // super-tile accumulators (n_acc * R * acc_cols <= 512)
     int n_grp;          // active epilogue warpgroups (divides n_acc)
     uint32_t q_buf_bytes;
+    FusedTopk topk;     // fused top-k outputs (kernels instantiated with kFuse)
 };
 
 template <int D>
@@ -130,7 +132,7 @@ __host__ __device__ __forceinline__ SmemMap smem_map(int D, int R, int stages, u
     return m;
 }
 
-template <int D, int H>
+template <int D, int H, bool kFuse>
 __global__ void __launch_bounds__(Fp8Roles<H>::kThreads, 1)
 logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const LogitsParams p)
@@ -187,8 +189,34 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
     const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total_tiles) / gridDim.x);
     const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total_tiles) / gridDim.x);
-    if (t0 >= t1 || p.num_units == 0)
+    // the fused top-k phase's view of this launch (its shared memory is the
+    // scoring stages', free once the CTA's tiles are done)
+    auto phase_args = [&](bool has_tiles, int u0) {
+        FusedPhaseArgs fa;
+        fa.units = units;
+        fa.num_units = p.num_units;
+        fa.total_tiles = total_tiles;
+        fa.t0 = t0;
+        fa.t1 = t1;
+        fa.R = p.R;
+        fa.u0 = u0;
+        fa.has_tiles = has_tiles;
+        fa.logits = p.logits;
+        fa.logits_stride = p.logits_stride;
+        fa.logits_width = p.logits_width;
+        fa.next_n = p.next_n;
+        fa.row_begin = p.row_begin;
+        fa.context_lens = p.context_lens;
+        fa.status = p.status;
+        fa.smem = smem;
+        fa.smem_bytes = mp.bar_off;
+        return fa;
+    };
+    if (t0 >= t1 || p.num_units == 0) {
+        if constexpr (kFuse)
+            fused_topk_phase(phase_args(false, 0), p.topk);
         return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -625,6 +653,11 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         atomicOr(p.status, DSA_DEV_TIMEOUT);
     if (warp == kProd)
         tmem_dealloc(tmem_base, p.n_acc * p.R * p.acc_cols);
+    if constexpr (kFuse) {
+        // outputs are invalid after a timeout (DSA_DEV_TIMEOUT is set): no selection
+        if (!*s_abort)
+            fused_topk_phase(phase_args(true, u0), p.topk);
+    }
 }
 
 constexpr int lcm2(int a, int b)
@@ -697,6 +730,8 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     const SmemMap mp = smem_map(D, R, stages, q_buf_bytes, w_cols, kEpiWarps, inline_units);
     if (static_cast<int>(mp.total) > budget || n_acc % lcm2(kMma, n_grp) != 0)
         return DSA_ERR_UNSUPPORTED;
+    if (a.topk.k > 0 && mp.bar_off < fused_phase_min_bytes())
+        return DSA_ERR_UNSUPPORTED;
     const int smem_bytes = static_cast<int>(mp.total) + 1024;
 
     LogitsParams p;
@@ -729,8 +764,9 @@ dsa_status launch_fp8_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     p.n_acc = n_acc;
     p.n_grp = n_grp;
     p.q_buf_bytes = q_buf_bytes;
+    p.topk = a.topk;
 
-    auto kern = logits_fp8_kernel<D, H>;
+    auto kern = a.topk.k > 0 ? logits_fp8_kernel<D, H, true> : logits_fp8_kernel<D, H, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e);

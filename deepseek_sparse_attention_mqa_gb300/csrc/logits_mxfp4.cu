@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "host.h"
+#include "fused_topk.cuh"
 #include "logits_common.cuh"
 #include "ptx.cuh"
 
@@ -95,6 +96,7 @@ struct Mx4Params {
     int n_mma;                 // active MMA warps (divides n_acc)
     int n_grp;                 // active epilogue groups (divides n_acc)
     uint32_t q_buf_bytes;
+    FusedTopk topk;            // fused top-k outputs (kernels instantiated with kFuse)
 };
 
 template <int D>
@@ -168,7 +170,7 @@ __device__ __forceinline__ void widen_row(const uint8_t* src, uint8_t* tile, int
     }
 }
 
-template <int D, int H>
+template <int D, int H, bool kFuse>
 __global__ void __launch_bounds__(kThreads, 1)
 logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
 {
@@ -229,8 +231,34 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
     }
     const int t0 = static_cast<int>((static_cast<long long>(blockIdx.x) * total_tiles) / gridDim.x);
     const int t1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * total_tiles) / gridDim.x);
-    if (t0 >= t1 || p.num_units == 0)
+    // the fused top-k phase's view of this launch (its shared memory is the
+    // scoring stages', free once the CTA's tiles are done)
+    auto phase_args = [&](bool has_tiles, int u0) {
+        FusedPhaseArgs fa;
+        fa.units = units;
+        fa.num_units = p.num_units;
+        fa.total_tiles = total_tiles;
+        fa.t0 = t0;
+        fa.t1 = t1;
+        fa.R = p.R;
+        fa.u0 = u0;
+        fa.has_tiles = has_tiles;
+        fa.logits = p.logits;
+        fa.logits_stride = p.logits_stride;
+        fa.logits_width = p.logits_width;
+        fa.next_n = p.next_n;
+        fa.row_begin = p.row_begin;
+        fa.context_lens = p.context_lens;
+        fa.status = p.status;
+        fa.smem = smem;
+        fa.smem_bytes = mp.bar;
+        return fa;
+    };
+    if (t0 >= t1 || p.num_units == 0) {
+        if constexpr (kFuse)
+            fused_topk_phase(phase_args(false, 0), p.topk);
         return;
+    }
 
     const uint32_t acc_stride = static_cast<uint32_t>(R * NB) * p.acc_cols;   // TMEM columns per super-tile
     if (threadIdx.x == 0) {
@@ -686,6 +714,11 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
         atomicOr(p.status, DSA_DEV_TIMEOUT);
     if (warp == kProd)
         tmem_dealloc(tmem_base, p.n_acc * acc_stride);
+    if constexpr (kFuse) {
+        // outputs are invalid after a timeout (DSA_DEV_TIMEOUT is set): no selection
+        if (!*s_abort)
+            fused_topk_phase(phase_args(true, u0), p.topk);
+    }
 }
 
 template <int D, int H>
@@ -728,6 +761,9 @@ dsa_status launch_mx4_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
         return DSA_ERR_UNSUPPORTED;
     const int smem_bytes =
         static_cast<int>(mx4_smem<D>(R, raw_stages, conv_stages, q_buf_bytes, w_cols, inline_units).total) + 1024;
+    if (a.topk.k > 0 &&
+        mx4_smem<D>(R, raw_stages, conv_stages, q_buf_bytes, w_cols, inline_units).bar < fused_phase_min_bytes())
+        return DSA_ERR_UNSUPPORTED;
 
     CUtensorMap tm_k;
     {
@@ -776,8 +812,9 @@ dsa_status launch_mx4_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     p.n_mma = n_mma;
     p.n_grp = n_grp;
     p.q_buf_bytes = q_buf_bytes;
+    p.topk = a.topk;
 
-    auto kern = logits_mxfp4_kernel<D, H>;
+    auto kern = a.topk.k > 0 ? logits_mxfp4_kernel<D, H, true> : logits_mxfp4_kernel<D, H, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e);

@@ -66,7 +66,8 @@ class StepInputs:
 
 class SparseAttentionStep:
     def __init__(self, case: Case, with_mla: bool = True, budget_bytes: int = LOGITS_BUDGET_BYTES,
-                 rows_per_chunk: int | None = None, inline_schedule: bool | None = None):
+                 rows_per_chunk: int | None = None, inline_schedule: bool | None = None,
+                 fused: bool = False):
         dev = case.q.device
         assert dev.type == "cuda", "SparseAttentionStep needs the case on a CUDA device"
         self.case = case
@@ -96,6 +97,13 @@ class SparseAttentionStep:
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         tw = _abi.topk_workspace_bytes(self.rows_per_chunk, self.width, c.topk)
         self.topk_ws = torch.empty((max(tw, 16),), dtype=torch.uint8, device=dev)
+        # fused score + top-k: one launch per chunk; its per-unit counters start at
+        # zero and every call leaves them at zero
+        self.fused = bool(fused)
+        if self.fused:
+            fw = max(_abi.score_topk_workspace_bytes(c.batch, c.next_n, c.num_heads, rb, re)
+                     for rb, re in self.chunks)
+            self.fused_ws = torch.zeros(((fw + 15) // 16 * 4,), dtype=torch.int32, device=dev)
         self.with_mla = bool(with_mla and c.latent is not None)
         if self.with_mla:
             lat = c.latent
@@ -119,6 +127,19 @@ class SparseAttentionStep:
                         c.context_lens, c.batch, c.next_n, rb, re, None if inline else self.sched,
                         self.logits, self.width, self.status, stream)
 
+    def score_topk_chunk(self, rb: int, re: int, stream=None):
+        """Logits and top-k of rows [rb, re) in one fused launch (plus the
+        schedule launch for chunks of more than INLINE_UNITS units)."""
+        c = self.case
+        inline = self.inline.get((rb, re), False)
+        if not inline:
+            _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, self.sched,
+                                self.status, stream)
+        _abi.score_topk(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, self.kcache, c.context_lens,
+                        c.batch, c.next_n, rb, re, None if inline else self.sched, self.logits,
+                        self.width, c.topk, self.idx[rb:re], self.count[rb:re], self.fused_ws,
+                        self.status, stream)
+
     def topk_chunk(self, rb: int, re: int, stream=None):
         c = self.case
         _abi.topk(self.logits, self.width, c.context_lens, c.batch, c.next_n, rb, re, c.topk,
@@ -132,13 +153,17 @@ class SparseAttentionStep:
     def run(self, stream=None):
         for rb, re in self.chunks:
             if re > rb:
-                self.indexer_chunk(rb, re, stream)
-                self.topk_chunk(rb, re, stream)
+                if self.fused:
+                    self.score_topk_chunk(rb, re, stream)
+                else:
+                    self.indexer_chunk(rb, re, stream)
+                    self.topk_chunk(rb, re, stream)
         if self.with_mla:
             self.mla(stream)
 
     def launches_per_step(self) -> int:
-        n = sum(2 if self.inline.get((rb, re), False) else 3 for rb, re in self.chunks if re > rb)
+        per = 1 if self.fused else 2
+        n = sum(per + (0 if self.inline.get((rb, re), False) else 1) for rb, re in self.chunks if re > rb)
         return n + (1 if self.with_mla else 0)
 
     def device_status(self) -> int:

@@ -108,7 +108,8 @@ DSA_API const char* dsa_status_string(dsa_status status);
 DSA_API int dsa_last_cuda_error(void);
 
 /* Library ABI version (major*100 + minor).  1.01: indexer_mqa_logits_paged
- * accepts sched = NULL for calls of at most 256 work units. */
+ * accepts sched = NULL for calls of at most 256 work units.  1.02: fused
+ * indexer_score_topk, dsa_kv_quantize_scatter, dsa_wait_selftest. */
 DSA_API int dsa_version(void);
 
 /*
@@ -176,6 +177,43 @@ DSA_API dsa_status indexer_mqa_logits_paged(const void* q, const void* q_scales,
                                     const void* sched, size_t sched_bytes, float* logits,
                                     int64_t logits_row_stride, int logits_width,
                                     int32_t* status_dev, void* stream);
+
+/*
+ * Fused indexer score + top-k ("feat(deepseek_v4): Add fp4 indexer for dsv4",
+ * commit notes: indexer_score_topk scores the paged K cache and returns each
+ * row's top-k token positions in one op).  Computes exactly what
+ * indexer_mqa_logits_paged() followed by indexer_topk() compute -- the same
+ * logits in `logits`, the same index sets in idx / count -- in ONE launch: the
+ * block that scores a work unit's last outstanding tiles selects that unit's
+ * rows from the logits just written, while the other blocks keep scoring.
+ *
+ * Arguments as indexer_mqa_logits_paged() (with logits 16-byte aligned and
+ * logits_row_stride a multiple of 4) plus:
+ * topk:     k, 1 <= k <= 16384.
+ * idx:      int32 [rows, idx_row_stride >= k] (ELEMENTS), row r - row_begin:
+ *           the positions of the row's min(k, vis) largest logits (any order;
+ *           among equal logits the lower position wins), then -1.
+ * count:    nullable int32 [rows]: min(k, vis).
+ * workspace: device buffer of dsa_score_topk_workspace_bytes(...) bytes, 4-byte
+ *           aligned, ALL ZERO before the first call (e.g. cudaMemset once after
+ *           allocating it).  Every call that completes leaves it zero again, so
+ *           it can be reused by the next call (and by graph replays) without
+ *           clearing; after a call that reported DSA_DEV_TIMEOUT it must be
+ *           cleared again.  Calls that overlap on the GPU need separate
+ *           workspaces.
+ * Errors: as indexer_mqa_logits_paged(); UNSUPPORTED (k); INVALID_ARG (idx,
+ *         idx_row_stride, workspace); CAPACITY (ws_bytes).
+ */
+DSA_API size_t dsa_score_topk_workspace_bytes(int batch, int next_n, int num_heads, int row_begin,
+                                              int row_end);
+DSA_API dsa_status indexer_score_topk(const void* q, const void* q_scales, int q_fmt,
+                                      const float* weights, int num_heads, const dsa_paged_cache* k,
+                                      const int32_t* context_lens, int batch, int next_n,
+                                      int row_begin, int row_end, const void* sched,
+                                      size_t sched_bytes, float* logits, int64_t logits_row_stride,
+                                      int logits_width, int topk, int32_t* idx,
+                                      int64_t idx_row_stride, int32_t* count, void* workspace,
+                                      size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /*
  * Allocation-free variant of indexer_mqa_logits_paged() (no counterpart on the
