@@ -312,3 +312,92 @@ def to_device(case: Case, device) -> Case:
             p2.scales = None if p.scales is None else p.scales.to(dev)
             setattr(c, f, p2)
     return c
+
+
+@dataclass
+class SwaCase:
+    """Sparse MLA over two latent caches: a compressed ("sparse") cache whose
+    entries are selected per row by ``idx`` (the first ``topk_lens[r]`` of
+    them), and a sliding-window cache of the sequence's tokens.  Rows of
+    sequence b are [cum_q[b], cum_q[b + 1]); ``seq_lens`` counts each sequence's
+    tokens including its new ones."""
+    batch: int
+    rows: int
+    heads: int
+    d_qk: int
+    d_v: int
+    fmt: int
+    softmax_scale: float
+    k: int
+    window: int
+    seq_lens: torch.Tensor          # [batch] int32
+    cum_q: torch.Tensor             # [batch + 1] int32
+    sparse: Paged
+    sparse_bt: torch.Tensor         # [batch, max_pages] int32
+    swa: Paged
+    swa_bt: torch.Tensor            # [batch, max_pages] int32
+    idx: torch.Tensor               # [rows, k] int32, -1 padding
+    topk_lens: torch.Tensor         # [rows] int32
+    q: torch.Tensor                 # [rows, heads, d_qk] bf16
+
+
+def _latent_pool(pages, P, D, fmt, g, dev):
+    if fmt == FMT_FP8:
+        v = _to_e4m3_bytes(torch.randn((pages, P, D), generator=g, device=dev)).reshape(pages, P * D).contiguous()
+        s = (torch.rand((pages, P), generator=g, device=dev) * 1.5 + 0.5).contiguous()
+        return Paged(FMT_FP8, D, P, pages, v, P * D, D, s.view(torch.uint8).reshape(pages, P * 4), P * 4, 4)
+    v = torch.randn((pages, P, D), generator=g, device=dev).to(torch.bfloat16)
+    return Paged(FMT_BF16, D, P, pages, v.view(torch.uint8).reshape(pages, P * D * 2).contiguous(), P * D * 2,
+                 D * 2, None, 0, 0)
+
+
+def _pages_for(lengths, P, gc):
+    """Block table [batch, max_pages] over a shuffled pool covering `lengths`."""
+    per = [(int(l) + P - 1) // P for l in lengths]
+    pool = max(1, sum(per))
+    perm = torch.randperm(pool, generator=gc)
+    bt = torch.full((len(per), max(1, max(per) if per else 1)), -1, dtype=torch.int32)
+    pos = 0
+    for b, n in enumerate(per):
+        bt[b, :n] = perm[pos:pos + n].to(torch.int32)
+        pos += n
+    return bt, pool
+
+
+def make_swa_case(seed=0, device="cpu", seq_lens=(300, 1000, 70), q_lens=(1, 3, 2), heads=16, d_qk=576,
+                  d_v=512, fmt=FMT_FP8, page_kv=64, swa_page_kv=64, k=128, window=128, ratio=4,
+                  scale=None) -> SwaCase:
+    """Random two-cache sparse MLA workload: each sequence's sparse cache holds
+    seq_len // ratio + 1 entries; each row selects k of them at random (a few
+    slots -1) and keeps a random leading count topk_lens[r] in [0, k]."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    gc = torch.Generator()
+    gc.manual_seed(int(seed))
+    L = torch.tensor(list(seq_lens), dtype=torch.int32)
+    ql = list(q_lens)
+    B = len(ql)
+    cum = torch.zeros(B + 1, dtype=torch.int32)
+    cum[1:] = torch.cumsum(torch.tensor(ql, dtype=torch.int32), 0)
+    R = int(cum[-1])
+    n_sparse = [int(l) // ratio + 1 for l in L.tolist()]
+    sbt, spool = _pages_for(n_sparse, page_kv, gc)
+    wbt, wpool = _pages_for(L.tolist(), swa_page_kv, gc)
+    idx = torch.full((R, k), -1, dtype=torch.int32)
+    tl = torch.zeros(R, dtype=torch.int32)
+    for b in range(B):
+        for r in range(int(cum[b]), int(cum[b + 1])):
+            take = min(k, n_sparse[b])
+            sel = torch.randperm(n_sparse[b], generator=gc)[:take].to(torch.int32)
+            idx[r, :take] = sel
+            if take > 4:
+                idx[r, torch.randint(0, take, (2,), generator=gc)] = -1
+            tl[r] = int(torch.randint(0, k + 1, (1,), generator=gc))
+    sparse = _latent_pool(spool, page_kv, d_qk, fmt, g, dev)
+    swa = _latent_pool(wpool, swa_page_kv, d_qk, fmt, g, dev)
+    q = torch.randn((R, heads, d_qk), generator=g, device=dev).to(torch.bfloat16).contiguous()
+    return SwaCase(batch=B, rows=R, heads=heads, d_qk=d_qk, d_v=d_v, fmt=fmt,
+                   softmax_scale=float(scale if scale is not None else 1.0 / math.sqrt(192)), k=k, window=window,
+                   seq_lens=L.to(dev), cum_q=cum.to(dev), sparse=sparse, sparse_bt=sbt.to(dev), swa=swa,
+                   swa_bt=wbt.to(dev), idx=idx.to(dev), topk_lens=tl.to(dev), q=q)

@@ -20,6 +20,10 @@ and the passages they follow:
 * ``topk`` -- full sort, descending logit, ties by ascending index, -1 padding.
 * ``sparse_mla`` -- softmax attention over the selected latent tokens with an
   fp32-style LSE output ("Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels").
+* ``sparse_mla_swa`` -- sparse MLA over the selected entries of one latent
+  cache plus a sliding window of another in one softmax, with per-row top-k
+  lengths and cumulative query lengths ("Add DeepSeek V4 sparse MLA TRTLLM-GEN
+  kernels": sliding_window_kv_cache, sparse_topk_lens, cum_seq_lens_q).
 * ``encode_e4m3 / encode_e2m1 / quantize_scatter`` -- writing new K rows into
   the paged FP8 (per-token fp32 scale) or MXFP4 (ue8m0 per 32 elements) cache
   through a slot mapping ("feat(deepseek_v4): Add fp4 indexer for dsv4": the FP4
@@ -100,6 +104,13 @@ def _load():
             _c_u16p, _int, _int, _int, _int, ctypes.c_double, _int, _c_u8p, _i64, _i64,
             _c_u8p, _i64, _i64, _c_i32p, _i64, _int, _int, _int, _c_i32p, _int,
             _c_i32p, _i64, _int, _c_f64p, _c_f64p]
+        lib.dsa_oracle_sparse_mla_swa.restype = _int
+        lib.dsa_oracle_sparse_mla_swa.argtypes = [
+            _c_u16p, _int, _int, _int, _int, ctypes.c_double, _int,
+            _c_u8p, _i64, _i64, _c_u8p, _i64, _i64, _c_i32p, _i64, _int, _int, _int,
+            _c_i32p, _i64, _int, _c_i32p,
+            _c_u8p, _i64, _i64, _c_u8p, _i64, _i64, _c_i32p, _i64, _int, _int, _int, _int,
+            _c_i32p, _c_i32p, _int, _int, _c_f64p, _c_f64p]
         lib.dsa_oracle_encode_e4m3.restype = ctypes.c_uint8
         lib.dsa_oracle_encode_e4m3.argtypes = [ctypes.c_float]
         lib.dsa_oracle_encode_e2m1.restype = ctypes.c_uint8
@@ -308,3 +319,42 @@ def quantize_scatter(k, slots, fmt, cache: PagedBytes):
         _ptr(cache.values, ctypes.c_uint8), cache.vps, cache.vts,
         _ptr(cache.scales, ctypes.c_uint8), cache.sps, cache.sts, cache.page_kv, cache.num_pages)
     _check(rc, "quantize_scatter")
+
+
+def sparse_mla_swa(q_bf16, softmax_scale, fmt, cache: PagedBytes, idx, d_v, seq_lens, topk_lens=None,
+                   swa: PagedBytes = None, window=0, cum_q=None, next_n=1):
+    """(out [rows, Hq, d_v] fp64, lse [rows, Hq] fp64) of sparse MLA over the
+    first topk_lens[r] entries of idx (cache ``cache``) plus the last
+    min(window, vis) visible positions of the window cache ``swa``, in one
+    softmax.  Rows map to sequences through cum_q ([batch + 1]) or r / next_n."""
+    lib = _load()
+    if hasattr(q_bf16, "dtype") and str(q_bf16.dtype) == "torch.bfloat16":
+        q_bf16 = q_bf16.view(__import__("torch").int16)
+    q = _np(q_bf16, np.uint16)
+    rows, Hq, d_qk = q.shape
+    ix = _np(idx, np.int32).reshape(rows, -1)
+    k = ix.shape[1]
+    sl = _np(seq_lens, np.int32).reshape(-1)
+    batch = sl.shape[0]
+    tl = None if topk_lens is None else _np(topk_lens, np.int32).reshape(-1)
+    cq = None if cum_q is None else _np(cum_q, np.int32).reshape(-1)
+    out = np.zeros((rows, Hq, d_v), dtype=np.float64)
+    lse = np.zeros((rows, Hq), dtype=np.float64)
+    bt = cache.block_table
+    sc = cache.scales if cache.scales is not None else np.zeros(16, np.uint8)
+    if swa is not None:
+        wbt = swa.block_table
+        wsc = swa.scales if swa.scales is not None else np.zeros(16, np.uint8)
+        wargs = (_ptr(swa.values, ctypes.c_uint8), swa.vps, swa.vts, _ptr(wsc, ctypes.c_uint8), swa.sps, swa.sts,
+                 _ptr(wbt, ctypes.c_int32), wbt.shape[1], wbt.shape[1], swa.page_kv, swa.num_pages, int(window))
+    else:
+        wargs = (None, 0, 0, None, 0, 0, None, 0, 0, 0, 0, 0)
+    rc = lib.dsa_oracle_sparse_mla_swa(
+        _ptr(q, ctypes.c_uint16), rows, Hq, d_qk, int(d_v), float(softmax_scale), int(fmt),
+        _ptr(cache.values, ctypes.c_uint8), cache.vps, cache.vts, _ptr(sc, ctypes.c_uint8), cache.sps, cache.sts,
+        _ptr(bt, ctypes.c_int32), bt.shape[1], bt.shape[1], cache.page_kv, cache.num_pages,
+        _ptr(ix, ctypes.c_int32), k, k, None if tl is None else _ptr(tl, ctypes.c_int32),
+        *wargs, _ptr(sl, ctypes.c_int32), None if cq is None else _ptr(cq, ctypes.c_int32), batch, int(next_n),
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    _check(rc, "sparse_mla_swa")
+    return out, lse

@@ -414,6 +414,159 @@ int dsa_oracle_sparse_mla(const uint16_t* q, int rows, int Hq, int d_qk, int d_v
     return err;
 }
 
+/* ------------------------------------ sparse MLA with a sliding window */
+
+/* Latent row of logical position s of sequence b in a paged cache, decoded to
+ * fp64 (e4m3 * token scale, or bf16) into c[0 : d).  Returns ORACLE_ERR_PAGE
+ * if the block-table entry is missing or outside the pool. */
+static int latent_row(int fmt, const uint8_t* vals, int64_t vps, int64_t vts, const uint8_t* scs, int64_t sps,
+                      int64_t sts, const int32_t* bt, int64_t bt_stride, int max_pages, int page_kv, int num_pages,
+                      int b, int s, int d, double* c)
+{
+    int page, e;
+    const uint8_t* row;
+    double tok_scale = 1.0;
+    if (page_of(bt, bt_stride, max_pages, page_kv, num_pages, b, s, &page))
+        return ORACLE_ERR_PAGE;
+    row = vals + (int64_t)page * vps + (int64_t)(s % page_kv) * vts;
+    if (fmt == 0)
+        tok_scale = (double)load_f32(scs + (int64_t)page * sps + (int64_t)(s % page_kv) * sts);
+    for (e = 0; e < d; ++e) {
+        if (fmt == 0) {
+            c[e] = dsa_oracle_e4m3(row[e]) * tok_scale;
+        } else {
+            uint16_t bits;
+            memcpy(&bits, row + 2 * e, 2);
+            c[e] = dsa_oracle_bf16(bits);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Sparse MLA decode over two latent caches in ONE softmax ("Add DeepSeek V4
+ * sparse MLA TRTLLM-GEN kernels": sparse attention over the top-k selected
+ * entries of one cache plus a sliding-window cache, dynamic per-row top-k
+ * lengths, varlen q through cumulative query lengths).  For row r:
+ *  - its sequence b and query position i: rows [cum_q[b], cum_q[b+1]) belong to
+ *    sequence b (i = r - cum_q[b], q_len = cum_q[b+1] - cum_q[b]); without
+ *    cum_q, b = r / next_n, i = r % next_n, q_len = next_n;
+ *  - its visible length in the window cache's token stream:
+ *    vis = clamp(seq_lens[b] - q_len + i + 1, 0, seq_lens[b]);
+ *  - its keys: the first min(k, topk_lens[r]) entries of idx[r] that are >= 0
+ *    (topk_lens NULL: all k), rows of the sparse cache; then the last
+ *    min(window, vis) visible positions [vis - w, vis) of the window cache
+ *    (none when wvals is NULL);
+ *  - s_j = scale * q . c_j[0:d_qk], lse = ln sum_j exp(s_j),
+ *    out = sum_j exp(s_j - lse) c_j[0:d_v]; no key: out = 0, lse = -inf.
+ * Both caches have the format fmt (0 FP8 + token scale, 2 bf16). */
+int dsa_oracle_sparse_mla_swa(const uint16_t* q, int rows, int Hq, int d_qk, int d_v, double softmax_scale,
+                              int fmt, const uint8_t* cvals, int64_t vps, int64_t vts, const uint8_t* cscales,
+                              int64_t sps, int64_t sts, const int32_t* bt, int64_t bt_stride, int max_pages,
+                              int page_kv, int num_pages, const int32_t* idx, int64_t idx_stride, int k,
+                              const int32_t* topk_lens, const uint8_t* wvals, int64_t wvps, int64_t wvts,
+                              const uint8_t* wscales, int64_t wsps, int64_t wsts, const int32_t* wbt,
+                              int64_t wbt_stride, int wmax_pages, int wpage_kv, int wnum_pages, int window,
+                              const int32_t* seq_lens, const int32_t* cum_q, int batch, int next_n, double* out,
+                              double* lse)
+{
+    int err = ORACLE_OK;
+    long r;
+    if (rows < 0 || Hq <= 0 || d_qk <= 0 || d_v <= 0 || d_v > d_qk || k < 0 || page_kv <= 0 || window < 0 ||
+        (fmt != ORACLE_FMT_FP8 && fmt != ORACLE_FMT_BF16) || (!cum_q && next_n <= 0) || batch < 0 ||
+        (wvals && wpage_kv <= 0))
+        return ORACLE_ERR_ARG;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < rows; ++r) {
+        int b, i, q_len, L, vis, kr, w, j, h, d, nkeys = 0;
+        int maxkeys = k + (wvals ? window : 0);
+        double *c, *sc;
+        if (cum_q) {
+            for (b = 0; b < batch; ++b)
+                if (r >= cum_q[b] && r < cum_q[b + 1])
+                    break;
+            if (b == batch) {
+#pragma omp atomic write
+                err = ORACLE_ERR_ARG;
+                continue;
+            }
+            i = (int)r - cum_q[b];
+            q_len = cum_q[b + 1] - cum_q[b];
+        } else {
+            b = (int)(r / next_n);
+            i = (int)(r % next_n);
+            q_len = next_n;
+        }
+        L = seq_lens ? seq_lens[b] : 0;
+        vis = dsa_oracle_visible(L, q_len, i);
+        kr = k;
+        if (topk_lens)
+            kr = topk_lens[r] < 0 ? 0 : (topk_lens[r] < k ? topk_lens[r] : k);
+        w = wvals ? (window < vis ? window : vis) : 0;
+        c = (double*)malloc(sizeof(double) * (size_t)(maxkeys > 0 ? maxkeys : 1) * (size_t)d_qk);
+        sc = (double*)malloc(sizeof(double) * (size_t)(maxkeys > 0 ? maxkeys : 1));
+        if (!c || !sc) {
+            free(c);
+            free(sc);
+#pragma omp atomic write
+            err = ORACLE_ERR_ARG;
+            continue;
+        }
+        for (j = 0; j < kr; ++j) {
+            int s = idx[r * idx_stride + j];
+            if (s < 0)
+                continue;
+            if (latent_row(fmt, cvals, vps, vts, cscales, sps, sts, bt, bt_stride, max_pages, page_kv, num_pages,
+                           b, s, d_qk, c + (size_t)nkeys * d_qk)) {
+#pragma omp atomic write
+                err = ORACLE_ERR_PAGE;
+                continue;
+            }
+            ++nkeys;
+        }
+        for (j = vis - w; j < vis; ++j) {
+            if (latent_row(fmt, wvals, wvps, wvts, wscales, wsps, wsts, wbt, wbt_stride, wmax_pages, wpage_kv,
+                           wnum_pages, b, j, d_qk, c + (size_t)nkeys * d_qk)) {
+#pragma omp atomic write
+                err = ORACLE_ERR_PAGE;
+                continue;
+            }
+            ++nkeys;
+        }
+        for (h = 0; h < Hq; ++h) {
+            const uint16_t* qh = q + ((int64_t)r * Hq + h) * d_qk;
+            double* o = out + ((int64_t)r * Hq + h) * d_v;
+            double m = -INFINITY, l = 0.0, LSE;
+            for (d = 0; d < d_v; ++d)
+                o[d] = 0.0;
+            if (nkeys == 0) {
+                lse[(int64_t)r * Hq + h] = -INFINITY;
+                continue;
+            }
+            for (j = 0; j < nkeys; ++j) {
+                double dot = 0.0;
+                for (d = 0; d < d_qk; ++d)
+                    dot += dsa_oracle_bf16(qh[d]) * c[(size_t)j * d_qk + d];
+                sc[j] = softmax_scale * dot;
+                if (sc[j] > m)
+                    m = sc[j];
+            }
+            for (j = 0; j < nkeys; ++j)
+                l += exp(sc[j] - m);
+            LSE = m + log(l);
+            lse[(int64_t)r * Hq + h] = LSE;
+            for (j = 0; j < nkeys; ++j) {
+                double pj = exp(sc[j] - LSE);
+                for (d = 0; d < d_v; ++d)
+                    o[d] += pj * c[(size_t)j * d_qk + d];
+            }
+        }
+        free(c);
+        free(sc);
+    }
+    return err;
+}
+
 /* --------------------------------------------- K-cache quantise / scatter */
 
 /* Round-half-to-even of a non-negative double to an integer (the doubles met
