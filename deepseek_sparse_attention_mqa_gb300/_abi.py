@@ -23,7 +23,7 @@ EXPORTS = (
     "dsa_indexer_build_schedule", "indexer_mqa_logits_paged", "dsa_topk_workspace_bytes",
     "indexer_topk", "dsa_sparse_mla_workspace_bytes", "sparse_mla_decode", "dsa_get_device_status",
     "indexer_mqa_logits_paged_noalloc", "dsa_wait_selftest", "dsa_kv_quantize_scatter",
-    "dsa_score_topk_workspace_bytes", "indexer_score_topk",
+    "dsa_score_topk_workspace_bytes", "indexer_score_topk", "sparse_mla_decode_swa",
 )
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
@@ -108,6 +108,10 @@ def lib():
         L.dsa_kv_quantize_scatter.argtypes = [_vp, _i, _i64, _i, _vp, ctypes.POINTER(PagedCache), _vp, _vp]
         L.dsa_wait_selftest.restype = _i
         L.dsa_wait_selftest.argtypes = [_vp, ctypes.c_int32, _i, _vp, _vp]
+        L.sparse_mla_decode_swa.restype = _i
+        L.sparse_mla_decode_swa.argtypes = [
+            _vp, _i, _i, _i, _i, ctypes.c_float, ctypes.POINTER(PagedCache), _vp, _i64, _i, _vp,
+            ctypes.POINTER(PagedCache), _i, _vp, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp, _vp]
         L.dsa_get_device_status.restype = _i
         L.dsa_get_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
         _lib = L
@@ -264,3 +268,16 @@ def kv_quantize_scatter(k_new, slot_mapping, cache: PagedCache, status=None, str
     _check(lib().dsa_kv_quantize_scatter(
         _ptr(k_new), dt, k_new.stride(0) if k_new.dim() == 2 else k_new.shape[-1], k_new.shape[0],
         _ptr(slot_mapping), ctypes.byref(cache), _ptr(status), _stream(stream)), "dsa_kv_quantize_scatter")
+
+
+def sparse_mla_swa(q_bf16, softmax_scale, cache: PagedCache, idx, k, out, lse, d_v, topk_lens=None,
+                   swa: PagedCache = None, window=0, seq_lens=None, cum_q=None, batch=0, next_n=1,
+                   status=None, stream=None):
+    """sparse_mla_decode_swa: selected entries of `cache` plus the sliding window
+    of `swa` in one softmax, per-row top-k lengths, varlen rows via cum_q."""
+    rows, heads, d_qk = q_bf16.shape
+    _check(lib().sparse_mla_decode_swa(
+        _ptr(q_bf16), rows, heads, d_qk, int(d_v), float(softmax_scale), ctypes.byref(cache), _ptr(idx),
+        idx.stride(0) if idx is not None else 0, int(k), _ptr(topk_lens),
+        None if swa is None else ctypes.byref(swa), int(window), _ptr(seq_lens), _ptr(cum_q), int(batch),
+        int(next_n), _ptr(out), _ptr(lse), None, 0, _ptr(status), _stream(stream)), "sparse_mla_decode_swa")

@@ -129,19 +129,25 @@ static bool row_range_ok(int batch, int next_n, int row_begin, int row_end)
            static_cast<int64_t>(batch) * next_n < (int64_t(1) << 31);
 }
 
-// Paged-cache checks shared by the indexer and MLA paths.
-static dsa_status check_cache(const dsa_paged_cache* c, bool need_scales)
+// Paged-cache checks shared by the indexer and MLA paths.  The indexer copies
+// whole pages with TMA (page_kv 32 or 64); the MLA gathers token by token and
+// takes any page size (e.g. a compressed cache holding a few entries per
+// physical block).
+static dsa_status check_cache(const dsa_paged_cache* c, bool need_scales, bool any_page = false)
 {
     if (!c || !c->values || !c->block_table)
         return DSA_ERR_INVALID_ARG;
-    if (c->page_kv != 32 && c->page_kv != 64)
+    if (any_page ? c->page_kv < 1 : (c->page_kv != 32 && c->page_kv != 64))
         return DSA_ERR_UNSUPPORTED;
     if (c->num_pages < 1 || c->head_dim < 1 || c->max_pages_per_seq < 1 ||
         c->bt_row_stride < c->max_pages_per_seq)
         return DSA_ERR_INVALID_ARG;
     if (!aligned16(c->values) || c->val_page_stride % 16 != 0 || c->val_page_stride <= 0)
         return DSA_ERR_INVALID_ARG;
-    if (need_scales && (!c->scales || !aligned16(c->scales) || c->sc_page_stride % 16 != 0 || c->sc_page_stride <= 0))
+    // the indexer copies token scales 16 bytes at a time; the MLA reads one fp32 per token
+    const int64_t sc_align = any_page ? 4 : 16;
+    if (need_scales && (!c->scales || (reinterpret_cast<uintptr_t>(c->scales) % sc_align) != 0 ||
+                        c->sc_page_stride % sc_align != 0 || c->sc_page_stride <= 0))
         return DSA_ERR_INVALID_ARG;
     return DSA_OK;
 }
@@ -399,6 +405,45 @@ size_t dsa_sparse_mla_workspace_bytes(int rows, int num_heads, int d_qk, int d_v
     return 0;
 }
 
+// Host checks of one MLA latent cache (fmt FP8 + token scale, or bf16).
+static dsa_status check_mla_cache(const dsa_paged_cache* kv, int d_qk)
+{
+    if (!kv)
+        return DSA_ERR_INVALID_ARG;
+    if (kv->fmt != DSA_KV_FP8_E4M3 && kv->fmt != DSA_KV_BF16)
+        return DSA_ERR_UNSUPPORTED;
+    if (kv->head_dim != d_qk)
+        return DSA_ERR_INVALID_ARG;
+    const bool fp8 = kv->fmt == DSA_KV_FP8_E4M3;
+    dsa_status st = check_cache(kv, fp8, true);
+    if (st != DSA_OK)
+        return st;
+    const int64_t row_bytes = fp8 ? d_qk : 2 * int64_t(d_qk);
+    if (kv->val_token_stride < row_bytes || kv->val_page_stride < kv->page_kv * kv->val_token_stride)
+        return DSA_ERR_INVALID_ARG;
+    if (fp8 && (kv->sc_token_stride < 4 || kv->sc_token_stride % 4 != 0))
+        return DSA_ERR_INVALID_ARG;
+    // positions and indices are tagged with bit 30 inside the kernels
+    if (static_cast<int64_t>(kv->max_pages_per_seq) * kv->page_kv >= (int64_t(1) << 30))
+        return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+static dsa_status run_sparse_mla(MlaArgs& a, void* stream)
+{
+    if (a.rows == 0)
+        return DSA_OK;
+    DeviceInfo dev;
+    const dsa_status st = current_device(&dev);
+    if (st != DSA_OK)
+        return st;
+    const bool tc_layout = aligned16(a.q) && aligned16(a.out) && a.kv->val_token_stride % 16 == 0 &&
+                           (!a.swa || a.swa->val_token_stride % 16 == 0);
+    if (sparse_mla_tc_supported(a) && tc_layout)
+        return launch_sparse_mla_tc(a, dev, static_cast<cudaStream_t>(stream));
+    return launch_sparse_mla_simt(a, static_cast<cudaStream_t>(stream));
+}
+
 dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads, int d_qk, int d_v, float softmax_scale,
                              const dsa_paged_cache* kv, const int32_t* seq_of_row, int next_n, const int32_t* idx,
                              int64_t idx_row_stride, int k, void* out_bf16, float* lse, void* workspace,
@@ -408,30 +453,14 @@ dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads, int d_
         return DSA_ERR_INVALID_ARG;
     if (d_qk < 16 || d_qk > 1024 || d_qk % 16 != 0 || d_v < 16 || d_v % 16 != 0 || d_v > d_qk || d_v > 512)
         return DSA_ERR_UNSUPPORTED;
-    if (kv->fmt != DSA_KV_FP8_E4M3 && kv->fmt != DSA_KV_BF16)
-        return DSA_ERR_UNSUPPORTED;
-    if (kv->head_dim != d_qk)
-        return DSA_ERR_INVALID_ARG;
-    const bool fp8 = kv->fmt == DSA_KV_FP8_E4M3;
-    dsa_status st = check_cache(kv, fp8);
+    dsa_status st = check_mla_cache(kv, d_qk);
     if (st != DSA_OK)
         return st;
-    const int64_t row_bytes = fp8 ? d_qk : 2 * int64_t(d_qk);
-    if (kv->val_token_stride < row_bytes || kv->val_page_stride < kv->page_kv * kv->val_token_stride)
-        return DSA_ERR_INVALID_ARG;
-    if (fp8 && (kv->sc_token_stride < 4 || kv->sc_token_stride % 4 != 0))
-        return DSA_ERR_INVALID_ARG;
     if (rows > 0 && (!q_bf16 || !idx || !out_bf16 || !lse || idx_row_stride < k))
         return DSA_ERR_INVALID_ARG;
     if (ws_bytes < dsa_sparse_mla_workspace_bytes(rows, num_heads, d_qk, d_v, k))
         return DSA_ERR_CAPACITY;
-    if (rows == 0)
-        return DSA_OK;
-    DeviceInfo dev;
-    st = current_device(&dev);
-    if (st != DSA_OK)
-        return st;
-    MlaArgs a;
+    MlaArgs a{};
     a.q = q_bf16;
     a.rows = rows;
     a.num_heads = num_heads;
@@ -449,9 +478,63 @@ dsa_status sparse_mla_decode(const void* q_bf16, int rows, int num_heads, int d_
     a.workspace = workspace;
     a.ws_bytes = ws_bytes;
     a.status = status_dev;
-    if (sparse_mla_tc_supported(a) && aligned16(q_bf16) && aligned16(out_bf16))
-        return launch_sparse_mla_tc(a, dev, static_cast<cudaStream_t>(stream));
-    return launch_sparse_mla_simt(a, static_cast<cudaStream_t>(stream));
+    return run_sparse_mla(a, stream);
+}
+
+dsa_status sparse_mla_decode_swa(const void* q_bf16, int rows, int num_heads, int d_qk, int d_v, float softmax_scale,
+                                 const dsa_paged_cache* kv, const int32_t* idx, int64_t idx_row_stride, int k,
+                                 const int32_t* topk_lens, const dsa_paged_cache* swa, int window,
+                                 const int32_t* seq_lens, const int32_t* cum_seq_lens_q, int batch, int next_n,
+                                 void* out_bf16, float* lse, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                                 void* stream)
+{
+    if (rows < 0 || num_heads < 1 || k < 0 || !kv || batch < 0 || (!cum_seq_lens_q && next_n < 1))
+        return DSA_ERR_INVALID_ARG;
+    if (d_qk < 16 || d_qk > 1024 || d_qk % 16 != 0 || d_v < 16 || d_v % 16 != 0 || d_v > d_qk || d_v > 512)
+        return DSA_ERR_UNSUPPORTED;
+    dsa_status st = check_mla_cache(kv, d_qk);
+    if (st != DSA_OK)
+        return st;
+    if (swa) {
+        st = check_mla_cache(swa, d_qk);
+        if (st != DSA_OK)
+            return st;
+        if (swa->fmt != kv->fmt)
+            return DSA_ERR_UNSUPPORTED;
+        if (window < 1 || !seq_lens)
+            return DSA_ERR_INVALID_ARG;
+    }
+    if (!cum_seq_lens_q && static_cast<int64_t>(rows) > static_cast<int64_t>(batch) * next_n)
+        return DSA_ERR_INVALID_ARG;
+    if (rows > 0 && (!q_bf16 || (k > 0 && !idx) || !out_bf16 || !lse || (k > 0 && idx_row_stride < k)))
+        return DSA_ERR_INVALID_ARG;
+    if (ws_bytes < dsa_sparse_mla_workspace_bytes(rows, num_heads, d_qk, d_v, k))
+        return DSA_ERR_CAPACITY;
+    MlaArgs a{};
+    a.q = q_bf16;
+    a.rows = rows;
+    a.num_heads = num_heads;
+    a.d_qk = d_qk;
+    a.d_v = d_v;
+    a.softmax_scale = softmax_scale;
+    a.kv = kv;
+    a.seq_of_row = nullptr;
+    a.next_n = next_n;
+    a.idx = idx;
+    a.idx_row_stride = idx_row_stride;
+    a.k = k;
+    a.out = out_bf16;
+    a.lse = lse;
+    a.workspace = workspace;
+    a.ws_bytes = ws_bytes;
+    a.status = status_dev;
+    a.topk_lens = topk_lens;
+    a.swa = swa;
+    a.window = swa ? window : 0;
+    a.seq_lens = seq_lens;
+    a.cum_q = cum_seq_lens_q;
+    a.batch = batch;
+    return run_sparse_mla(a, stream);
 }
 
 dsa_status dsa_kv_quantize_scatter(const void* k_new, int k_dtype, int64_t k_row_stride, int n_tokens,

@@ -115,6 +115,53 @@ __device__ __forceinline__ void unit_rows_of(int u, int next_n, int G, int row_b
     *nrows = min(G, hi - *first_row);
 }
 
+// --------------------------------------------------------- sparse MLA rows
+//
+// Token slots of a sparse MLA row: the kept entries of its index list first,
+// then its sliding-window positions, tagged with this bit (positions < 2^30).
+constexpr int32_t kSwaTag = 0x40000000;
+
+// Sequence, query position and query length of MLA row r: through cumulative
+// query lengths (rows [cum_q[b], cum_q[b+1]) belong to sequence b; -1 if r is
+// in none), an explicit row -> sequence map, or r / next_n.
+struct MlaRowSeq {
+    int seq, i, q_len;
+};
+__device__ __forceinline__ MlaRowSeq mla_row_seq(int r, const int32_t* cum_q, int batch, const int32_t* seq_of_row,
+                                                 int next_n)
+{
+    MlaRowSeq o;
+    if (cum_q) {
+        int lo = 0, hi = batch;                  // last b with cum_q[b] <= r
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cum_q[mid] <= r)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int c0 = cum_q[lo], c1 = lo < batch ? cum_q[lo + 1] : c0;
+        if (lo >= batch || r >= c1) {
+            o.seq = -1;
+            o.i = 0;
+            o.q_len = 0;
+        } else {
+            o.seq = lo;
+            o.i = r - c0;
+            o.q_len = c1 - c0;
+        }
+    } else if (seq_of_row) {
+        o.seq = seq_of_row[r];
+        o.i = 0;
+        o.q_len = 1;
+    } else {
+        o.seq = r / next_n;
+        o.i = r % next_n;
+        o.q_len = next_n;
+    }
+    return o;
+}
+
 // Top-k outputs of a fused indexer score + top-k launch (k = 0: logits only).
 struct FusedTopk {
     int k;

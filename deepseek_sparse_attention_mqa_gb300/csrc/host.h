@@ -105,6 +105,13 @@ struct MlaArgs {
     void* workspace;
     size_t ws_bytes;
     int32_t* status;
+    // sliding window and dynamic lengths (all null / 0: plain sparse MLA)
+    const int32_t* topk_lens;       // [rows]: leading entries of idx to use
+    const dsa_paged_cache* swa;     // window cache
+    int window;
+    const int32_t* seq_lens;        // [batch]
+    const int32_t* cum_q;           // [batch + 1]
+    int batch;
 };
 dsa_status launch_sparse_mla_simt(const MlaArgs& a, cudaStream_t stream);
 bool sparse_mla_tc_supported(const MlaArgs& a);

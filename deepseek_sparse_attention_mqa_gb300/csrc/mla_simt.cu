@@ -32,17 +32,57 @@ __device__ __forceinline__ float e4m3_to_float(uint8_t v)
     return __half2float(__half(h));
 }
 
+// One latent cache as the kernel reads it.
+struct SimtCache {
+    const uint8_t* vals;
+    int64_t vps, vts;
+    const uint8_t* scs;
+    int64_t sps, sts;
+    const int32_t* bt;
+    int64_t bt_stride;
+    int max_pages, page_kv, num_pages;
+};
+
+struct SimtParams {
+    const __nv_bfloat16* q;
+    int num_heads, d_qk, d_v;
+    float softmax_scale;
+    SimtCache kv;                      // the selected (sparse) entries
+    SimtCache swa;                     // the sliding window (vals null: none)
+    int window;
+    const int32_t* seq_lens;
+    const int32_t* cum_q;
+    int batch;
+    const int32_t* seq_of_row;
+    int next_n;
+    const int32_t* idx;
+    int64_t idx_stride;
+    int k;
+    const int32_t* topk_lens;
+    __nv_bfloat16* out;
+    float* lse;
+    int32_t* status;
+};
+
+// Latent row of logical position s of sequence b: its bytes (and fp32 token
+// scale), or null if the block table has no valid page for it.
+__device__ __forceinline__ const uint8_t* simt_row(const SimtCache& c, int b, int s, float* tok_scale)
+{
+    const int lp = s / c.page_kv;
+    const int page = lp < c.max_pages ? c.bt[static_cast<int64_t>(b) * c.bt_stride + lp] : -1;
+    if (page < 0 || page >= c.num_pages)
+        return nullptr;
+    if (c.scs)
+        *tok_scale = *reinterpret_cast<const float*>(c.scs + page * c.sps + (s % c.page_kv) * c.sts);
+    return c.vals + page * c.vps + (s % c.page_kv) * c.vts;
+}
+
 template <int kFmt>
 __global__ void __launch_bounds__(kThreads)
-mla_simt_kernel(const __nv_bfloat16* __restrict__ q, int num_heads, int d_qk, int d_v,
-                float softmax_scale, const uint8_t* __restrict__ vals, int64_t vps, int64_t vts,
-                const uint8_t* __restrict__ scs, int64_t sps, int64_t sts,
-                const int32_t* __restrict__ block_table, int64_t bt_stride, int max_pages,
-                int page_kv, int num_pages, const int32_t* __restrict__ seq_of_row, int next_n,
-                const int32_t* __restrict__ idx, int64_t idx_stride, int k,
-                __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t* __restrict__ status)
+mla_simt_kernel(const SimtParams p)
 {
     extern __shared__ float smf[];
+    const int d_qk = p.d_qk, d_v = p.d_v, num_heads = p.num_heads;
     float* q_s = smf;                                  // [kHeadsPerCta][d_qk]
     float* c_s = q_s + kHeadsPerCta * d_qk;            // [kTokChunk][d_qk]
     __shared__ int valid_s[kTokChunk];
@@ -50,12 +90,30 @@ mla_simt_kernel(const __nv_bfloat16* __restrict__ q, int num_heads, int d_qk, in
     const int r = blockIdx.x;
     const int h0 = blockIdx.y * kHeadsPerCta;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = seq_of_row ? seq_of_row[r] : r / next_n;
+    const MlaRowSeq rs = mla_row_seq(r, p.cum_q, p.batch, p.seq_of_row, p.next_n);
+    const int b = rs.seq;
+    // this row's token slots: the first kr entries of its index list, then the
+    // w window positions [win0, win0 + w)
+    int kr = p.k, w = 0, win0 = 0;
+    if (b < 0) {
+        kr = 0;                                        // a row outside every sequence: no key
+        if (threadIdx.x == 0 && blockIdx.y == 0 && p.status)
+            atomicOr(p.status, DSA_DEV_BAD_INDEX);
+    } else {
+        if (p.topk_lens)
+            kr = min(max(p.topk_lens[r], 0), p.k);
+        if (p.swa.vals) {
+            const int vis = visible_len(max(p.seq_lens[b], 0), rs.q_len, rs.i);
+            w = min(p.window, vis);
+            win0 = vis - w;
+        }
+    }
+    const int nslots = kr + w;
 
     for (int e = threadIdx.x; e < kHeadsPerCta * d_qk; e += kThreads) {
         const int hh = e / d_qk, d = e % d_qk;
         const int h = h0 + hh;
-        q_s[e] = h < num_heads ? __bfloat162float(q[(static_cast<int64_t>(r) * num_heads + h) * d_qk + d]) : 0.f;
+        q_s[e] = h < num_heads ? __bfloat162float(p.q[(static_cast<int64_t>(r) * num_heads + h) * d_qk + d]) : 0.f;
     }
 
     float m[kHeadsPerWarp], l[kHeadsPerWarp], o[kHeadsPerWarp][kMaxVPerLane];
@@ -68,32 +126,30 @@ mla_simt_kernel(const __nv_bfloat16* __restrict__ q, int num_heads, int d_qk, in
             o[a][v] = 0.f;
     }
 
-    const int32_t* irow = idx + static_cast<int64_t>(r) * idx_stride;
-    for (int j0 = 0; j0 < k; j0 += kTokChunk) {
+    const int32_t* irow = p.idx + static_cast<int64_t>(r) * p.idx_stride;
+    for (int j0 = 0; j0 < nslots; j0 += kTokChunk) {
         __syncthreads();
-        // gather + decode: warp w handles tokens w, w+8, ...
+        // gather + decode: warp w handles slots w, w+8, ...
         for (int t = warp; t < kTokChunk; t += kThreads / 32) {
             const int j = j0 + t;
-            int s = j < k ? irow[j] : -1;
-            int page = -1;
-            if (s >= 0) {
-                const int lp = s / page_kv;
-                if (lp < max_pages)
-                    page = block_table[static_cast<int64_t>(b) * bt_stride + lp];
-                if (page < 0 || page >= num_pages) {
-                    if (lane == 0 && status)
-                        atomicOr(status, DSA_DEV_BAD_INDEX);
-                    s = -1;
+            const uint8_t* src = nullptr;
+            float tok_scale = 1.f;
+            if (j < kr) {
+                const int s = irow[j];
+                if (s >= 0) {
+                    src = simt_row(p.kv, b, s, &tok_scale);
+                    if (!src && lane == 0 && p.status)
+                        atomicOr(p.status, DSA_DEV_BAD_INDEX);
                 }
+            } else if (j < nslots) {
+                src = simt_row(p.swa, b, win0 + j - kr, &tok_scale);
+                if (!src && lane == 0 && p.status)
+                    atomicOr(p.status, DSA_DEV_BAD_INDEX);
             }
             if (lane == 0)
-                valid_s[t] = s >= 0;
-            if (s < 0)
+                valid_s[t] = src != nullptr;
+            if (!src)
                 continue;
-            const uint8_t* src = vals + page * vps + (s % page_kv) * vts;
-            float tok_scale = 1.f;
-            if (kFmt == DSA_KV_FP8_E4M3)
-                tok_scale = *reinterpret_cast<const float*>(scs + page * sps + (s % page_kv) * sts);
             for (int d = lane; d < d_qk; d += 32) {
                 float v;
                 if (kFmt == DSA_KV_FP8_E4M3)
@@ -117,7 +173,7 @@ mla_simt_kernel(const __nv_bfloat16* __restrict__ q, int num_heads, int d_qk, in
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1)
                     dot += __shfl_xor_sync(0xffffffffu, dot, off);
-                const float sc = dot * softmax_scale;
+                const float sc = dot * p.softmax_scale;
                 const float mn = fmaxf(m[a], sc);
                 const float alpha = expf(m[a] - mn);
                 const float pj = expf(sc - mn);
@@ -144,14 +200,33 @@ mla_simt_kernel(const __nv_bfloat16* __restrict__ q, int num_heads, int d_qk, in
         for (int v = 0; v < kMaxVPerLane; ++v) {
             const int d = lane + 32 * v;
             if (d < d_v)
-                out[base * d_v + d] = __float2bfloat16(o[a][v] * inv);
+                p.out[base * d_v + d] = __float2bfloat16(o[a][v] * inv);
         }
         if (lane == 0)
-            lse[base] = l[a] > 0.f ? m[a] + logf(l[a]) : -INFINITY;
+            p.lse[base] = l[a] > 0.f ? m[a] + logf(l[a]) : -INFINITY;
     }
 }
 
 }  // namespace
+
+static SimtCache simt_cache(const dsa_paged_cache* c)
+{
+    SimtCache s{};
+    if (!c)
+        return s;
+    s.vals = static_cast<const uint8_t*>(c->values);
+    s.vps = c->val_page_stride;
+    s.vts = c->val_token_stride;
+    s.scs = c->fmt == DSA_KV_FP8_E4M3 ? static_cast<const uint8_t*>(c->scales) : nullptr;
+    s.sps = c->sc_page_stride;
+    s.sts = c->sc_token_stride;
+    s.bt = c->block_table;
+    s.bt_stride = c->bt_row_stride;
+    s.max_pages = c->max_pages_per_seq;
+    s.page_kv = c->page_kv;
+    s.num_pages = c->num_pages;
+    return s;
+}
 
 dsa_status launch_sparse_mla_simt(const MlaArgs& a, cudaStream_t stream)
 {
@@ -160,27 +235,38 @@ dsa_status launch_sparse_mla_simt(const MlaArgs& a, cudaStream_t stream)
     const int smem = (kHeadsPerCta + kTokChunk) * a.d_qk * 4;
     if (a.rows == 0)
         return DSA_OK;
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    SimtParams p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.num_heads = a.num_heads;
+    p.d_qk = a.d_qk;
+    p.d_v = a.d_v;
+    p.softmax_scale = a.softmax_scale;
+    p.kv = simt_cache(kv);
+    p.swa = simt_cache(a.swa);
+    p.window = a.swa ? a.window : 0;
+    p.seq_lens = a.seq_lens;
+    p.cum_q = a.cum_q;
+    p.batch = a.batch;
+    p.seq_of_row = a.seq_of_row;
+    p.next_n = a.next_n;
+    p.idx = a.idx;
+    p.idx_stride = a.idx_row_stride;
+    p.k = a.k;
+    p.topk_lens = a.topk_lens;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    p.status = a.status;
     cudaError_t e;
     if (kv->fmt == DSA_KV_FP8_E4M3) {
         e = cudaFuncSetAttribute(mla_simt_kernel<DSA_KV_FP8_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return cuda_fail(e);
-        mla_simt_kernel<DSA_KV_FP8_E4M3><<<grid, kThreads, smem, stream>>>(
-            q, a.num_heads, a.d_qk, a.d_v, a.softmax_scale, static_cast<const uint8_t*>(kv->values),
-            kv->val_page_stride, kv->val_token_stride, static_cast<const uint8_t*>(kv->scales), kv->sc_page_stride,
-            kv->sc_token_stride, kv->block_table, kv->bt_row_stride, kv->max_pages_per_seq, kv->page_kv,
-            kv->num_pages, a.seq_of_row, a.next_n, a.idx, a.idx_row_stride, a.k, out, a.lse, a.status);
+        mla_simt_kernel<DSA_KV_FP8_E4M3><<<grid, kThreads, smem, stream>>>(p);
     } else {
         e = cudaFuncSetAttribute(mla_simt_kernel<DSA_KV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return cuda_fail(e);
-        mla_simt_kernel<DSA_KV_BF16><<<grid, kThreads, smem, stream>>>(
-            q, a.num_heads, a.d_qk, a.d_v, a.softmax_scale, static_cast<const uint8_t*>(kv->values),
-            kv->val_page_stride, kv->val_token_stride, nullptr, 0, 0, kv->block_table, kv->bt_row_stride,
-            kv->max_pages_per_seq, kv->page_kv, kv->num_pages, a.seq_of_row, a.next_n, a.idx,
-            a.idx_row_stride, a.k, out, a.lse, a.status);
+        mla_simt_kernel<DSA_KV_BF16><<<grid, kThreads, smem, stream>>>(p);
     }
     return check_launch();
 }

@@ -92,6 +92,21 @@ struct MlaParams {
     __nv_bfloat16* out;
     float* lse;
     int32_t* status;
+    // per-row top-k lengths, the sliding-window cache and varlen rows (null: none)
+    const int32_t* topk_lens;
+    const uint8_t* wvals;
+    int64_t wvps, wvts;
+    const uint8_t* wscs;
+    int64_t wsps, wsts;
+    const int32_t* wbt;
+    int64_t wbt_stride;
+    int wmax_pages;
+    int wpage_kv;
+    int wnum_pages;
+    int window;
+    const int32_t* seq_lens;
+    const int32_t* cum_q;
+    int batch;
 };
 
 struct MlaSmem {
@@ -186,7 +201,25 @@ sparse_mla_tc_kernel(const MlaParams p)
     const uint32_t crank = cluster_ctarank();
     const uint32_t peer = crank ^ 1u;
     const int row = blockIdx.y;
-    const int seq = p.seq_of_row ? p.seq_of_row[row] : row / p.next_n;
+    const MlaRowSeq rs = mla_row_seq(row, p.cum_q, p.batch, p.seq_of_row, p.next_n);
+    const int seq = rs.seq;
+    // this row's token slots: the first kr entries of its index list, then the
+    // w window positions [win0, win0 + w) of the window cache
+    int kr = p.k, w = 0, win0 = 0;
+    if (seq < 0) {
+        kr = 0;                                  // a row outside every sequence: no key
+        if (threadIdx.x == 0 && cluster_ctarank() == 0 && p.status)
+            atomicOr(p.status, DSA_DEV_BAD_INDEX);
+    } else {
+        if (p.topk_lens)
+            kr = min(max(p.topk_lens[row], 0), p.k);
+        if (p.wvals) {
+            const int vis = visible_len(max(p.seq_lens[seq], 0), rs.q_len, rs.i);
+            w = min(p.window, vis);
+            win0 = vis - w;
+        }
+    }
+    const int nslots = kr + w;
     // Latent dims of this CTA: its value dims [256 c, 256 c + 256) (tile chunks
     // 0-3, also V for its half of O) and, at d_qk 576, half of the rope dims,
     // [512 + 32 c, 544 + 32 c) (the first half of tile chunk 4), so that both
@@ -199,7 +232,7 @@ sparse_mla_tc_kernel(const MlaParams p)
     auto seg_dim = [&](int sg) -> int {
         return sg < 16 ? static_cast<int>(crank) * 256 + sg * 16 : 512 + static_cast<int>(crank) * 32 + (sg - 16) * 16;
     };
-    const int nblk = (p.k + kNT - 1) / kNT;
+    const int nblk = (nslots + kNT - 1) / kNT;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(q_full), 4);
@@ -317,34 +350,52 @@ sparse_mla_tc_kernel(const MlaParams p)
         // earlier, block j + 3's block-table entry is loaded and block j + 4's
         // index.  Each load thus has a whole iteration to land.
         auto tok_of = [&](int jb) -> int { return jb * kNT + gw * 16 + lane; };
-        auto load_idx = [&](int jb) -> int {       // -1: no token (padding or past k)
-            return (lane < 16 && jb < nblk && tok_of(jb) < p.k) ? irow[tok_of(jb)] : -1;
+        // a slot's token: an index of the sparse cache, a window position tagged
+        // with kSwaTag, or -1 (no token: padding or past the row's slots)
+        auto load_idx = [&](int jb) -> int {
+            if (lane >= 16 || jb >= nblk)
+                return -1;
+            const int t = tok_of(jb);
+            if (t < kr)
+                return irow[t];
+            return t < nslots ? ((win0 + t - kr) | kSwaTag) : -1;
         };
         auto load_page = [&](int sidx) -> int {    // block-table entry of a token (-1 if none)
             if (sidx < 0)
                 return -1;
+            if (sidx & kSwaTag) {
+                const int lp = (sidx & ~kSwaTag) / p.wpage_kv;
+                return lp < p.wmax_pages ? p.wbt[static_cast<int64_t>(seq) * p.wbt_stride + lp] : -1;
+            }
             const int lp = sidx / p.page_kv;
             return lp < p.max_pages ? p.bt[static_cast<int64_t>(seq) * p.bt_stride + lp] : -1;
         };
-        // row address of a token from its index and page: latent byte offset and
-        // scale byte offset, or valid = 0 (a selected token with no valid page is
-        // reported and contributes nothing)
+        // row address of a token from its index and page: the latent row's and
+        // its scale's global addresses, or valid = 0 (a selected token with no
+        // valid page is reported and contributes nothing)
         auto address = [&](int sidx, int pg, int64_t& off, int64_t& soff, int& valid) {
             off = 0;
             soff = 0;
             valid = 0;
             if (sidx < 0)
                 return;
-            if (pg >= 0 && pg < p.num_pages) {
-                off = pg * p.vps + (sidx % p.page_kv) * p.vts;
-                soff = pg * p.sps + (sidx % p.page_kv) * p.sts;
+            const bool swa = (sidx & kSwaTag) != 0;
+            const int pos = sidx & ~kSwaTag;
+            const int P = swa ? p.wpage_kv : p.page_kv;
+            if (pg >= 0 && pg < (swa ? p.wnum_pages : p.num_pages)) {
+                const uint8_t* v = swa ? p.wvals + pg * p.wvps + (pos % P) * p.wvts
+                                       : p.vals + pg * p.vps + (pos % P) * p.vts;
+                const uint8_t* sc = swa ? p.wscs + pg * p.wsps + (pos % P) * p.wsts
+                                        : p.scs + pg * p.sps + (pos % P) * p.sts;
+                off = static_cast<int64_t>(reinterpret_cast<uintptr_t>(v));
+                soff = static_cast<int64_t>(reinterpret_cast<uintptr_t>(sc));
                 valid = 1;
             } else if (p.status) {
                 atomicOr(p.status, DSA_DEV_BAD_INDEX);
             }
         };
         auto load_scale = [&](int64_t soff, int valid) -> float {
-            return valid ? *reinterpret_cast<const float*>(p.scs + soff) : 0.f;
+            return valid ? *reinterpret_cast<const float*>(static_cast<uintptr_t>(soff)) : 0.f;
         };
         auto issue_loads = [&](uint4 (&raw)[kGatherItems], int64_t off, int valid) {
 #pragma unroll
@@ -355,7 +406,8 @@ sparse_mla_tc_kernel(const MlaParams p)
                 const int v = __shfl_sync(0xffffffffu, valid, tl & 15);
                 raw[i] = make_uint4(0, 0, 0, 0);
                 if (flat < 16 * nseg && v)
-                    raw[i] = *reinterpret_cast<const uint4*>(p.vals + o + seg_dim(seg));
+                    raw[i] = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(static_cast<uintptr_t>(o)) +
+                                                             seg_dim(seg));
             }
         };
         // prologue: indices of blocks 0-3, pages of blocks 0-2, addresses of 0-1
@@ -726,7 +778,7 @@ sparse_mla_tc_kernel(const MlaParams p)
 bool sparse_mla_tc_supported(const MlaArgs& a)
 {
     return a.kv->fmt == DSA_KV_FP8_E4M3 && a.num_heads <= 128 && (a.d_qk == 576 || a.d_qk == 512) &&
-           a.d_v == 512 && a.kv->sc_token_stride >= 4;
+           a.d_v == 512 && a.kv->sc_token_stride >= 4 && (!a.swa || a.swa->fmt == DSA_KV_FP8_E4M3);
 }
 
 dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream)
@@ -760,6 +812,23 @@ dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStr
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.lse = a.lse;
     p.status = a.status;
+    p.topk_lens = a.topk_lens;
+    const dsa_paged_cache* w = a.swa;
+    p.wvals = w ? static_cast<const uint8_t*>(w->values) : nullptr;
+    p.wvps = w ? w->val_page_stride : 0;
+    p.wvts = w ? w->val_token_stride : 0;
+    p.wscs = w ? static_cast<const uint8_t*>(w->scales) : nullptr;
+    p.wsps = w ? w->sc_page_stride : 0;
+    p.wsts = w ? w->sc_token_stride : 0;
+    p.wbt = w ? w->block_table : nullptr;
+    p.wbt_stride = w ? w->bt_row_stride : 0;
+    p.wmax_pages = w ? w->max_pages_per_seq : 0;
+    p.wpage_kv = w ? w->page_kv : 1;
+    p.wnum_pages = w ? w->num_pages : 0;
+    p.window = w ? a.window : 0;
+    p.seq_lens = a.seq_lens;
+    p.cum_q = a.cum_q;
+    p.batch = a.batch;
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e);

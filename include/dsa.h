@@ -285,7 +285,8 @@ DSA_API dsa_status indexer_topk(const float* logits, int64_t logits_row_stride, 
  *
  * q_bf16:   bf16 [rows, num_heads, d_qk].
  * kv:       the paged latent cache (FP8 + fp32 token scale, or BF16) with
- *           head_dim == d_qk; the value vector is its first d_v elements.
+ *           head_dim == d_qk and any page_kv >= 1; the value vector is its
+ *           first d_v elements.
  * idx:      int32 [rows, idx_row_stride >= k] (ELEMENTS), logical positions.
  * out_bf16: bf16 [rows, num_heads, d_v]; lse: fp32 [rows, num_heads].
  * workspace: device scratch of dsa_sparse_mla_workspace_bytes(...) bytes.
@@ -346,6 +347,43 @@ DSA_API dsa_status dsa_kv_quantize_scatter(const void* k_new, int k_dtype, int64
  */
 DSA_API dsa_status dsa_wait_selftest(const int32_t* flag, int32_t expect, int limit_us,
                                      int32_t* status_dev, void* stream);
+
+/*
+ * Sparse MLA decode over a sliding window plus selected entries ("Add DeepSeek
+ * V4 sparse MLA TRTLLM-GEN kernels": trtllm_batch_decode_sparse_mla_dsv4 with
+ * sliding_window_kv_cache, dynamic per-row sparse_topk_lens and varlen q
+ * through cum_seq_lens_q).  Row r belongs to sequence b with query position i
+ * and query length q_len: rows [cum_seq_lens_q[b], cum_seq_lens_q[b+1]) are
+ * sequence b's (i = r - cum[b]); without cum_seq_lens_q, b = r / next_n,
+ * i = r % next_n, q_len = next_n.  Its keys, in ONE softmax:
+ *  - the first min(k, topk_lens[r]) entries of idx[r] that are >= 0 (all k
+ *    when topk_lens is NULL): logical entries of sequence b in `kv`;
+ *  - when swa is not NULL, the last w = min(window, vis) positions
+ *    [vis - w, vis) of sequence b in `swa`, where
+ *    vis = clamp(seq_lens[b] - q_len + i + 1, 0, seq_lens[b]) (the row's
+ *    causal view of its sequence, seq_lens counting the new tokens).
+ * Then as sparse_mla_decode(): s_j = softmax_scale * q . c_j[0:d_qk],
+ * lse = ln sum_j exp(s_j), out = sum_j exp(s_j - lse) * c_j[0:d_v]; a row with
+ * no key gets out = 0, lse = -inf (a row outside every sequence also sets
+ * DSA_DEV_BAD_INDEX).
+ *
+ * kv, swa:  latent caches of the same format (FP8 + token scale, or BF16) with
+ *           head_dim == d_qk and any page_kv >= 1 (a compressed cache may hold
+ *           a few entries per physical block), each with its own block table.
+ * topk_lens: nullable device int32 [rows].   seq_lens: device int32 [batch]
+ *           (required with swa).   cum_seq_lens_q: nullable device int32
+ *           [batch + 1], non-decreasing, cum[0] = 0, cum[batch] = rows.
+ * Other arguments as sparse_mla_decode().
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA.
+ */
+DSA_API dsa_status sparse_mla_decode_swa(const void* q_bf16, int rows, int num_heads, int d_qk, int d_v,
+                                         float softmax_scale, const dsa_paged_cache* kv,
+                                         const int32_t* idx, int64_t idx_row_stride, int k,
+                                         const int32_t* topk_lens, const dsa_paged_cache* swa,
+                                         int window, const int32_t* seq_lens,
+                                         const int32_t* cum_seq_lens_q, int batch, int next_n,
+                                         void* out_bf16, float* lse, void* workspace,
+                                         size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /*
  * Opt-in, SYNCHRONISING read of a device status word: waits for `stream`,
