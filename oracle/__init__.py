@@ -12,7 +12,9 @@ and the passages they follow:
 * ``decode_e4m3 / decode_e2m1 / decode_ue8m0 / decode_bf16`` -- the OCP FP8,
   FP4 and UE8M0 definitions and bfloat16 (upper half of binary32).
 * ``visible`` -- draft-row windows ("feat(deepseek_v4): Add fp4 indexer for
-  dsv4", varlen windows per draft row; reading: L - next_n + i + 1, clamped).
+  dsv4", varlen windows per draft row; reading: L - next_n + i + 1, clamped),
+  over a compressed cache floor(window / ratio) entries (the CSA index length
+  context_len // 4 of the same page).
 * ``logits_fp8 / logits_mxfp4`` -- the lightning-indexer score
   k_scale[s] * sum_h w[r,h] * relu(q[r,h].k[s]) over a paged cache
   ("SM120 FP8 paged MQA page 32", Summary; "Add fp4 indexer for dsv4", FP4
@@ -89,16 +91,16 @@ def _load():
         lib.dsa_oracle_logits_fp8.restype = _int
         lib.dsa_oracle_logits_fp8.argtypes = [
             _c_u8p, _c_f32p, _int, _int, _c_u8p, _i64, _i64, _c_u8p, _i64, _i64,
-            _c_i32p, _i64, _int, _int, _int, _c_i32p, _int, _int, _int, _int,
+            _c_i32p, _i64, _int, _int, _int, _c_i32p, _int, _int, _int, _int, _int,
             _c_f64p, _i64, _int]
         lib.dsa_oracle_logits_mxfp4.restype = _int
         lib.dsa_oracle_logits_mxfp4.argtypes = [
             _c_u8p, _c_u8p, _c_f32p, _int, _int, _c_u8p, _i64, _i64, _c_u8p, _i64, _i64,
-            _c_i32p, _i64, _int, _int, _int, _c_i32p, _int, _int, _int, _int,
+            _c_i32p, _i64, _int, _int, _int, _c_i32p, _int, _int, _int, _int, _int,
             _c_f64p, _i64, _int]
         lib.dsa_oracle_topk.restype = _int
         lib.dsa_oracle_topk.argtypes = [
-            _c_f64p, _i64, _c_i32p, _int, _int, _int, _int, _int, _c_i32p, _i64, _c_i32p]
+            _c_f64p, _i64, _c_i32p, _int, _int, _int, _int, _int, _int, _c_i32p, _i64, _c_i32p]
         lib.dsa_oracle_sparse_mla.restype = _int
         lib.dsa_oracle_sparse_mla.argtypes = [
             _c_u16p, _int, _int, _int, _int, ctypes.c_double, _int, _c_u8p, _i64, _i64,
@@ -159,8 +161,9 @@ def decode_bf16(bits: int) -> float:
     return _load().dsa_oracle_bf16(bits)
 
 
-def visible(L: int, next_n: int, i: int) -> int:
-    return _load().dsa_oracle_visible(L, next_n, i)
+def visible(L: int, next_n: int, i: int, ratio: int = 1) -> int:
+    """Entries row i sees: floor(clamp(L - next_n + i + 1, 0, L) / ratio)."""
+    return _load().dsa_oracle_visible(L, next_n, i) // int(ratio)
 
 
 class PagedBytes:
@@ -188,7 +191,7 @@ def _check(rc, what):
 
 
 def logits_fp8(q, w, cache: PagedBytes, context_lens, next_n, row_begin=None, row_end=None,
-               width=None):
+               width=None, ratio=1):
     """fp64 logits [row_end-row_begin, width]; entries past each row's visible
     length are NaN (not defined by the method)."""
     lib = _load()
@@ -200,7 +203,7 @@ def logits_fp8(q, w, cache: PagedBytes, context_lens, next_n, row_begin=None, ro
     rb = 0 if row_begin is None else int(row_begin)
     re = batch * next_n if row_end is None else int(row_end)
     if width is None:
-        width = int(max([0] + [lib.dsa_oracle_visible(int(L), next_n, next_n - 1) for L in ctx]))
+        width = int(max([0] + [lib.dsa_oracle_visible(int(L), next_n, next_n - 1) // int(ratio) for L in ctx]))
     out = np.full((max(re - rb, 0), max(width, 1)), np.nan, dtype=np.float64)
     bt = cache.block_table
     rc = lib.dsa_oracle_logits_fp8(
@@ -208,14 +211,14 @@ def logits_fp8(q, w, cache: PagedBytes, context_lens, next_n, row_begin=None, ro
         _ptr(cache.values, ctypes.c_uint8), cache.vps, cache.vts,
         _ptr(cache.scales, ctypes.c_uint8), cache.sps, cache.sts,
         _ptr(bt, ctypes.c_int32), bt.shape[1], bt.shape[1], cache.page_kv, cache.num_pages,
-        _ptr(ctx, ctypes.c_int32), batch, int(next_n), rb, re,
+        _ptr(ctx, ctypes.c_int32), batch, int(next_n), int(ratio), rb, re,
         _ptr(out, ctypes.c_double), out.shape[1], int(width))
     _check(rc, "logits_fp8")
     return out[:, :width]
 
 
 def logits_mxfp4(q, q_scales, w, cache: PagedBytes, context_lens, next_n, row_begin=None,
-                 row_end=None, width=None):
+                 row_end=None, width=None, ratio=1):
     """fp64 logits for an MXFP4 cache and MXFP4 q (packed e2m1 + ue8m0 per 32)."""
     lib = _load()
     q = _np(q, np.uint8)
@@ -228,7 +231,7 @@ def logits_mxfp4(q, q_scales, w, cache: PagedBytes, context_lens, next_n, row_be
     rb = 0 if row_begin is None else int(row_begin)
     re = batch * next_n if row_end is None else int(row_end)
     if width is None:
-        width = int(max([0] + [lib.dsa_oracle_visible(int(L), next_n, next_n - 1) for L in ctx]))
+        width = int(max([0] + [lib.dsa_oracle_visible(int(L), next_n, next_n - 1) // int(ratio) for L in ctx]))
     out = np.full((max(re - rb, 0), max(width, 1)), np.nan, dtype=np.float64)
     bt = cache.block_table
     rc = lib.dsa_oracle_logits_mxfp4(
@@ -236,13 +239,13 @@ def logits_mxfp4(q, q_scales, w, cache: PagedBytes, context_lens, next_n, row_be
         _ptr(cache.values, ctypes.c_uint8), cache.vps, cache.vts,
         _ptr(cache.scales, ctypes.c_uint8), cache.sps, cache.sts,
         _ptr(bt, ctypes.c_int32), bt.shape[1], bt.shape[1], cache.page_kv, cache.num_pages,
-        _ptr(ctx, ctypes.c_int32), batch, int(next_n), rb, re,
+        _ptr(ctx, ctypes.c_int32), batch, int(next_n), int(ratio), rb, re,
         _ptr(out, ctypes.c_double), out.shape[1], int(width))
     _check(rc, "logits_mxfp4")
     return out[:, :width]
 
 
-def topk(logits, context_lens, next_n, k, row_begin=None, row_end=None):
+def topk(logits, context_lens, next_n, k, row_begin=None, row_end=None, ratio=1):
     """(idx [rows, k] int32 in sorted order with -1 padding, count [rows] int32)."""
     lib = _load()
     lg = np.ascontiguousarray(_np(logits, np.float64))
@@ -256,7 +259,7 @@ def topk(logits, context_lens, next_n, k, row_begin=None, row_end=None):
     idx = np.empty((rows, k), dtype=np.int32)
     cnt = np.empty((rows,), dtype=np.int32)
     rc = lib.dsa_oracle_topk(_ptr(lg, ctypes.c_double), lg.shape[1], _ptr(ctx, ctypes.c_int32),
-                             batch, int(next_n), rb, re, int(k), _ptr(idx, ctypes.c_int32), k,
+                             batch, int(next_n), int(ratio), rb, re, int(k), _ptr(idx, ctypes.c_int32), k,
                              _ptr(cnt, ctypes.c_int32))
     _check(rc, "topk")
     return idx, cnt

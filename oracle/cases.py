@@ -46,6 +46,7 @@ def oracle_cache(paged, block_table, seqs=None):
 
 
 def visible(case, r):
-    """Visible length of absolute row r of a workload (the oracle's window rule)."""
+    """Visible entries of absolute row r of a workload (the oracle's window rule,
+    over the workload's compression ratio)."""
     b, i = divmod(r, case.next_n)
-    return _visible(int(case.context_lens[b]), case.next_n, i)
+    return _visible(int(case.context_lens[b]), case.next_n, i, getattr(case, "ratio", 1))

@@ -28,6 +28,10 @@
  *  - visible length of draft row i of a sequence with context length L and
  *    next_n rows: clamp(L - next_n + i + 1, 0, L) (context length includes the
  *    next_n new tokens, bound inclusive);
+ *  - over a compressed K cache whose entry e summarises `ratio` consecutive
+ *    tokens ("feat(deepseek_v4): Add fp4 indexer for dsv4": the CSA index
+ *    length is context_len // 4), the row sees floor(visible length / ratio)
+ *    entries (ratio 1: one entry per token);
  *  - entries at s >= visible length are not written;
  *  - e2m1 packing: the low nibble of a byte is the even element;
  *  - MXFP4 caches carry no per-token scale (k_scale = 1);
@@ -146,13 +150,13 @@ int dsa_oracle_logits_fp8(const uint8_t* q, const float* w, int H, int D,
                           const uint8_t* kscales, int64_t sps, int64_t sts,
                           const int32_t* block_table, int64_t bt_stride, int max_pages,
                           int page_kv, int num_pages, const int32_t* context_lens, int batch,
-                          int next_n, int row_begin, int row_end, double* out,
+                          int next_n, int ratio, int row_begin, int row_end, double* out,
                           int64_t out_stride, int out_width)
 {
     double lut[256];
     int c, err = ORACLE_OK;
     long r;
-    if (H <= 0 || D <= 0 || page_kv <= 0 || next_n <= 0 || row_begin < 0 ||
+    if (H <= 0 || D <= 0 || page_kv <= 0 || next_n <= 0 || ratio <= 0 || row_begin < 0 ||
         row_end > batch * next_n || row_begin > row_end)
         return ORACLE_ERR_ARG;
     for (c = 0; c < 256; ++c)
@@ -161,7 +165,7 @@ int dsa_oracle_logits_fp8(const uint8_t* q, const float* w, int H, int D,
 #pragma omp parallel for schedule(dynamic, 1)
     for (r = row_begin; r < row_end; ++r) {
         int b = (int)(r / next_n), i = (int)(r % next_n);
-        int vis = dsa_oracle_visible(context_lens[b], next_n, i);
+        int vis = dsa_oracle_visible(context_lens[b], next_n, i) / ratio;
         int s;
         if (vis > out_width) {
 #pragma omp atomic write
@@ -210,19 +214,19 @@ int dsa_oracle_logits_mxfp4(const uint8_t* q, const uint8_t* q_sc, const float* 
                             const uint8_t* kscales, int64_t sps, int64_t sts,
                             const int32_t* block_table, int64_t bt_stride, int max_pages,
                             int page_kv, int num_pages, const int32_t* context_lens, int batch,
-                            int next_n, int row_begin, int row_end, double* out,
+                            int next_n, int ratio, int row_begin, int row_end, double* out,
                             int64_t out_stride, int out_width)
 {
     int err = ORACLE_OK;
     long r;
-    if (H <= 0 || D <= 0 || D % 32 != 0 || page_kv <= 0 || next_n <= 0 || row_begin < 0 ||
+    if (H <= 0 || D <= 0 || D % 32 != 0 || page_kv <= 0 || next_n <= 0 || ratio <= 0 || row_begin < 0 ||
         row_end > batch * next_n || row_begin > row_end)
         return ORACLE_ERR_ARG;
 
 #pragma omp parallel for schedule(dynamic, 1)
     for (r = row_begin; r < row_end; ++r) {
         int b = (int)(r / next_n), i = (int)(r % next_n);
-        int vis = dsa_oracle_visible(context_lens[b], next_n, i);
+        int vis = dsa_oracle_visible(context_lens[b], next_n, i) / ratio;
         int s;
         if (vis > out_width) {
 #pragma omp atomic write
@@ -281,17 +285,17 @@ static int by_logit_desc(const void* a, const void* b)
  * NULL it receives min(k, vis) per row.  logits rows are chunk-relative
  * (row r at (r - row_begin) * stride). */
 int dsa_oracle_topk(const double* logits, int64_t stride, const int32_t* context_lens, int batch,
-                    int next_n, int row_begin, int row_end, int k, int32_t* idx,
+                    int next_n, int ratio, int row_begin, int row_end, int k, int32_t* idx,
                     int64_t idx_stride, int32_t* count)
 {
     long r;
     int err = ORACLE_OK;
-    if (k <= 0 || next_n <= 0 || row_begin < 0 || row_end > batch * next_n || row_begin > row_end)
+    if (k <= 0 || next_n <= 0 || ratio <= 0 || row_begin < 0 || row_end > batch * next_n || row_begin > row_end)
         return ORACLE_ERR_ARG;
 #pragma omp parallel for schedule(dynamic, 1)
     for (r = row_begin; r < row_end; ++r) {
         int b = (int)(r / next_n), i = (int)(r % next_n);
-        int vis = dsa_oracle_visible(context_lens[b], next_n, i);
+        int vis = dsa_oracle_visible(context_lens[b], next_n, i) / ratio;
         int s, take = vis < k ? vis : k;
         int32_t* out = idx + (r - row_begin) * idx_stride;
         scored* buf = (scored*)malloc(sizeof(scored) * (size_t)(vis > 0 ? vis : 1));
