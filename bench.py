@@ -217,7 +217,8 @@ def time_indexer_steps(st, steps, flush, stream):
         for ci, (rb, re) in enumerate(chunks):
             inline = st.inline[(rb, re)]          # no schedule launch: the logits kernel builds the units
             if not inline:
-                _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status)
+                _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, st.sched, st.status,
+                                    compress_ratio=st.ratio)
             e[3 * ci + 1].record(stream)
             if st.fused:
                 _abi.score_topk(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, st.kcache, c.context_lens,

@@ -48,6 +48,7 @@ class PagedCache(ctypes.Structure):
         ("scales", ctypes.c_void_p), ("sc_page_stride", ctypes.c_int64),
         ("sc_token_stride", ctypes.c_int64), ("block_table", ctypes.c_void_p),
         ("bt_row_stride", ctypes.c_int64), ("max_pages_per_seq", ctypes.c_int32),
+        ("compress_ratio", ctypes.c_int32),
     ]
 
 
@@ -78,7 +79,7 @@ def lib():
         L.dsa_indexer_schedule_bytes.restype = _sz
         L.dsa_indexer_schedule_bytes.argtypes = [_i, _i, _i, _i, _i]
         L.dsa_indexer_build_schedule.restype = _i
-        L.dsa_indexer_build_schedule.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp]
+        L.dsa_indexer_build_schedule.argtypes = [_vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp]
         L.indexer_mqa_logits_paged.restype = _i
         L.indexer_mqa_logits_paged.argtypes = [
             _vp, _vp, _i, _vp, _i, ctypes.POINTER(PagedCache), _vp, _i, _i, _i, _i, _vp, _sz,
@@ -90,7 +91,7 @@ def lib():
         L.dsa_topk_workspace_bytes.restype = _sz
         L.dsa_topk_workspace_bytes.argtypes = [_i, _i, _i]
         L.indexer_topk.restype = _i
-        L.indexer_topk.argtypes = [_vp, _i64, _i, _vp, _i, _i, _i, _i, _i, _vp, _i64, _vp, _vp,
+        L.indexer_topk.argtypes = [_vp, _i64, _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _i64, _vp, _vp,
                                    _sz, _vp, _vp]
         L.dsa_sparse_mla_workspace_bytes.restype = _sz
         L.dsa_sparse_mla_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
@@ -135,8 +136,9 @@ def _stream(stream):
 
 
 def make_cache(fmt, head_dim, page_kv, num_pages, values, val_page_stride, val_token_stride,
-               scales, sc_page_stride, sc_token_stride, block_table) -> PagedCache:
-    """dsa_paged_cache over device tensors (block_table [batch, max_pages] int32)."""
+               scales, sc_page_stride, sc_token_stride, block_table, compress_ratio=1) -> PagedCache:
+    """dsa_paged_cache over device tensors (block_table [batch, max_pages] int32);
+    compress_ratio = tokens per entry of a compressed indexer cache."""
     c = PagedCache()
     c.fmt, c.head_dim, c.page_kv, c.num_pages = int(fmt), int(head_dim), int(page_kv), int(num_pages)
     c.values = values.data_ptr()
@@ -146,6 +148,7 @@ def make_cache(fmt, head_dim, page_kv, num_pages, values, val_page_stride, val_t
     c.block_table = block_table.data_ptr()
     c.bt_row_stride = int(block_table.stride(0))
     c.max_pages_per_seq = int(block_table.shape[1])
+    c.compress_ratio = int(compress_ratio)
     c._keep = (values, scales, block_table)
     return c
 
@@ -155,9 +158,9 @@ def schedule_bytes(batch, next_n, num_heads, row_begin, row_end) -> int:
 
 
 def build_schedule(context_lens, batch, next_n, num_heads, row_begin, row_end, sched,
-                   status=None, stream=None):
+                   status=None, stream=None, compress_ratio=1):
     _check(lib().dsa_indexer_build_schedule(
-        _ptr(context_lens), batch, next_n, num_heads, row_begin, row_end, _ptr(sched),
+        _ptr(context_lens), batch, next_n, num_heads, int(compress_ratio), row_begin, row_end, _ptr(sched),
         sched.numel() * sched.element_size(), _ptr(status), _stream(stream)),
         "dsa_indexer_build_schedule")
 
@@ -222,11 +225,11 @@ def topk_workspace_bytes(rows, width, k) -> int:
 
 
 def topk(logits, logits_width, context_lens, batch, next_n, row_begin, row_end, k, idx,
-         count=None, workspace=None, status=None, stream=None):
+         count=None, workspace=None, status=None, stream=None, compress_ratio=1):
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().indexer_topk(
         _ptr(logits), logits.stride(0), int(logits_width), _ptr(context_lens), batch, next_n,
-        row_begin, row_end, k, _ptr(idx), idx.stride(0), _ptr(count), _ptr(workspace), ws_bytes,
+        int(compress_ratio), row_begin, row_end, k, _ptr(idx), idx.stride(0), _ptr(count), _ptr(workspace), ws_bytes,
         _ptr(status), _stream(stream)), "indexer_topk")
 
 

@@ -59,6 +59,17 @@ EncodeTiledFn encode_fn()
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kMaxRatio = 65536;
+
+// Tokens per entry of an indexer K cache: its compress_ratio, 0 and 1 both
+// meaning one entry per token; -1 if out of range.
+int ratio_of(int32_t r)
+{
+    if (r < 0 || r > kMaxRatio)
+        return -1;
+    return r <= 1 ? 1 : r;
+}
+
 }  // namespace
 
 dsa_status current_device(DeviceInfo* out)
@@ -173,6 +184,8 @@ dsa_status validate_logits_call(const void* q, const void* q_scales, int q_fmt, 
     dsa_status st = check_cache(k, true);
     if (st != DSA_OK)
         return st;
+    if (ratio_of(k->compress_ratio) < 0)
+        return DSA_ERR_INVALID_ARG;
     if (q_fmt == DSA_KV_FP8_E4M3) {
         if (k->val_token_stride != D || k->sc_token_stride != 4 || k->val_page_stride < int64_t(k->page_kv) * D ||
             k->sc_page_stride < int64_t(k->page_kv) * 4)
@@ -215,7 +228,7 @@ const char* dsa_status_string(dsa_status s)
 
 int dsa_last_cuda_error(void) { return g_last_cuda_error; }
 
-int dsa_version(void) { return 102; }
+int dsa_version(void) { return 200; }
 
 size_t dsa_indexer_schedule_bytes(int batch, int next_n, int num_heads, int row_begin, int row_end)
 {
@@ -226,10 +239,13 @@ size_t dsa_indexer_schedule_bytes(int batch, int next_n, int num_heads, int row_
 }
 
 dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int batch, int next_n, int num_heads,
-                                      int row_begin, int row_end, void* sched, size_t sched_bytes,
-                                      int32_t* status_dev, void* stream)
+                                      int compress_ratio, int row_begin, int row_end, void* sched,
+                                      size_t sched_bytes, int32_t* status_dev, void* stream)
 {
     if (!row_range_ok(batch, next_n, row_begin, row_end) || num_heads < 1 || num_heads > kMaxUnitCols)
+        return DSA_ERR_INVALID_ARG;
+    const int ratio = ratio_of(compress_ratio);
+    if (ratio < 0)
         return DSA_ERR_INVALID_ARG;
     if (!sched || !aligned16(sched) || (batch > 0 && !context_lens))
         return DSA_ERR_INVALID_ARG;
@@ -243,7 +259,7 @@ dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int batch, in
     dsa_status st = current_device(&dev);
     if (st != DSA_OK)
         return st;
-    return launch_build_schedule(context_lens, batch, next_n, G, row_begin, row_end, static_cast<int>(units),
+    return launch_build_schedule(context_lens, batch, next_n, ratio, G, row_begin, row_end, static_cast<int>(units),
                                  static_cast<int32_t*>(sched), status_dev, static_cast<cudaStream_t>(stream));
 }
 
@@ -272,6 +288,7 @@ static dsa_status launch_logits_call(const void* q, const void* q_scales, int q_
     a.row_end = row_end;
     a.rows_per_unit = unit_rows(next_n, num_heads);
     a.num_units = static_cast<int>(units);
+    a.ratio = ratio_of(k->compress_ratio);
     a.sched = static_cast<const int32_t*>(sched);
     a.logits = logits;
     a.logits_row_stride = logits_row_stride;
@@ -359,13 +376,16 @@ size_t dsa_topk_workspace_bytes(int rows, int logits_width, int k)
 }
 
 dsa_status indexer_topk(const float* logits, int64_t logits_row_stride, int logits_width,
-                        const int32_t* context_lens, int batch, int next_n, int row_begin, int row_end, int k,
-                        int32_t* idx, int64_t idx_row_stride, int32_t* count, void* workspace, size_t ws_bytes,
-                        int32_t* status_dev, void* stream)
+                        const int32_t* context_lens, int batch, int next_n, int compress_ratio, int row_begin,
+                        int row_end, int k, int32_t* idx, int64_t idx_row_stride, int32_t* count, void* workspace,
+                        size_t ws_bytes, int32_t* status_dev, void* stream)
 {
     (void)workspace;
     (void)ws_bytes;
     if (!row_range_ok(batch, next_n, row_begin, row_end))
+        return DSA_ERR_INVALID_ARG;
+    const int ratio = ratio_of(compress_ratio);
+    if (ratio < 0)
         return DSA_ERR_INVALID_ARG;
     if (k < 1 || k > 16384)
         return DSA_ERR_UNSUPPORTED;
@@ -387,6 +407,7 @@ dsa_status indexer_topk(const float* logits, int64_t logits_row_stride, int logi
     a.next_n = next_n;
     a.row_begin = row_begin;
     a.row_end = row_end;
+    a.ratio = ratio;
     a.k = k;
     a.idx = idx;
     a.idx_row_stride = idx_row_stride;

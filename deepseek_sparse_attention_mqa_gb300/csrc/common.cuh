@@ -26,6 +26,14 @@ __host__ __device__ __forceinline__ int visible_len(int L, int next_n, int i)
     return static_cast<int>(v > L ? L : v);
 }
 
+// Entries row i sees in a compressed K cache of `ratio` tokens per entry:
+// floor(visible_len / ratio) ("feat(deepseek_v4): Add fp4 indexer for dsv4",
+// the CSA index length context_len // 4); ratio 1 is one entry per token.
+__host__ __device__ __forceinline__ int visible_entries(int L, int next_n, int i, int ratio)
+{
+    return visible_len(L, next_n, i) / ratio;
+}
+
 // Rows per work unit for a head count: as many draft rows of one sequence as
 // fit in one MMA N dimension.
 __host__ __device__ __forceinline__ int unit_rows(int next_n, int num_heads)
@@ -39,11 +47,11 @@ __host__ __device__ __forceinline__ int unit_rows(int next_n, int num_heads)
 //
 // Layout of the caller-owned schedule buffer (int32 words):
 //   header[0..7]: magic, num_units, rows_per_unit, row_begin, row_end, next_n,
-//                 total_tiles, batch
+//                 total_tiles, compression ratio
 //   units[num_units] (32-byte records): first_row (absolute), nrows, seq,
 //                 tile_begin (prefix of 128-token tiles over the units),
-//                 tile_end, vis_max (largest visible length of the unit's
-//                 rows), ctx_len (the sequence's context length, >= 0), 0.
+//                 tile_end, vis_max (largest visible entry count of the
+//                 unit's rows), ctx_len (the sequence's context length, >= 0), 0.
 //                 A record is everything a kernel needs about its unit, read
 //                 with one 32-byte load and no dependent lookups.
 constexpr int32_t kSchedMagic = 0x44534132;  // "DSA2"

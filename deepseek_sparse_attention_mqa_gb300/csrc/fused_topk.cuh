@@ -53,6 +53,7 @@ struct FusedPhaseArgs {
     int64_t logits_stride;
     int logits_width;
     int next_n;
+    int ratio;
     int row_begin;
     const int32_t* context_lens;
     int32_t* status;
@@ -65,7 +66,7 @@ __device__ __forceinline__ void fused_select_row(const FusedPhaseArgs& a, const 
                                                  int row, SelectSmem& sh, uint8_t* dyn, uint32_t dyn_bytes)
 {
     const int i = row - ui.seq * a.next_n;
-    const int vis = min(visible_len(ui.ctx_len, a.next_n, i), a.logits_width);
+    const int vis = min(visible_entries(ui.ctx_len, a.next_n, i, a.ratio), a.logits_width);
     const int64_t rloc = row - a.row_begin;
     int32_t* out = f.idx + rloc * f.idx_stride;
     if (f.count && threadIdx.x == 0)

@@ -40,7 +40,7 @@ dsa_status validate_logits_call(const void* q, const void* q_scales, int q_fmt, 
                                 int64_t logits_row_stride, int logits_width, int64_t* units);
 
 // Launchers implemented in the kernel translation units.
-dsa_status launch_build_schedule(const int32_t* context_lens, int batch, int next_n,
+dsa_status launch_build_schedule(const int32_t* context_lens, int batch, int next_n, int ratio,
                                  int rows_per_unit, int row_begin, int row_end, int num_units,
                                  int32_t* sched, int32_t* status, cudaStream_t stream);
 
@@ -57,6 +57,7 @@ struct LogitsArgs {
     int row_end;
     int rows_per_unit;
     int num_units;
+    int ratio;                  // tokens per K-cache entry
     const int32_t* sched;
     float* logits;
     int64_t logits_row_stride;
@@ -76,6 +77,7 @@ struct TopkArgs {
     int next_n;
     int row_begin;
     int row_end;
+    int ratio;                  // tokens per K-cache entry
     int k;
     int32_t* idx;
     int64_t idx_row_stride;

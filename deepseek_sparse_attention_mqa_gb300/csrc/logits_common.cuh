@@ -181,8 +181,8 @@ constexpr uint32_t kInlineScratchBytes = 160;   // 33 ints of scan scratch, 16-b
 // Writes records [0, num_units) to `su` exactly as the schedule kernel does and
 // returns the total number of 128-token tiles.
 __device__ __forceinline__ int build_inline_units(SchedUnit* su, int* scratch, const int32_t* context_lens,
-                                                  int batch, int next_n, int G, int row_begin, int row_end,
-                                                  int num_units, int32_t* status)
+                                                  int batch, int next_n, int ratio, int G, int row_begin,
+                                                  int row_end, int num_units, int32_t* status)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = static_cast<int>(blockDim.x + 31) >> 5;
@@ -192,7 +192,7 @@ __device__ __forceinline__ int build_inline_units(SchedUnit* su, int* scratch, c
         if (seq < batch && nrows > 0) {
             const int L = context_lens[seq];
             ctx = L < 0 ? 0 : L;
-            vis = visible_len(ctx, next_n, first_row + nrows - 1 - seq * next_n);
+            vis = visible_entries(ctx, next_n, first_row + nrows - 1 - seq * next_n, ratio);
             tiles = (vis + kTileTokens - 1) / kTileTokens;
         } else if (status) {
             atomicOr(status, DSA_DEV_SCHEDULE);

@@ -72,6 +72,7 @@ struct Mx4Params {
     int num_pages;
     int page_kv;
     int next_n;
+    int ratio;                 // tokens per K-cache entry
     int row_begin;
     int row_end;
     int num_units;
@@ -215,7 +216,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
         const int32_t* hdr = p.sched;
         units = reinterpret_cast<const SchedUnit*>(p.sched + kSchedHeaderWords);
         if (hdr[0] != kSchedMagic || hdr[1] != p.num_units || hdr[2] != p.rows_per_unit ||
-            hdr[3] != p.row_begin || hdr[4] != p.row_end || hdr[5] != p.next_n) {
+            hdr[3] != p.row_begin || hdr[4] != p.row_end || hdr[5] != p.next_n || hdr[7] != p.ratio) {
             if (threadIdx.x == 0 && p.status)
                 atomicOr(p.status, DSA_DEV_SCHEDULE);
             return;
@@ -224,7 +225,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
     } else {
         SchedUnit* su = reinterpret_cast<SchedUnit*>(smem + mp.units);
         int* scratch = reinterpret_cast<int*>(smem + mp.units + p.inline_units * 32);
-        total_tiles = build_inline_units(su, scratch, p.context_lens, p.batch, p.next_n, p.rows_per_unit,
+        total_tiles = build_inline_units(su, scratch, p.context_lens, p.batch, p.next_n, p.ratio, p.rows_per_unit,
                                          p.row_begin, p.row_end, p.num_units,
                                          blockIdx.x == 0 ? p.status : nullptr);
         units = su;
@@ -247,6 +248,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
         fa.logits_stride = p.logits_stride;
         fa.logits_width = p.logits_width;
         fa.next_n = p.next_n;
+        fa.ratio = p.ratio;
         fa.row_begin = p.row_begin;
         fa.context_lens = p.context_lens;
         fa.status = p.status;
@@ -608,7 +610,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
                 L = ui.ctx_len;
                 i0 = ui.first_row - ui.seq * p.next_n;
                 if (e == 0 && lane == 0 && p.status &&
-                    visible_len(L, p.next_n, i0 + ui.nrows - 1) > p.logits_width)
+                    visible_entries(L, p.next_n, i0 + ui.nrows - 1, p.ratio) > p.logits_width)
                     atomicOr(p.status, DSA_DEV_WIDTH);
             }
             if (j % p.n_grp == group) {
@@ -676,7 +678,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
                                     part[q & 3] = fmaf(wS[cb + q], fmaxf(dot[q], 0.f), part[q & 3]);
                             rowsum += (part[0] + part[1]) + (part[2] + part[3]);
                         }
-                        const int vis = min(visible_len(L, p.next_n, i0 + i), p.logits_width);
+                        const int vis = min(visible_entries(L, p.next_n, i0 + i, p.ratio), p.logits_width);
                         if (s < vis)
                             p.logits[static_cast<int64_t>(ui.first_row + i - p.row_begin) * p.logits_stride + s] = rowsum;
                     }
@@ -788,6 +790,7 @@ dsa_status launch_mx4_dh(const LogitsArgs& a, const DeviceInfo& dev, cudaStream_
     p.num_pages = k->num_pages;
     p.page_kv = P;
     p.next_n = a.next_n;
+    p.ratio = a.ratio;
     p.row_begin = a.row_begin;
     p.row_end = a.row_end;
     p.num_units = a.num_units;

@@ -129,8 +129,8 @@ extern "C" DSA_API dsa_status indexer_mqa_logits_paged_noalloc(
         return st;
     // every word the logits kernel reads is rewritten by the schedule build first,
     // so nothing has to be cleared between calls
-    st = dsa_indexer_build_schedule(context_lens, batch, next_n, num_heads, row_begin, row_end, sched,
-                                    kNoallocSchedBytes, status_dev, stream);
+    st = dsa_indexer_build_schedule(context_lens, batch, next_n, num_heads, k->compress_ratio, row_begin, row_end,
+                                    sched, kNoallocSchedBytes, status_dev, stream);
     if (st != DSA_OK)
         return st;
     return indexer_mqa_logits_paged(q, q_scales, q_fmt, weights, num_heads, k, context_lens, batch, next_n,

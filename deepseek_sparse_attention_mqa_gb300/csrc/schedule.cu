@@ -22,7 +22,7 @@ namespace {
 constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads)
-build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int next_n, int G,
+build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int next_n, int ratio, int G,
                       int row_begin, int row_end, int num_units, int32_t* __restrict__ sched,
                       int32_t* __restrict__ status)
 {
@@ -43,7 +43,7 @@ build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int n
                 const int L = context_lens[seq];
                 ctx = L < 0 ? 0 : L;
                 const int last_i = first_row + nrows - 1 - seq * next_n;
-                vis = visible_len(ctx, next_n, last_i);
+                vis = visible_entries(ctx, next_n, last_i, ratio);
                 tiles = (vis + kTileTokens - 1) / kTileTokens;
             } else if (status) {
                 atomicOr(status, DSA_DEV_SCHEDULE);
@@ -98,17 +98,17 @@ build_schedule_kernel(const int32_t* __restrict__ context_lens, int batch, int n
         sched[4] = row_end;
         sched[5] = next_n;
         sched[6] = carry_s;
-        sched[7] = batch;
+        sched[7] = ratio;
     }
 }
 
 }  // namespace
 
-dsa_status launch_build_schedule(const int32_t* context_lens, int batch, int next_n,
+dsa_status launch_build_schedule(const int32_t* context_lens, int batch, int next_n, int ratio,
                                  int rows_per_unit, int row_begin, int row_end, int num_units,
                                  int32_t* sched, int32_t* status, cudaStream_t stream)
 {
-    build_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(context_lens, batch, next_n,
+    build_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(context_lens, batch, next_n, ratio,
                                                            rows_per_unit, row_begin, row_end,
                                                            num_units, sched, status);
     return check_launch();

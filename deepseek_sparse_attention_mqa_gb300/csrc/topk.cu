@@ -90,7 +90,7 @@ struct TopkShared {
 template <bool kCached>
 __global__ void __launch_bounds__(kThreads, 2)
 topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
-            const int32_t* __restrict__ context_lens, int next_n, int row_begin, int k,
+            const int32_t* __restrict__ context_lens, int next_n, int ratio, int row_begin, int k,
             int32_t* __restrict__ idx, int64_t idx_stride, int32_t* __restrict__ count,
             int32_t* __restrict__ status)
 {
@@ -103,7 +103,7 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     const int rloc = blockIdx.y;
     const int r = row_begin + rloc;
     const int b = r / next_n, i = r % next_n;
-    int vis = visible_len(max(0, context_lens[b]), next_n, i);
+    int vis = visible_entries(max(0, context_lens[b]), next_n, i, ratio);
     if (vis > width) {
         if (tid == 0 && crank == 0 && status)
             atomicOr(status, DSA_DEV_WIDTH);
@@ -466,11 +466,11 @@ dsa_status launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t st
         if (e != cudaSuccess)
             return cuda_fail(e);
         e = cudaLaunchKernelEx(&cfg, topk_kernel<true>, a.logits, a.logits_row_stride, a.logits_width,
-                               a.context_lens, a.next_n, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
+                               a.context_lens, a.next_n, a.ratio, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
                                a.status);
     } else {
         e = cudaLaunchKernelEx(&cfg, topk_kernel<false>, a.logits, a.logits_row_stride, a.logits_width,
-                               a.context_lens, a.next_n, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
+                               a.context_lens, a.next_n, a.ratio, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
                                a.status);
     }
     if (e != cudaSuccess)

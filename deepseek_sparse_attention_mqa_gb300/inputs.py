@@ -70,7 +70,7 @@ class Case:
     page_kv: int
     fmt: int
     topk: int
-    width: int                      # logits row capacity (max visible length)
+    width: int                      # logits row capacity (max visible entries)
     context_lens: torch.Tensor      # [batch] int32
     block_table: torch.Tensor       # [batch, max_pages] int32, -1 where unused
     kcache: Paged
@@ -85,6 +85,7 @@ class Case:
     latent: Optional[Paged] = None
     q_mla: Optional[torch.Tensor] = None   # [R, Hq, d_qk] bf16
     meta: dict = field(default_factory=dict)
+    ratio: int = 1                  # tokens per K-cache entry (compressed indexer cache)
 
     @property
     def rows(self) -> int:
@@ -214,9 +215,12 @@ def make_case(name: str, seed: Optional[int] = None, device="cpu", batch: Option
         L = _lens(cfg["lens"], B, gc)
         B = L.numel()
     R = B * n
-    width = int(cfg.get("width", 0)) or int(L.max().item())
-    width = max(width, int(L.max().item()) if B else 0)
-    pages_per_seq = [(int(l) + P - 1) // P for l in L.tolist()]
+    # a compressed K cache (ratio > 1) holds one entry per `ratio` tokens
+    ratio = int(cfg.get("ratio", 1))
+    entries = [int(l) // ratio for l in L.tolist()]
+    width = int(cfg.get("width", 0)) or (max(entries) if B else 0)
+    width = max(width, max(entries) if B else 0)
+    pages_per_seq = [(e + P - 1) // P for e in entries]
     used = sum(pages_per_seq)
     pool = max(1, used * int(cfg.get("pool_factor", 1)))
     max_pages = max(1, (width + P - 1) // P)
@@ -270,7 +274,7 @@ def make_case(name: str, seed: Optional[int] = None, device="cpu", batch: Option
                 topk=int(cfg["topk"]), width=width, context_lens=L.to(dev),
                 block_table=bt.to(dev), kcache=kc, q=q.contiguous(),
                 q_scales=None if q_scales is None else q_scales.contiguous(),
-                weights=w.contiguous(), meta=dict(seed=int(seed), pool=pool, used_pages=used))
+                weights=w.contiguous(), meta=dict(seed=int(seed), pool=pool, used_pages=used), ratio=ratio)
 
     mla = cfg.get("mla")
     if with_mla and mla:

@@ -80,9 +80,11 @@ class SparseAttentionStep:
         self.chunks = [(rb, min(self.rows, rb + self.rows_per_chunk))
                        for rb in range(0, self.rows, self.rows_per_chunk)] or [(0, 0)]
         kc = c.kcache
+        self.ratio = int(getattr(c, "ratio", 1))
         self.kcache = _abi.make_cache(kc.fmt, kc.head_dim, kc.page_kv, kc.num_pages, kc.values,
                                       kc.val_page_stride, kc.val_token_stride, kc.scales,
-                                      kc.sc_page_stride, kc.sc_token_stride, c.block_table)
+                                      kc.sc_page_stride, kc.sc_token_stride, c.block_table,
+                                      compress_ratio=self.ratio)
         # a chunk of at most INLINE_UNITS units needs no schedule launch: the logits
         # kernel builds its units itself (inline_schedule=False forces the buffer)
         self.inline = {(rb, re): (inline_schedule is not False and
@@ -122,7 +124,7 @@ class SparseAttentionStep:
         inline = self.inline.get((rb, re), False)
         if not inline:
             _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, self.sched,
-                                self.status, stream)
+                                self.status, stream, compress_ratio=self.ratio)
         _abi.mqa_logits(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, self.kcache,
                         c.context_lens, c.batch, c.next_n, rb, re, None if inline else self.sched,
                         self.logits, self.width, self.status, stream)
@@ -134,7 +136,7 @@ class SparseAttentionStep:
         inline = self.inline.get((rb, re), False)
         if not inline:
             _abi.build_schedule(c.context_lens, c.batch, c.next_n, c.num_heads, rb, re, self.sched,
-                                self.status, stream)
+                                self.status, stream, compress_ratio=self.ratio)
         _abi.score_topk(c.q, c.q_scales, c.fmt, c.weights, c.num_heads, self.kcache, c.context_lens,
                         c.batch, c.next_n, rb, re, None if inline else self.sched, self.logits,
                         self.width, c.topk, self.idx[rb:re], self.count[rb:re], self.fused_ws,
@@ -143,7 +145,8 @@ class SparseAttentionStep:
     def topk_chunk(self, rb: int, re: int, stream=None):
         c = self.case
         _abi.topk(self.logits, self.width, c.context_lens, c.batch, c.next_n, rb, re, c.topk,
-                  self.idx[rb:re], self.count[rb:re], self.topk_ws, self.status, stream)
+                  self.idx[rb:re], self.count[rb:re], self.topk_ws, self.status, stream,
+                  compress_ratio=self.ratio)
 
     def mla(self, stream=None):
         c = self.case

@@ -84,6 +84,15 @@ typedef enum {
  * and the page strides 16-byte aligned; val_token_stride == the dense row size
  * (head_dim bytes for FP8, head_dim/2 for MXFP4, 2*head_dim for BF16);
  * sc_token_stride == 4 (FP8) or head_dim/32 (MXFP4).
+ *
+ * Compressed indexer caches ("feat(deepseek_v4): Add fp4 indexer for dsv4":
+ * the CSA index length is context_len // 4; "SM120 FP8 paged MQA page 32":
+ * a 64-token storage block holds 32 states of a ratio-2 layer): with
+ * compress_ratio = c > 1, entry e of a sequence summarises tokens
+ * [c*e, c*e + c), the block table addresses ENTRIES (page_kv entries per
+ * page), and a row that sees vis tokens sees floor(vis / c) entries; logits
+ * and top-k positions are entry indices.  Layers of different ratios can share
+ * one block table and physical pool, each with its own page_kv.  1 <= c <= 65536.
  */
 typedef struct {
     int32_t fmt;               /* dsa_format */
@@ -99,6 +108,8 @@ typedef struct {
     const int32_t* block_table; /* device, [batch, bt_row_stride] int32 */
     int64_t bt_row_stride;     /* ELEMENTS between sequences' rows */
     int32_t max_pages_per_seq; /* valid columns of each block-table row */
+    int32_t compress_ratio;    /* indexer caches: tokens per entry (0 or 1: one
+                                  entry per token); see below */
 } dsa_paged_cache;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -109,7 +120,10 @@ DSA_API int dsa_last_cuda_error(void);
 
 /* Library ABI version (major*100 + minor).  1.01: indexer_mqa_logits_paged
  * accepts sched = NULL for calls of at most 256 work units.  1.02: fused
- * indexer_score_topk, dsa_kv_quantize_scatter, dsa_wait_selftest. */
+ * indexer_score_topk, dsa_kv_quantize_scatter, dsa_wait_selftest.  2.00:
+ * compressed indexer caches (dsa_paged_cache.compress_ratio; a compress_ratio
+ * argument of dsa_indexer_build_schedule and indexer_topk),
+ * sparse_mla_decode_swa, MLA caches of any page size. */
 DSA_API int dsa_version(void);
 
 /*
@@ -128,6 +142,7 @@ DSA_API int dsa_version(void);
  * inside a captured graph at every replay.
  *
  * context_lens: device int32 [batch], lengths INCLUDING the next_n new tokens.
+ * compress_ratio: the K cache's compress_ratio (0 or 1: one entry per token).
  * sched: device buffer of at least dsa_indexer_schedule_bytes(...) bytes,
  *        16-byte aligned, caller-owned; its contents are opaque.
  * Errors: DSA_ERR_INVALID_ARG (sizes, row range, null pointers),
@@ -136,8 +151,9 @@ DSA_API int dsa_version(void);
 DSA_API size_t dsa_indexer_schedule_bytes(int batch, int next_n, int num_heads, int row_begin,
                                   int row_end);
 DSA_API dsa_status dsa_indexer_build_schedule(const int32_t* context_lens, int batch, int next_n,
-                                      int num_heads, int row_begin, int row_end, void* sched,
-                                      size_t sched_bytes, int32_t* status_dev, void* stream);
+                                      int num_heads, int compress_ratio, int row_begin,
+                                      int row_end, void* sched, size_t sched_bytes,
+                                      int32_t* status_dev, void* stream);
 
 /*
  * Paged lightning-indexer MQA logits (DeepSeek sparse attention):
@@ -253,8 +269,9 @@ DSA_API dsa_status indexer_mqa_logits_paged_noalloc(const void* q, const void* q
  * dsv4": indexer_score_topk; "Add DeepSeek V4 sparse MLA TRTLLM-GEN kernels":
  * dynamic per-row top-k lengths).  For each row, the k largest of
  * logits[row][0 : vis(row)) (vis as above, clipped to logits_width) are
- * selected; idx[row][0 : min(k, vis)) receives their token positions (in no
- * particular order) and idx[row][min(k, vis) : k) receives -1.  Among exactly
+ * selected (vis in entries: floor(vis / compress_ratio), compress_ratio 0 or 1
+ * meaning one entry per token); idx[row][0 : min(k, vis)) receives their
+ * positions (in no particular order) and idx[row][min(k, vis) : k) receives -1.  Among exactly
  * equal logits (-0 equals +0) the lower position wins.  count (nullable)
  * receives min(k, vis).
  *
@@ -267,8 +284,8 @@ DSA_API dsa_status indexer_mqa_logits_paged_noalloc(const void* q, const void* q
  */
 DSA_API size_t dsa_topk_workspace_bytes(int rows, int logits_width, int k);
 DSA_API dsa_status indexer_topk(const float* logits, int64_t logits_row_stride, int logits_width,
-                        const int32_t* context_lens, int batch, int next_n, int row_begin,
-                        int row_end, int k, int32_t* idx, int64_t idx_row_stride,
+                        const int32_t* context_lens, int batch, int next_n, int compress_ratio,
+                        int row_begin, int row_end, int k, int32_t* idx, int64_t idx_row_stride,
                         int32_t* count, void* workspace, size_t ws_bytes, int32_t* status_dev,
                         void* stream);
 

@@ -39,11 +39,12 @@ def test_status_strings_and_version(L):
 
 
 def test_paged_cache_struct_layout():
-    # int32 x4, ptr, i64, i64, ptr, i64, i64, ptr, i64, int32 (+pad) = 88 bytes on LP64
+    # int32 x4, ptr, i64, i64, ptr, i64, i64, ptr, i64, int32, int32 = 88 bytes on LP64
     assert ctypes.sizeof(_abi.PagedCache) == 88
     assert _abi.PagedCache.values.offset == 16
     assert _abi.PagedCache.block_table.offset == 64
     assert _abi.PagedCache.max_pages_per_seq.offset == 80
+    assert _abi.PagedCache.compress_ratio.offset == 84
 
 
 def test_schedule_bytes_counts_units(L):
@@ -66,9 +67,11 @@ def test_host_validation_rejects_before_any_gpu_call(L):
     vp = ctypes.c_void_p
     fake = vp(0x1000)   # never dereferenced: validation fails first
     # null schedule buffer
-    assert L.dsa_indexer_build_schedule(fake, 2, 1, 64, 0, 2, None, 4096, None, None) == 1
+    assert L.dsa_indexer_build_schedule(fake, 2, 1, 64, 1, 0, 2, None, 4096, None, None) == 1
     # capacity
-    assert L.dsa_indexer_build_schedule(fake, 2, 1, 64, 0, 2, fake, 8, None, None) == 3
+    assert L.dsa_indexer_build_schedule(fake, 2, 1, 64, 1, 0, 2, fake, 8, None, None) == 3
+    # compression ratio out of range
+    assert L.dsa_indexer_build_schedule(fake, 2, 1, 64, -2, 0, 2, fake, 4096, None, None) == 1
     # unsupported head count
     c = _abi.PagedCache()
     c.fmt, c.head_dim, c.page_kv, c.num_pages = 0, 128, 64, 4
@@ -94,8 +97,8 @@ def test_host_validation_rejects_before_any_gpu_call(L):
     a[2] = 1
     assert L.indexer_mqa_logits_paged(*a) == 2
     # top-k: k out of range, stride too small
-    assert L.indexer_topk(fake, 256, 256, fake, 2, 1, 0, 2, 0, fake, 64, None, None, 0, None, None) == 2
-    assert L.indexer_topk(fake, 256, 256, fake, 2, 1, 0, 2, 128, fake, 64, None, None, 0, None, None) == 1
+    assert L.indexer_topk(fake, 256, 256, fake, 2, 1, 1, 0, 2, 0, fake, 64, None, None, 0, None, None) == 2
+    assert L.indexer_topk(fake, 256, 256, fake, 2, 1, 1, 0, 2, 128, fake, 64, None, None, 0, None, None) == 1
     # MLA: d_v > d_qk, bad format
     m = _abi.PagedCache()
     m.fmt, m.head_dim, m.page_kv, m.num_pages = 0, 576, 64, 4
