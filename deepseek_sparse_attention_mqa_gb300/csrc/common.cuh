@@ -31,7 +31,8 @@ __host__ __device__ __forceinline__ int visible_len(int L, int next_n, int i)
 // the CSA index length context_len // 4); ratio 1 is one entry per token.
 __host__ __device__ __forceinline__ int visible_entries(int L, int next_n, int i, int ratio)
 {
-    return visible_len(L, next_n, i) / ratio;
+    const int v = visible_len(L, next_n, i);
+    return ratio == 1 ? v : v / ratio;          // no integer division for uncompressed caches
 }
 
 // Rows per work unit for a head count: as many draft rows of one sequence as

@@ -545,20 +545,25 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 auto process = [&](const uint32_t (&r)[32], int c) {
                     const float4* w4 = reinterpret_cast<const float4*>(wS + c * 32);
                     if constexpr (H >= 32) {
-                        // one row per chunk: 8 independent partial sums
-                        float part[8];
+                        // one row per chunk: 8 independent partial sums in 4 packed
+                        // pairs, one packed FMA per two heads (the relu stays two maxes)
+                        uint64_t part[4];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            part[q] = 0.f;
+                        for (int q = 0; q < 4; ++q)
+                            part[q] = 0ull;
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4) {
                             const float4 wv = w4[q4];
-                            part[(4 * q4 + 0) & 7] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f), part[(4 * q4 + 0) & 7]);
-                            part[(4 * q4 + 1) & 7] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f), part[(4 * q4 + 1) & 7]);
-                            part[(4 * q4 + 2) & 7] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f), part[(4 * q4 + 2) & 7]);
-                            part[(4 * q4 + 3) & 7] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f), part[(4 * q4 + 3) & 7]);
+                            const uint64_t a01 = pack_f32x2(fmaxf(__uint_as_float(r[4 * q4 + 0]), 0.f),
+                                                            fmaxf(__uint_as_float(r[4 * q4 + 1]), 0.f));
+                            const uint64_t a23 = pack_f32x2(fmaxf(__uint_as_float(r[4 * q4 + 2]), 0.f),
+                                                            fmaxf(__uint_as_float(r[4 * q4 + 3]), 0.f));
+                            part[(2 * q4) & 3] = fma_f32x2(pack_f32x2(wv.x, wv.y), a01, part[(2 * q4) & 3]);
+                            part[(2 * q4 + 1) & 3] = fma_f32x2(pack_f32x2(wv.z, wv.w), a23, part[(2 * q4 + 1) & 3]);
                         }
-                        cur += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                        const float2 p0 = unpack_f32x2(part[0]), p1 = unpack_f32x2(part[1]);
+                        const float2 p2 = unpack_f32x2(part[2]), p3 = unpack_f32x2(part[3]);
+                        cur += ((p0.x + p0.y) + (p1.x + p1.y)) + ((p2.x + p2.y) + (p3.x + p3.y));
                         if (((c + 1) * 32) % H == 0) {
                             emit((c * 32) / H, cur);
                             cur = 0.f;

@@ -167,6 +167,10 @@ __device__ __forceinline__ float exp2_int(int e)
     return __int_as_float((127 + e) << 23);
 }
 
+// kDual: per-row top-k lengths, the sliding-window cache and cumulative query
+// lengths; without it the kernel reads the index lists alone (the gather keeps
+// fewer values live).
+template <bool kDual>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 sparse_mla_tc_kernel(const MlaParams p)
 {
@@ -201,12 +205,14 @@ sparse_mla_tc_kernel(const MlaParams p)
     const uint32_t crank = cluster_ctarank();
     const uint32_t peer = crank ^ 1u;
     const int row = blockIdx.y;
-    const MlaRowSeq rs = mla_row_seq(row, p.cum_q, p.batch, p.seq_of_row, p.next_n);
+    const MlaRowSeq rs = kDual ? mla_row_seq(row, p.cum_q, p.batch, p.seq_of_row, p.next_n)
+                               : MlaRowSeq{p.seq_of_row ? p.seq_of_row[row] : row / p.next_n, 0, 1};
     const int seq = rs.seq;
     // this row's token slots: the first kr entries of its index list, then the
     // w window positions [win0, win0 + w) of the window cache
     int kr = p.k, w = 0, win0 = 0;
-    if (seq < 0) {
+    if (!kDual) {
+    } else if (seq < 0) {
         kr = 0;                                  // a row outside every sequence: no key
         if (threadIdx.x == 0 && cluster_ctarank() == 0 && p.status)
             atomicOr(p.status, DSA_DEV_BAD_INDEX);
@@ -356,6 +362,8 @@ sparse_mla_tc_kernel(const MlaParams p)
             if (lane >= 16 || jb >= nblk)
                 return -1;
             const int t = tok_of(jb);
+            if (!kDual)
+                return t < p.k ? irow[t] : -1;
             if (t < kr)
                 return irow[t];
             return t < nslots ? ((win0 + t - kr) | kSwaTag) : -1;
@@ -363,7 +371,7 @@ sparse_mla_tc_kernel(const MlaParams p)
         auto load_page = [&](int sidx) -> int {    // block-table entry of a token (-1 if none)
             if (sidx < 0)
                 return -1;
-            if (sidx & kSwaTag) {
+            if (kDual && (sidx & kSwaTag)) {
                 const int lp = (sidx & ~kSwaTag) / p.wpage_kv;
                 return lp < p.wmax_pages ? p.wbt[static_cast<int64_t>(seq) * p.wbt_stride + lp] : -1;
             }
@@ -379,8 +387,8 @@ sparse_mla_tc_kernel(const MlaParams p)
             valid = 0;
             if (sidx < 0)
                 return;
-            const bool swa = (sidx & kSwaTag) != 0;
-            const int pos = sidx & ~kSwaTag;
+            const bool swa = kDual && (sidx & kSwaTag) != 0;
+            const int pos = kDual ? (sidx & ~kSwaTag) : sidx;
             const int P = swa ? p.wpage_kv : p.page_kv;
             if (pg >= 0 && pg < (swa ? p.wnum_pages : p.num_pages)) {
                 const uint8_t* v = swa ? p.wvals + pg * p.wvps + (pos % P) * p.wvts
@@ -829,10 +837,12 @@ dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStr
     p.seq_lens = a.seq_lens;
     p.cum_q = a.cum_q;
     p.batch = a.batch;
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    const bool dual = a.topk_lens || a.swa || a.cum_q;
+    auto kern = dual ? sparse_mla_tc_kernel<true> : sparse_mla_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    sparse_mla_tc_kernel<<<dim3(2, a.rows), kThreads, smem_bytes, stream>>>(p);
+    kern<<<dim3(2, a.rows), kThreads, smem_bytes, stream>>>(p);
     return check_launch();
 }
 

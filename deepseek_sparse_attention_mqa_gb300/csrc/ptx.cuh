@@ -269,6 +269,31 @@ __device__ __forceinline__ void tmem_st_wait()
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------- packed fp32 pairs
+
+// Two fp32 values in one 64-bit register pair (x in the low half).
+__device__ __forceinline__ uint64_t pack_f32x2(float x, float y)
+{
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(x), "f"(y));
+    return v;
+}
+
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+// a * b + c on both halves, each rounded like fmaf (one packed FMA issue).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor of tcgen05.mma (sm_100 family):
