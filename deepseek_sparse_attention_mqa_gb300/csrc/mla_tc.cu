@@ -110,7 +110,7 @@ struct MlaParams {
 };
 
 struct MlaSmem {
-    uint32_t q, lat, p, x, scale, valid, qexp, red, bar, misc, total;
+    uint32_t q, lat, p, x, xs, scale, valid, qexp, red, bar, misc, total;
 };
 
 __host__ __device__ constexpr MlaSmem mla_smem()
@@ -120,12 +120,13 @@ __host__ __device__ constexpr MlaSmem mla_smem()
     m.lat = m.q + kQChunkBytes;                      // the rope chunk of Q (value dims are in TMEM)
     m.p = m.lat + kLatBufs * kMaxChunks * kLChunkBytes;
     m.x = m.p + 128 * 128;
-    m.scale = m.x + 128 * kNT * 4;
+    m.xs = m.x + 128 * kNT * 4;                      // this CTA's partial scores, staged for the peer
+    m.scale = m.xs + 128 * kNT * 4;
     m.valid = m.scale + kLatBufs * kNT * 4;
     m.qexp = m.valid + kLatBufs * kNT * 4;
     m.red = m.qexp + 128 * 4;
     m.bar = m.red + 2 * 2 * 128 * 4;
-    m.misc = m.bar + 24 * 8;
+    m.misc = m.bar + 40 * 8;
     m.total = m.misc + 16;
     return m;
 }
@@ -181,6 +182,7 @@ sparse_mla_tc_kernel(const MlaParams p)
     uint8_t* sLat = smem + mp.lat;
     uint8_t* sP = smem + mp.p;
     uint8_t* sX = smem + mp.x;
+    uint8_t* sXs = smem + mp.xs;
     float* sScale = reinterpret_cast<float*>(smem + mp.scale);
     int* sValid = reinterpret_cast<int*>(smem + mp.valid);
     int* sQexp = reinterpret_cast<int*>(smem + mp.qexp);       // per-head power-of-two Q scale
@@ -192,8 +194,8 @@ sparse_mla_tc_kernel(const MlaParams p)
     uint64_t* lat_empty = bars + 4;  // [kLatBufs]
     uint64_t* s_full = bars + 7;     // [2]
     uint64_t* s_empty = bars + 9;    // [2]
-    uint64_t* x_full = bars + 11;    // peer's partial scores arrived in sX
-    uint64_t* x_free = bars + 12;    // peer consumed what this CTA wrote
+    uint64_t* xw_full = bars + 24;   // [8] per softmax warp: the peer's partial scores arrived in sX
+    uint64_t* xw_free = bars + 32;   // [8] per softmax warp: the peer consumed what this warp sent
     uint64_t* p_full = bars + 13;
     uint64_t* p_empty = bars + 14;
     uint64_t* o_done = bars + 15;
@@ -250,8 +252,10 @@ sparse_mla_tc_kernel(const MlaParams p)
             mbar_init(smem_u32(&s_full[i]), 1);
             mbar_init(smem_u32(&s_empty[i]), 8);
         }
-        mbar_init(smem_u32(x_full), 1);            // local expect_tx + the peer's st.async bytes
-        mbar_init(smem_u32(x_free), 8);            // the peer's 8 softmax warps
+        for (int i = 0; i < 8; ++i) {
+            mbar_init(smem_u32(&xw_full[i]), 1);    // local expect_tx + the peer warp's bulk copy bytes
+            mbar_init(smem_u32(&xw_free[i]), 1);    // the peer warp's remote arrive
+        }
         mbar_init(smem_u32(p_full), 8);
         mbar_init(smem_u32(p_empty), 1);
         mbar_init(smem_u32(o_done), 1);
@@ -580,11 +584,18 @@ sparse_mla_tc_kernel(const MlaParams p)
             ++pair_uses;
             return r;
         };
-        // the peer's X row of this head: this thread's 32 partial scores go to units
-        // [half*8, half*8 + 8) of it (16-byte units XOR-swizzled by head)
-        const uint32_t peer_x_row = mapa_shared(smem_u32(sX + h * (kNT * 4)), peer);
-        const uint32_t peer_x_full = mapa_shared(smem_u32(x_full), peer);
-        const uint32_t peer_x_free = mapa_shared(smem_u32(x_free), peer);
+        // Score exchange, per softmax warp: this warp's 32 threads stage their 32
+        // partial scores (128 B each, 16-byte units XOR-swizzled by lane) in its
+        // 4 KB slice of sXs, and one lane copies the slice with a single bulk
+        // shared-memory copy into the same slice of the peer's sX, where the
+        // peer's warp of the same (quarter, half) -- the same heads and tokens --
+        // reads it; the copy completes on that warp's own mbarrier.
+        const int widx = half * 4 + quarter;
+        uint8_t* stage_row = sXs + widx * 4096 + lane * 128;
+        const uint8_t* recv_row = sX + widx * 4096 + lane * 128;
+        const uint32_t peer_slice = mapa_shared(smem_u32(sX + widx * 4096), peer);
+        const uint32_t peer_full = mapa_shared(smem_u32(&xw_full[widx]), peer);
+        const uint32_t peer_free = mapa_shared(smem_u32(&xw_free[widx]), peer);
         float m_run = -INFINITY, l_run = 0.f;
         // this head's Q was stored times 2^e; partial scores are scaled back (exact)
         bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(q_full), 0));
@@ -610,26 +621,31 @@ sparse_mla_tc_kernel(const MlaParams p)
             for (int i = 0; i < 32; ++i)
                 ra[i] = __float_as_uint(__uint_as_float(ra[i]) * qback);
 
-            // ---- exchange partial scores with the peer CTA: asynchronous remote
-            // stores whose bytes complete the peer's x_full transaction count
-            if (warp == 0 && lane == 0)
-                mbar_arrive_expect_tx(smem_u32(x_full), static_cast<uint32_t>(128 * kNT * 4));
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(x_free), (j & 1) ^ 1))) {
+            // ---- exchange partial scores with the peer CTA (one bulk copy per warp)
+            if (lane == 0)
+                mbar_arrive_expect_tx(smem_u32(&xw_full[widx]), 4096u);
+            // the peer has consumed this warp's previous copy (so it has landed and
+            // this warp's staging slice was read)
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&xw_free[widx]), (j & 1) ^ 1))) {
                 ok = false;
                 break;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                st_async_v4(peer_x_row + (((half * 8 + u) ^ (h & 7)) << 4), ra[4 * u], ra[4 * u + 1], ra[4 * u + 2],
-                            ra[4 * u + 3], peer_x_full);
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(x_full), j & 1))) {
+                *reinterpret_cast<uint4*>(stage_row + ((u ^ (lane & 7)) << 4)) =
+                    make_uint4(ra[4 * u], ra[4 * u + 1], ra[4 * u + 2], ra[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                bulk_copy_to_cluster(peer_slice, smem_u32(sXs + widx * 4096), 4096u, peer_full);
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&xw_full[widx]), j & 1))) {
                 ok = false;
                 break;
             }
             float sco[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const float4 x = *reinterpret_cast<const float4*>(sX + h * (kNT * 4) + (((half * 8 + u) ^ (h & 7)) << 4));
+                const float4 x = *reinterpret_cast<const float4*>(recv_row + ((u ^ (lane & 7)) << 4));
                 // both CTAs form partial(CTA 0) + partial(CTA 1) in the same order
                 const float o0 = __uint_as_float(ra[4 * u]), o1 = __uint_as_float(ra[4 * u + 1]);
                 const float o2 = __uint_as_float(ra[4 * u + 2]), o3 = __uint_as_float(ra[4 * u + 3]);
@@ -650,7 +666,7 @@ sparse_mla_tc_kernel(const MlaParams p)
             // thread's st.async to the peer to complete.
             __syncwarp();
             if (lane == 0)
-                mbar_arrive_remote_relaxed(peer_x_free);
+                mbar_arrive_remote_relaxed(peer_free);
 
             // ---- scores in base 2; masked slots are -inf
             const int lb = j % kLatBufs;

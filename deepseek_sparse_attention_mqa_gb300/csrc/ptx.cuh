@@ -371,7 +371,19 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
                  : "memory");
 }
 
-// Named barrier among `count` threads (a multiple of 32) of this CTA; id 0 is
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA's shared memory in the cluster by the copy engine; the bytes
+// complete the transaction count of an mbarrier in the DESTINATION CTA.
+// dst and mbar are cluster addresses (mapa), src a local shared address; both
+// addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
+// Named barrier among `count` threads// Named barrier among `count` threads (a multiple of 32) of this CTA; id 0 is
 // __syncthreads'.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {
