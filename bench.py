@@ -534,7 +534,9 @@ def measure_full_step(dev, args, flush, workload="full_step", fused=True):
             "stage_us_median": {k: round(statistics.median(v), 2) for k, v in stage.items()},
             "mla_roofline": {"bound": "tensor", "achieved": round(mla_flops / (mla_us * 1e-6) / 1e12, 1),
                              "peak": bf16, "unit": "TFLOP/s", "frac": round(mla_flops / (mla_us * 1e-6) / 1e12 / bf16, 4),
-                             "peak_source": src + " bf16 burst (f16 operands run at the bf16 rate)"},
+                             "peak_source": src + " bf16 burst (f16 operands run at the bf16 rate)",
+                             "algorithmic_flops": mla_flops,
+                             "traffic": load_traffic("sparse_mla_tc", "full_step") if workload == "full_step" else None},
             "launches_per_step": st.launches_per_step(), "device_status": status}
 
 
