@@ -165,6 +165,9 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     volatile int* s_u0 = reinterpret_cast<volatile int*>(smem + mp.misc_off + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the next kernel (the top-k, launched as a programmatic dependent) may
+    // start its prologue on SMs this grid frees; it waits for the logits
+    pdl_launch_dependents();
 
     // ---- the schedule: a prebuilt buffer (its header checked, uniformly over the
     // CTA, before any allocation) or the units built here in shared memory

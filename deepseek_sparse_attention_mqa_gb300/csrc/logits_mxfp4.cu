@@ -208,6 +208,9 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
     volatile int* s_u0 = reinterpret_cast<volatile int*>(smem + mp.misc + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the next kernel (the top-k, launched as a programmatic dependent) may
+    // start its prologue on SMs this grid frees; it waits for the logits
+    pdl_launch_dependents();
     // the schedule: a prebuilt buffer (header checked uniformly over the CTA) or
     // the units built here in shared memory
     const SchedUnit* units;

@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "host.h"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(kThreads)
 mla_simt_kernel(const SimtParams p)
 {
     extern __shared__ float smf[];
+    pdl_wait();                                        // nothing the previous kernel writes is read before
     const int d_qk = p.d_qk, d_v = p.d_v, num_heads = p.num_heads;
     float* q_s = smf;                                  // [kHeadsPerCta][d_qk]
     float* c_s = q_s + kHeadsPerCta * d_qk;            // [kTokChunk][d_qk]
@@ -209,6 +211,23 @@ mla_simt_kernel(const SimtParams p)
 
 }  // namespace
 
+// Launch as a programmatic dependent of the previous kernel of the stream.
+template <class K>
+static cudaError_t launch_pdl(K kern, dim3 grid, int smem, cudaStream_t stream, const SimtParams& p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 static SimtCache simt_cache(const dsa_paged_cache* c)
 {
     SimtCache s{};
@@ -261,13 +280,15 @@ dsa_status launch_sparse_mla_simt(const MlaArgs& a, cudaStream_t stream)
         e = cudaFuncSetAttribute(mla_simt_kernel<DSA_KV_FP8_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return cuda_fail(e);
-        mla_simt_kernel<DSA_KV_FP8_E4M3><<<grid, kThreads, smem, stream>>>(p);
+        e = launch_pdl(mla_simt_kernel<DSA_KV_FP8_E4M3>, grid, smem, stream, p);
     } else {
         e = cudaFuncSetAttribute(mla_simt_kernel<DSA_KV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return cuda_fail(e);
-        mla_simt_kernel<DSA_KV_BF16><<<grid, kThreads, smem, stream>>>(p);
+        e = launch_pdl(mla_simt_kernel<DSA_KV_BF16>, grid, smem, stream, p);
     }
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     return check_launch();
 }
 

@@ -203,6 +203,10 @@ sparse_mla_tc_kernel(const MlaParams p)
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc + 4);
 
+    // launched as a programmatic dependent of the previous kernel of the stream
+    // (the top-k): nothing is read before this wait, so only the launch latency
+    // overlaps its end
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t crank = cluster_ctarank();
     const uint32_t peer = crank ^ 1u;
@@ -858,7 +862,21 @@ dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStr
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    kern<<<dim3(2, a.rows), kThreads, smem_bytes, stream>>>(p);
+    // programmatic dependent launch: Q preparation, TMEM and barrier set-up
+    // overlap the end of the previous kernel; the gather waits for it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, a.rows, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     return check_launch();
 }
 

@@ -371,6 +371,23 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
                  : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialization) start its blocks now; they wait for this grid's completion at
+// their griddepcontrol.wait before reading what it writes.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this kernel depends on have completed and their
+// memory is visible (returns at once when there is no such dependency).
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
 // another CTA's shared memory in the cluster by the copy engine; the bytes
 // complete the transaction count of an mbarrier in the DESTINATION CTA.

@@ -97,6 +97,11 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     extern __shared__ uint32_t s_keys[];                 // [slice] when kCached
     __shared__ TopkShared sh;
 
+    // launched as a programmatic dependent of the previous kernel of the stream:
+    // nothing it may have written is read before this wait (the launch latency
+    // is what overlaps); the MLA that follows may then start its blocks
+    pdl_wait();
+    pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t crank = cluster_ctarank();
     const int C = static_cast<int>(gridDim.x);           // cluster spans gridDim.x
@@ -453,13 +458,17 @@ dsa_status launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t st
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the kernel's blocks may start while the
+    // logits kernel finishes; they wait (griddepcontrol.wait) before reading it
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e;
     if (cached) {
         e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
