@@ -18,6 +18,8 @@ indexer_score_topk is timed beside it, --fused makes it the headline).  Reported
 * spec_mxfp4, prefill  the speculative/varlen MXFP4 and the causal prefill
                indexer configurations timed the same way (their own value,
                kernel times and roofline: HBM for MXFP4, FP8 tensor for prefill);
+* kv_scatter   the K-cache quantise/scatter of a prefill's and a decode step's
+               new tokens into FP8 and MXFP4 paged caches, with its HBM roofline;
 * full_step    the whole graph-captured step of the full decode workload
                (indexer + top-k + sparse MLA, 128 heads 576/512) in us/step,
                with each stage also timed alone and the sparse MLA's tensor
@@ -411,6 +413,8 @@ def run_ours(args, rank, world, local):
             result["spec_mxfp4"] = measure_indexer_config("spec_mxfp4", dev, n_side, flush, fused)
             result["prefill"] = measure_indexer_config("prefill", dev, max(5, min(20, args.steps)), flush,
                                                        False)
+        if not args.skip_configs:
+            result["kv_scatter"] = measure_scatter(dev, flush, n_side)
         if not args.skip_full_step:
             result["full_step"] = measure_full_step(dev, args, flush, fused=fused)
             result["full_step_indexer_h64"] = measure_full_step(dev, args, flush, "full_step_h64", fused=fused)
@@ -552,6 +556,50 @@ def measure_full_step(dev, args, flush, workload="full_step", fused=True):
                              "algorithmic_flops": mla_flops,
                              "traffic": load_traffic("sparse_mla_tc", "full_step") if workload == "full_step" else None},
             "launches_per_step": st.launches_per_step(), "device_status": status}
+
+
+def measure_scatter(dev, flush, steps):
+    """K-cache quantise/scatter of one prefill's and one decode step's new tokens
+    (bf16 K, 128 dims) into a shuffled page-64 FP8 cache and a page-32 MXFP4
+    cache; HBM roofline on the algorithmic bytes (K read once, codes + scales
+    written once, slot mapping read once)."""
+    from deepseek_sparse_attention_mqa_gb300 import _abi
+    hbm, _, _, src = measured_peaks()
+    out = {}
+    for name, n, fmt, P in (("prefill_fp8", 16384, 0, 64), ("prefill_mxfp4", 16384, 1, 32),
+                            ("decode_fp8", 64, 0, 64)):
+        D = 128
+        g = torch.Generator(device=dev).manual_seed(7)
+        pages = 2 * ((n + P - 1) // P)
+        tok = D if fmt == 0 else D // 2
+        stok = 4 if fmt == 0 else D // 32
+        vals = torch.zeros((pages, P * tok), dtype=torch.uint8, device=dev)
+        scs = torch.zeros((pages, P * stok + (16 if fmt == 1 else 0)), dtype=torch.uint8, device=dev)
+        bt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+        cache = _abi.make_cache(fmt, D, P, pages, vals, P * tok, tok, scs, scs.shape[1], stok, bt)
+        k = torch.randn((n, D), generator=g, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(pages * P, generator=g, device=dev)[:n].to(torch.int64)
+        stream = torch.cuda.current_stream()
+        for _ in range(3):
+            _abi.kv_quantize_scatter(k, slots, cache)
+        ts = []
+        for i in range(steps):
+            flush(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            _abi.kv_quantize_scatter(k, slots, cache)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(ts)
+        nbytes = n * (D * 2 + tok + stok + 8)
+        out[name] = {"tokens": n, "head_dim": D, "format": "e4m3 + fp32 token scale" if fmt == 0 else "MXFP4",
+                     "page_kv": P, "us_median": round(us, 2),
+                     "roofline": {"bound": "hbm", "achieved": round(nbytes / (us * 1e-6) / 1e9, 1), "peak": hbm,
+                                  "unit": "GB/s", "frac": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4),
+                                  "peak_source": src, "algorithmic_bytes": nbytes}}
+    return out
 
 
 def cpu_baseline(case, pairs, mac_budget=12e9):
