@@ -118,8 +118,8 @@ __host__ __device__ constexpr MlaSmem mla_smem()
     MlaSmem m{};
     m.q = 0;
     m.lat = m.q + kQChunkBytes;                      // the rope chunk of Q (value dims are in TMEM)
-    m.p = m.lat + kLatBufs * kMaxChunks * kLChunkBytes;
-    m.x = m.p + 128 * 128;
+    m.p = m.lat + kLatBufs * kMaxChunks * kLChunkBytes;  // (P lives in TMEM, in its block's S columns)
+    m.x = m.p;
     m.xs = m.x + 128 * kNT * 4;                      // this CTA's partial scores, staged for the peer
     m.scale = m.xs + 128 * kNT * 4;
     m.valid = m.scale + kLatBufs * kNT * 4;
@@ -180,7 +180,6 @@ sparse_mla_tc_kernel(const MlaParams p)
     constexpr MlaSmem mp = mla_smem();
     uint8_t* sQ = smem + mp.q;
     uint8_t* sLat = smem + mp.lat;
-    uint8_t* sP = smem + mp.p;
     uint8_t* sX = smem + mp.x;
     uint8_t* sXs = smem + mp.xs;
     float* sScale = reinterpret_cast<float*>(smem + mp.scale);
@@ -254,7 +253,7 @@ sparse_mla_tc_kernel(const MlaParams p)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&s_empty[i]), 8);
+            mbar_init(smem_u32(&s_empty[i]), 1);   // PV of the block that used the buffer (it holds P)
         }
         for (int i = 0; i < 8; ++i) {
             mbar_init(smem_u32(&xw_full[i]), 1);    // local expect_tx + the peer warp's bulk copy bytes
@@ -521,20 +520,21 @@ sparse_mla_tc_kernel(const MlaParams p)
             };
             auto issue_pv = [&](int j) {
                 tc_fence_after_sync();
-                // O[:, v] += P[:, t] V[t, v]: A = P (K-major over tokens), B = V read
-                // MN-major from the latent tile (64-dim blocks 8 KB apart = LBO,
-                // 8-token groups 1 KB apart = SBO)
+                // O[:, v] += P[:, t] V[t, v]: A = P from TMEM (lane = head, the f16
+                // token pairs the softmax wrote over this block's S columns, 8
+                // columns per 16-token step), B = V read MN-major from the latent
+                // tile (64-dim blocks 8 KB apart = LBO, 8-token groups 1 KB apart = SBO)
                 const uint32_t d = tmem_base + 256;
-                const uint32_t pa = smem_u32(sP);
+                const uint32_t pa = tmem_base + static_cast<uint32_t>((j & 1) * kNT);
                 const uint32_t vb = smem_u32(sLat + (j % kLatBufs) * (kMaxChunks * kLChunkBytes));
 #pragma unroll
                 for (int ks = 0; ks < kNT / 16; ++ks) {
-                    const uint64_t ad = make_smem_desc(pa + ks * 32, 16, 1024, kLayoutSw128);
                     const uint64_t bd = make_smem_desc(vb + ks * 2048, kLChunkBytes, 1024, kLayoutSw128);
-                    umma_f16(d, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16_ts(d, pa + ks * 8, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(smem_u32(p_empty));
                 umma_commit(smem_u32(&lat_empty[j % kLatBufs]));
+                umma_commit(smem_u32(&s_empty[j & 1]));   // the S/P buffer is free for QK(j + 2)
             };
             int jq = 0, jp = 0;                         // next QK / PV block to issue
             uint64_t t_idle = 0;
@@ -581,10 +581,12 @@ sparse_mla_tc_kernel(const MlaParams p)
         // waits, so a warp that gives up cannot strand its partner)
         uint32_t pair_uses = 0;
         auto pair_sync = [&]() -> bool {
+            tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&pair_bar[quarter]));
             const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pair_bar[quarter]), pair_uses & 1));
+            tc_fence_after_sync();
             ++pair_uses;
             return r;
         };
@@ -617,10 +619,6 @@ sparse_mla_tc_kernel(const MlaParams p)
             uint32_t ra[32];
             tmem_ld_32x32b_x32(tmem_base + lane_base + sb * kNT + tcol, ra);
             tmem_ld_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_u32(&s_empty[sb]));
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 ra[i] = __float_as_uint(__uint_as_float(ra[i]) * qback);
@@ -693,12 +691,6 @@ sparse_mla_tc_kernel(const MlaParams p)
                 break;
             }
             const float m_blk = fmaxf(sMax[h], sMax[128 + h]);
-            // P of the previous block has been consumed (and O is stable) before
-            // P is rewritten or O rescaled
-            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(p_empty), (j - 1) & 1))) {
-                ok = false;
-                break;
-            }
             const float m_new = fmaxf(m_run, m_blk);
             // lazily refreshed running max: a head moves its max only when it grew
             // by more than 2^8 (both threads of the head decide alike); the O
@@ -714,7 +706,12 @@ sparse_mla_tc_kernel(const MlaParams p)
                 m_run = m_new;
             }
             if (__any_sync(0xffffffffu, f != 1.f)) {
-                // j > 0 here: O holds blocks < j and PV(j - 1) has completed
+                // j > 0 here: O holds blocks < j; PV(j - 1) has to complete before O
+                // is rescaled
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(p_empty), (j - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after_sync();
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
@@ -729,24 +726,23 @@ sparse_mla_tc_kernel(const MlaParams p)
                 }
                 tmem_st_wait();
             }
-            // P (f16, token scale folded in for V) -> row h, units [half*4, half*4 + 4)
-            // of the swizzled K-major tile
+            // P (f16, token scale folded in for V) -> TMEM lane h, over this block's
+            // S columns: token pair (t, t + 1) of this thread's half in column
+            // sb * 64 + half * 16 + t / 2 (both threads of the pair have read
+            // their scores: the pair sync above ordered their loads)
             const float m_use = m_run == -INFINITY ? 0.f : m_run;
+            uint32_t pk[16];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                    const int t = 8 * u + 2 * q2;
-                    const float p0 = exp2f(sco[t] - m_use);          // -inf -> 0
-                    const float p1 = exp2f(sco[t + 1] - m_use);
-                    l_run += p0 + p1;
-                    const __half2 b = __floats2half2_rn(p0 * scl[t], p1 * scl[t + 1]);
-                    pk[q2] = *reinterpret_cast<const uint32_t*>(&b);
-                }
-                *reinterpret_cast<uint4*>(sP + swizzled_offset(h, half * 4 + u, 128)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int t2 = 0; t2 < 16; ++t2) {
+                const int t = 2 * t2;
+                const float p0 = exp2f(sco[t] - m_use);          // -inf -> 0
+                const float p1 = exp2f(sco[t + 1] - m_use);
+                l_run += p0 + p1;
+                const __half2 b = __floats2half2_rn(p0 * scl[t], p1 * scl[t + 1]);
+                pk[t2] = *reinterpret_cast<const uint32_t*>(&b);
             }
-            fence_proxy_async_smem();
+            tmem_st_32x32b_x16(tmem_base + lane_base + sb * kNT + half * 16, pk);
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
