@@ -195,7 +195,11 @@ sparse_mla_tc_kernel(const MlaParams p)
     uint64_t* s_empty = bars + 9;    // [2]
     uint64_t* xw_full = bars + 24;   // [8] per softmax warp: the peer's partial scores arrived in sX
     uint64_t* xw_free = bars + 32;   // [8] per softmax warp: the peer consumed what this warp sent
-    uint64_t* p_full = bars + 13;
+    // [2] per S/P buffer: the 8 softmax warps wrote P of the buffer's block.  One
+    // barrier per buffer, because a warp may write P(j + 1) before a warp of
+    // another lane quarter has written P(j); P(j + 2) cannot come before PV(j)
+    // has completed, so a phase never mixes two blocks' arrivals.
+    uint64_t* p_full = bars + 11;
     uint64_t* p_empty = bars + 14;
     uint64_t* o_done = bars + 15;
     uint64_t* pair_bar = bars + 16;  // [4] the two softmax warps of a lane quarter
@@ -254,12 +258,12 @@ sparse_mla_tc_kernel(const MlaParams p)
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
             mbar_init(smem_u32(&s_empty[i]), 1);   // PV of the block that used the buffer (it holds P)
+            mbar_init(smem_u32(&p_full[i]), 8);
         }
         for (int i = 0; i < 8; ++i) {
             mbar_init(smem_u32(&xw_full[i]), 1);    // local expect_tx + the peer warp's bulk copy bytes
             mbar_init(smem_u32(&xw_free[i]), 1);    // the peer warp's remote arrive
         }
-        mbar_init(smem_u32(p_full), 8);
         mbar_init(smem_u32(p_empty), 1);
         mbar_init(smem_u32(o_done), 1);
         for (int i = 0; i < 4; ++i)
@@ -547,7 +551,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                     progress = true;
                 }
                 // PV(jp): P_jp is written (S(jp) was issued before, so jp < jq)
-                if (jp < jq && mbar_test_wait(smem_u32(p_full), jp & 1)) {
+                if (jp < jq && mbar_test_wait(smem_u32(&p_full[jp & 1]), (jp >> 1) & 1)) {
                     issue_pv(jp++);
                     progress = true;
                 }
@@ -746,7 +750,7 @@ sparse_mla_tc_kernel(const MlaParams p)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_u32(p_full));
+                mbar_arrive(smem_u32(&p_full[sb]));
         }
         if (!ok)
             *s_abort = 1;
