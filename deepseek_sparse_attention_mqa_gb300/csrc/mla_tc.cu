@@ -22,10 +22,12 @@
 //
 //   warps 0-3, 9-12  softmax, two threads per head (TMEM lane = head): warps
 //              0-3 take tokens 0-31 of each block, warps 9-12 tokens 32-63.
-//              Each sends its half of the partial scores to the peer CTA with
-//              st.async (completing on the peer's mbarrier), adds the peer's
-//              half, scales by token scale * softmax scale and keeps an online
-//              max / sum in base 2; the two threads of a head combine their
+//              Each warp sends its partial scores to the same warp of the peer
+//              CTA with one bulk shared-memory copy (completing on that warp's
+//              mbarrier), adds the peer's, scales and masks each token pair with
+//              one packed FMA (token scale * softmax scale * log2 e, and a -inf
+//              bias for empty slots) and keeps an online max / sum in base 2
+//              (packed fp32 pairs, hardware exp2); the two threads of a head combine their
 //              block maxima through shared memory and a two-thread mbarrier.
 //              The running max is refreshed lazily (O in TMEM is rescaled only
 //              when the max grows by more than 2^8).  P is written as f16
@@ -65,7 +67,7 @@ constexpr int kMmaWarp = 8;
 constexpr int kSoftWarp1 = 9;           // softmax warps 0-3 (tokens 0-31) and 9-12 (tokens 32-63)
 constexpr uint32_t kTmemCols = 512;     // S[2] at columns 0 / 64, Q (value dims, f16 pairs) at 128, O at 256
 constexpr uint32_t kQCol = 128;
-constexpr int kLatBufs = 3;             // latent tiles (with their scales and valid flags) in flight
+constexpr int kLatBufs = 3;             // latent tiles (with their per-token scales, multipliers and biases) in flight
 constexpr float kRescaleLog2 = 8.f;     // refresh the running max only past 2^8
 constexpr int kMaxSeg = 18;             // 16-byte FP8 segments per token and CTA (256 + 32 dims)
 constexpr int kGatherItems = (16 * kMaxSeg + 31) / 32;      // 16-byte segments per gather lane
@@ -110,7 +112,7 @@ struct MlaParams {
 };
 
 struct MlaSmem {
-    uint32_t q, lat, p, x, xs, scale, valid, qexp, red, bar, misc, total;
+    uint32_t q, lat, p, x, xs, scale, mult, bias, qexp, red, bar, misc, total;
 };
 
 __host__ __device__ constexpr MlaSmem mla_smem()
@@ -122,8 +124,9 @@ __host__ __device__ constexpr MlaSmem mla_smem()
     m.x = m.p;
     m.xs = m.x + 128 * kNT * 4;                      // this CTA's partial scores, staged for the peer
     m.scale = m.xs + 128 * kNT * 4;
-    m.valid = m.scale + kLatBufs * kNT * 4;
-    m.qexp = m.valid + kLatBufs * kNT * 4;
+    m.mult = m.scale + kLatBufs * kNT * 4;          // per token: scale * softmax scale * log2(e), 0 if none
+    m.bias = m.mult + kLatBufs * kNT * 4;            // per token: 0, or -inf for a slot with no token
+    m.qexp = m.bias + kLatBufs * kNT * 4;
     m.red = m.qexp + 128 * 4;
     m.bar = m.red + 2 * 2 * 128 * 4;
     m.misc = m.bar + 40 * 8;
@@ -183,7 +186,8 @@ sparse_mla_tc_kernel(const MlaParams p)
     uint8_t* sX = smem + mp.x;
     uint8_t* sXs = smem + mp.xs;
     float* sScale = reinterpret_cast<float*>(smem + mp.scale);
-    int* sValid = reinterpret_cast<int*>(smem + mp.valid);
+    float* sMult = reinterpret_cast<float*>(smem + mp.mult);
+    float* sBias = reinterpret_cast<float*>(smem + mp.bias);
     int* sQexp = reinterpret_cast<int*>(smem + mp.qexp);       // per-head power-of-two Q scale
     float* sMax = reinterpret_cast<float*>(smem + mp.red);        // [2][128] block max per half
     float* sSum = sMax + 2 * 128;                                  // [2][128] final sum per half
@@ -462,7 +466,8 @@ sparse_mla_tc_kernel(const MlaParams p)
             }
             if (lane < 16) {
                 sScale[st * kNT + gw * 16 + lane] = scale0;
-                sValid[st * kNT + gw * 16 + lane] = valid0;
+                sMult[st * kNT + gw * 16 + lane] = valid0 ? scale0 * p.scale_log2 : 0.f;
+                sBias[st * kNT + gw * 16 + lane] = valid0 ? 0.f : -INFINITY;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -623,9 +628,12 @@ sparse_mla_tc_kernel(const MlaParams p)
             uint32_t ra[32];
             tmem_ld_32x32b_x32(tmem_base + lane_base + sb * kNT + tcol, ra);
             tmem_ld_wait();
+            // this CTA's partial scores as token pairs, scaled back by 2^-e (exact)
+            uint64_t sc2[16];
+            const uint64_t qb2 = pack_f32x2(qback, qback);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                ra[i] = __float_as_uint(__uint_as_float(ra[i]) * qback);
+            for (int i = 0; i < 16; ++i)
+                sc2[i] = mul_f32x2(pack_f32x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), qb2);
 
             // ---- exchange partial scores with the peer CTA (one bulk copy per warp)
             if (lane == 0)
@@ -638,8 +646,8 @@ sparse_mla_tc_kernel(const MlaParams p)
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<uint4*>(stage_row + ((u ^ (lane & 7)) << 4)) =
-                    make_uint4(ra[4 * u], ra[4 * u + 1], ra[4 * u + 2], ra[4 * u + 3]);
+                *reinterpret_cast<ulonglong2*>(stage_row + ((u ^ (lane & 7)) << 4)) =
+                    make_ulonglong2(sc2[2 * u], sc2[2 * u + 1]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
@@ -648,24 +656,13 @@ sparse_mla_tc_kernel(const MlaParams p)
                 ok = false;
                 break;
             }
-            float sco[32];
+            // full scores: own + peer partial (IEEE addition commutes, so both CTAs
+            // get the same bits)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const float4 x = *reinterpret_cast<const float4*>(recv_row + ((u ^ (lane & 7)) << 4));
-                // both CTAs form partial(CTA 0) + partial(CTA 1) in the same order
-                const float o0 = __uint_as_float(ra[4 * u]), o1 = __uint_as_float(ra[4 * u + 1]);
-                const float o2 = __uint_as_float(ra[4 * u + 2]), o3 = __uint_as_float(ra[4 * u + 3]);
-                if (crank == 0) {
-                    sco[4 * u + 0] = o0 + x.x;
-                    sco[4 * u + 1] = o1 + x.y;
-                    sco[4 * u + 2] = o2 + x.z;
-                    sco[4 * u + 3] = o3 + x.w;
-                } else {
-                    sco[4 * u + 0] = x.x + o0;
-                    sco[4 * u + 1] = x.y + o1;
-                    sco[4 * u + 2] = x.z + o2;
-                    sco[4 * u + 3] = x.w + o3;
-                }
+                const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(recv_row + ((u ^ (lane & 7)) << 4));
+                sc2[2 * u] = add_f32x2(sc2[2 * u], x.x);
+                sc2[2 * u + 1] = add_f32x2(sc2[2 * u + 1], x.y);
             }
             // X is consumed (its values are in registers): hand it back to the
             // peer.  A relaxed arrive: a releasing one would also wait for this
@@ -674,20 +671,27 @@ sparse_mla_tc_kernel(const MlaParams p)
             if (lane == 0)
                 mbar_arrive_remote_relaxed(peer_free);
 
-            // ---- scores in base 2; masked slots are -inf
+            // ---- scores in base 2, one packed FMA per token pair: score * (token
+            // scale * softmax scale * log2 e) + (0, or -inf for a slot with no token;
+            // its gathered row is zero, so its score is 0 and the FMA gives -inf)
             const int lb = j % kLatBufs;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&lat_full[lb]), (j / kLatBufs) & 1))) {
                 ok = false;
                 break;
             }
-            const float* scl = sScale + lb * kNT + tcol;
-            const int* vld = sValid + lb * kNT + tcol;
-            float m_half = -INFINITY;
+            const ulonglong2* mul4 = reinterpret_cast<const ulonglong2*>(sMult + lb * kNT + tcol);
+            const ulonglong2* bia4 = reinterpret_cast<const ulonglong2*>(sBias + lb * kNT + tcol);
+            float mh0 = -INFINITY, mh1 = -INFINITY;
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                sco[t] = vld[t] ? sco[t] * (scl[t] * p.scale_log2) : -INFINITY;
-                m_half = fmaxf(m_half, sco[t]);
+            for (int u = 0; u < 8; ++u) {
+                const ulonglong2 mu = mul4[u], bi = bia4[u];
+                sc2[2 * u] = fma_f32x2(sc2[2 * u], mu.x, bi.x);
+                sc2[2 * u + 1] = fma_f32x2(sc2[2 * u + 1], mu.y, bi.y);
+                const float2 a = unpack_f32x2(sc2[2 * u]), b = unpack_f32x2(sc2[2 * u + 1]);
+                mh0 = fmaxf(mh0, fmaxf(a.x, b.x));
+                mh1 = fmaxf(mh1, fmaxf(a.y, b.y));
             }
+            const float m_half = fmaxf(mh0, mh1);
             // block max of the head over both halves
             sMax[half * 128 + h] = m_half;
             if (!pair_sync()) {
@@ -719,7 +723,7 @@ sparse_mla_tc_kernel(const MlaParams p)
                 tc_fence_after_sync();
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
-                    uint32_t o[16];                       // 16 columns at a time: sco[] stays in registers
+                    uint32_t o[16];                       // 16 columns at a time: the scores stay in registers
                     const uint32_t col = 256 + half * 128 + c * 16;
                     tmem_ld_32x32b_x16(tmem_base + lane_base + col, o);
                     tmem_ld_wait();
@@ -735,16 +739,25 @@ sparse_mla_tc_kernel(const MlaParams p)
             // sb * 64 + half * 16 + t / 2 (both threads of the pair have read
             // their scores: the pair sync above ordered their loads)
             const float m_use = m_run == -INFINITY ? 0.f : m_run;
+            const uint64_t negm = pack_f32x2(-m_use, -m_use);
+            const ulonglong2* scl4 = reinterpret_cast<const ulonglong2*>(sScale + lb * kNT + tcol);
+            uint64_t l2 = pack_f32x2(0.f, 0.f);
             uint32_t pk[16];
 #pragma unroll
-            for (int t2 = 0; t2 < 16; ++t2) {
-                const int t = 2 * t2;
-                const float p0 = exp2f(sco[t] - m_use);          // -inf -> 0
-                const float p1 = exp2f(sco[t + 1] - m_use);
-                l_run += p0 + p1;
-                const __half2 b = __floats2half2_rn(p0 * scl[t], p1 * scl[t + 1]);
-                pk[t2] = *reinterpret_cast<const uint32_t*>(&b);
+            for (int u = 0; u < 8; ++u) {
+                const ulonglong2 sv = scl4[u];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float2 d = unpack_f32x2(add_f32x2(sc2[2 * u + e], negm));
+                    const uint64_t pp = pack_f32x2(ex2_approx(d.x), ex2_approx(d.y));   // -inf -> 0
+                    l2 = add_f32x2(l2, pp);
+                    const float2 pv = unpack_f32x2(mul_f32x2(pp, e == 0 ? sv.x : sv.y));
+                    const __half2 b = __floats2half2_rn(pv.x, pv.y);
+                    pk[2 * u + e] = *reinterpret_cast<const uint32_t*>(&b);
+                }
             }
+            const float2 lp = unpack_f32x2(l2);
+            l_run += lp.x + lp.y;
             tmem_st_32x32b_x16(tmem_base + lane_base + sb * kNT + half * 16, pk);
             tmem_st_wait();
             tc_fence_before_sync();
