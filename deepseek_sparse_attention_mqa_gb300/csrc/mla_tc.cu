@@ -176,7 +176,7 @@ __device__ __forceinline__ float exp2_int(int e)
 // fewer values live).
 template <bool kDual>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-sparse_mla_tc_kernel(const MlaParams p)
+sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const MlaParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -204,6 +204,7 @@ sparse_mla_tc_kernel(const MlaParams p)
     // another lane quarter has written P(j); P(j + 2) cannot come before PV(j)
     // has completed, so a phase never mixes two blocks' arrivals.
     uint64_t* p_full = bars + 11;
+    uint64_t* q_stage = bars + 13;   // the Q slice staged in shared memory
     uint64_t* p_empty = bars + 14;
     uint64_t* o_done = bars + 15;
     uint64_t* pair_bar = bars + 16;  // [4] the two softmax warps of a lane quarter
@@ -255,6 +256,7 @@ sparse_mla_tc_kernel(const MlaParams p)
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(q_full), 4);
+        mbar_init(smem_u32(q_stage), 1);
         for (int i = 0; i < kLatBufs; ++i) {
             mbar_init(smem_u32(&lat_full[i]), 4);
             mbar_init(smem_u32(&lat_empty[i]), 1);
@@ -288,78 +290,25 @@ sparse_mla_tc_kernel(const MlaParams p)
     if (warp >= kConvWarp0 && warp < kMmaWarp) {
         // ================================ gather ================================
         const int ct = threadIdx.x - kConvWarp0 * 32;   // 0..127
-        // Q slice -> f16 swizzled K-major tile (row = head, 8 units of 16 B per
-        // chunk).  Thread ct owns head ct: Q is scaled by 2^e, e chosen per head
-        // from this CTA's slice so that max|q| 2^e lies in [2^14, 2^15) -- exact,
-        // and inside f16 range whatever the bf16 magnitudes; the partial scores
-        // are scaled back by 2^-e in fp32.
-        {
-            const int h = ct;
-            // f16 unit u (8 dims) of this CTA's slice: two units per FP8 segment
-            const __nv_bfloat16* qh = p.q + (static_cast<int64_t>(row) * p.num_heads + h) * p.d_qk;
-            const int nunit = 2 * nseg;
-            auto qdim = [&](int u) -> int { return seg_dim(u >> 1) + (u & 1) * 8; };
-            float amax = 0.f;
-            if (h < p.num_heads)
-                for (int u = 0; u < nunit; ++u) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(qh + qdim(u));
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[i]));
-                        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-                    }
-                }
-            int e = 0;
-            if (amax > 0.f && amax <= 3.0e38f) {
-                int ex;
-                frexpf(amax, &ex);                          // amax in [2^(ex-1), 2^ex)
-                e = max(-100, min(100, 15 - ex));
-            }
-            sQexp[h] = e;
-            const float sc = exp2_int(e);
-            auto conv = [&](int u) -> uint4 {              // 8 dims of unit u, f16 x 2^e
-                uint4 o = make_uint4(0, 0, 0, 0);
-                if (h < p.num_heads) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(qh + qdim(u));
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t r4[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[i]));
-                        const __half2 hf = __floats2half2_rn(f.x * sc, f.y * sc);
-                        r4[i] = *reinterpret_cast<const uint32_t*>(&hf);
-                    }
-                    o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
-                }
-                return o;
-            };
-            // the 256 value dims go to TMEM lane h (this warp's lane quarter),
-            // columns [kQCol, kQCol + 128): 32 columns (8 units) per store
-            const uint32_t q_lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
-#pragma unroll 1
-            for (int r = 0; r < 4; ++r) {
-                uint32_t wv[32];
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    const uint4 o = conv(8 * r + b);
-                    wv[4 * b] = o.x;
-                    wv[4 * b + 1] = o.y;
-                    wv[4 * b + 2] = o.z;
-                    wv[4 * b + 3] = o.w;
-                }
-                tmem_st_32x32b_x32(tmem_base + q_lane + kQCol + 32 * r, wv);
-            }
-            tmem_st_wait();
-            // the rope dims (d_qk 576) go to the shared-memory chunk
-            for (int u = 32; u < nunit; ++u)
-                *reinterpret_cast<uint4*>(sQ + swizzled_offset(h, u - 32, 128)) = conv(u);
+        // Q slice -> f16.  Thread ct owns head ct: Q is scaled by 2^e, e chosen
+        // per head from this CTA's slice so that max|q| 2^e lies in [2^14, 2^15)
+        // -- exact, and inside f16 range whatever the bf16 magnitudes; the
+        // partial scores are scaled back by 2^-e in fp32.  The slice is first
+        // staged in shared memory (the latent tiles are not in use yet) by five
+        // TMA boxes of 128 heads x 64 dims, 128B-swizzled: its four 64-dim value
+        // chunks and the rope chunk (dims 512-575, of which this CTA takes 32),
+        // so that one thread per head reads its 16-byte units without bank
+        // conflicts.  Read directly from global memory, each warp load touched
+        // 32 rows 1152 B apart and the loads serialised in the load/store unit.
+        const uint8_t* qst = sLat;
+        const int nunit = 2 * nseg;
+        if (warp == kConvWarp0 && lane == 0) {
+            const int nbox = rope ? 5 : 4;
+            mbar_arrive_expect_tx(smem_u32(q_stage), static_cast<uint32_t>(nbox * 128 * 128));
+            for (int b = 0; b < nbox; ++b)
+                tma_load_2d(smem_u32(qst + b * 128 * 128), &tm_q, smem_u32(q_stage),
+                            b < 4 ? static_cast<int>(crank) * 256 + 64 * b : 512, row * p.num_heads);
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(q_full));
 
         const int32_t* irow = p.idx + static_cast<int64_t>(row) * p.idx_stride;
         const int gw = warp - kConvWarp0;               // this warp gathers tokens [16 gw, 16 gw + 16) of a block
@@ -437,6 +386,84 @@ sparse_mla_tc_kernel(const MlaParams p)
         int s0 = load_idx(0), s1 = load_idx(1), s2 = load_idx(2), s3 = load_idx(3);
         const int pg0 = load_page(s0), pg1 = load_page(s1);
         int pg2 = load_page(s2);
+        // (the index and block-table loads above fly while Q is prepared)
+        bool q_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(q_stage), 0));
+        if (!q_ok)
+            *s_abort = 1;
+        {
+            const int h = ct;
+            const bool hv = q_ok && h < p.num_heads;
+            auto unit = [&](int u) -> uint4 {
+                // value unit u < 32: box u / 8, 16-byte unit u % 8 of head h's 128 B row;
+                // rope unit u - 32: box 4, unit 4 crank + u - 32
+                const uint32_t off = u < 32 ? (u >> 3) * 16384u + swizzled_offset(h, u & 7, 128)
+                                            : 4u * 16384u + swizzled_offset(h, crank * 4 + (u - 32), 128);
+                return hv ? *reinterpret_cast<const uint4*>(qst + off) : make_uint4(0, 0, 0, 0);
+            };
+            // max |q| of the slice: for non-negative bf16 values the order of the bit
+            // patterns as unsigned 16-bit integers is the order of the values, so
+            // the sign bits are masked off and two values are compared per
+            // packed integer max
+            uint32_t m2 = 0;
+#pragma unroll 4
+            for (int u = 0; u < nunit; ++u) {
+                const uint4 v = unit(u);
+                m2 = __vmaxu2(m2, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+                m2 = __vmaxu2(m2, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+            }
+            const float amax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+            int e = 0;
+            if (amax > 0.f && amax <= 3.0e38f) {
+                int ex;
+                frexpf(amax, &ex);                          // amax in [2^(ex-1), 2^ex)
+                e = max(-100, min(100, 15 - ex));
+            }
+            sQexp[h] = e;
+            const float sc = exp2_int(e);
+            const uint64_t sc2 = pack_f32x2(sc, sc);
+            auto conv = [&](int u) -> uint4 {              // 8 dims of unit u, f16 x 2^e
+                const uint4 v = unit(u);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                uint32_t r4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    // bf16 -> fp32 is a 16-bit shift; times 2^e (exact), then f16
+                    const float2 f = unpack_f32x2(mul_f32x2(
+                        pack_f32x2(__uint_as_float(w4[i] << 16), __uint_as_float(w4[i] & 0xFFFF0000u)), sc2));
+                    const __half2 hf = __floats2half2_rn(f.x, f.y);
+                    r4[i] = *reinterpret_cast<const uint32_t*>(&hf);
+                }
+                return make_uint4(r4[0], r4[1], r4[2], r4[3]);
+            };
+            // the 256 value dims go to TMEM lane h (this warp's lane quarter),
+            // columns [kQCol, kQCol + 128): 32 columns (8 units) per store
+            const uint32_t q_lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+#pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+                uint32_t wv[32];
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const uint4 o = conv(8 * r + b);
+                    wv[4 * b] = o.x;
+                    wv[4 * b + 1] = o.y;
+                    wv[4 * b + 2] = o.z;
+                    wv[4 * b + 3] = o.w;
+                }
+                tmem_st_32x32b_x32(tmem_base + q_lane + kQCol + 32 * r, wv);
+            }
+            tmem_st_wait();
+            // the rope dims (d_qk 576) go to the shared-memory chunk
+            for (int u = 32; u < nunit; ++u)
+                *reinterpret_cast<uint4*>(sQ + swizzled_offset(h, u - 32, 128)) = conv(u);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(q_full));
+        // all four gather warps read staged Q rows from the latent tiles: none
+        // writes a tile before all are done (named barrier 1, the 128 gather threads)
+        named_bar_sync(1, 128);
         int64_t off0, soff0, off1, soff1;
         int valid0, valid1;
         address(s0, pg0, off0, soff0, valid0);
@@ -872,11 +899,22 @@ dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStr
     p.batch = a.batch;
     const bool dual = a.topk_lens || a.swa || a.cum_q;
     auto kern = dual ? sparse_mla_tc_kernel<true> : sparse_mla_tc_kernel<false>;
+    // q as [rows * num_heads][d_qk] bf16, boxes of 64 dims x 128 heads, 128B-swizzled
+    CUtensorMap tm_q;
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.d_qk), static_cast<uint64_t>(a.rows) * a.num_heads};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.d_qk) * 2};
+        const uint32_t box[2] = {64, 128};
+        const dsa_status st = encode_tiled(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, dims, strides, box,
+                                           CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != DSA_OK)
+            return st;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    // programmatic dependent launch: Q preparation, TMEM and barrier set-up
-    // overlap the end of the previous kernel; the gather waits for it
+    // programmatic dependent launch: the launch overlaps the end of the
+    // previous kernel, which the kernel waits for at entry
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, a.rows, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -887,7 +925,7 @@ dsa_status launch_sparse_mla_tc(const MlaArgs& a, const DeviceInfo& dev, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tm_q, p);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return check_launch();
