@@ -490,6 +490,7 @@ def measure_full_step(dev, args, flush, workload="full_step", fused=True):
     from deepseek_sparse_attention_mqa_gb300 import inputs
     from deepseek_sparse_attention_mqa_gb300.step import SparseAttentionStep
     case = inputs.make_case(workload, device=dev)
+    torch.cuda.empty_cache()             # drop the generator's temporaries (the latent pool is built in fp32)
     st = SparseAttentionStep(case, with_mla=True, fused=fused)
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
