@@ -171,3 +171,89 @@ class SparseAttentionStep:
 
     def device_status(self) -> int:
         return _abi.device_status(self.status)
+
+
+class HostStepPipeline:
+    """Steps fed from pinned host memory with their copies overlapped, the way a
+    serving loop runs: two slots, each with its own input arena
+    (``StepInputs``), step buffers and pinned result buffer, and three streams.
+    The inputs of step i are copied in on the input stream once step i - 2 (the
+    slot's previous user) has finished computing; step i runs on the compute
+    stream once its inputs are in; its top-k indices go back to the host on the
+    output stream once it has run.  So the copies of step i + 1 and step i - 1
+    overlap the computation of step i.
+
+    ``submit()`` enqueues one step and returns its slot; ``results(slot)`` waits
+    for that slot's indices and returns the pinned host tensor (valid until the
+    slot is submitted again).  Write a step's inputs into ``inputs[slot].host``
+    before submitting it to that slot.  With ``graphs`` (the default) each
+    slot's computation is captured once in a CUDA graph and replayed, so a
+    submission costs the host two copies, four event operations and one replay
+    instead of one library call per kernel."""
+
+    def __init__(self, case: Case, with_mla: bool = False, fused: bool = False, graphs: bool = True):
+        self.inputs = [StepInputs(case, with_mla=with_mla) for _ in range(2)]
+        self.steps = [SparseAttentionStep(ins.case(), with_mla=with_mla, fused=fused) for ins in self.inputs]
+        self.idx_host = [torch.empty(st.idx.shape, dtype=torch.int32).pin_memory() for st in self.steps]
+        self.h2d_stream = torch.cuda.Stream()
+        self.compute_stream = torch.cuda.Stream()
+        self.d2h_stream = torch.cuda.Stream()
+        self._in_ready = [torch.cuda.Event() for _ in range(2)]
+        self._computed = [torch.cuda.Event() for _ in range(2)]
+        self._out_ready = [torch.cuda.Event() for _ in range(2)]
+        self._used = [False, False]
+        self._next = 0
+        # the arenas were filled on the current stream at construction
+        for s in (self.h2d_stream, self.compute_stream, self.d2h_stream):
+            s.wait_stream(torch.cuda.current_stream())
+        self.graphs = None
+        if graphs:
+            with torch.cuda.stream(self.compute_stream):
+                for st in self.steps:                   # warm-up outside the capture
+                    st.run(self.compute_stream)
+            self.compute_stream.synchronize()
+            self.graphs = []
+            for st in self.steps:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.compute_stream):
+                    st.run(self.compute_stream)
+                self.graphs.append(g)
+            self.compute_stream.synchronize()
+
+    @property
+    def h2d_bytes(self) -> int:
+        return self.inputs[0].nbytes
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.idx_host[0].numel() * self.idx_host[0].element_size()
+
+    def submit(self) -> int:
+        s = self._next
+        self._next ^= 1
+        if self._used[s]:
+            # the slot's device inputs are step i - 2's until it has computed
+            self.h2d_stream.wait_event(self._computed[s])
+        self.inputs[s].copy_in(self.h2d_stream)
+        self._in_ready[s].record(self.h2d_stream)
+        self.compute_stream.wait_event(self._in_ready[s])
+        if self.graphs is not None:
+            with torch.cuda.stream(self.compute_stream):
+                self.graphs[s].replay()
+        else:
+            self.steps[s].run(self.compute_stream)
+        self._computed[s].record(self.compute_stream)
+        self.d2h_stream.wait_event(self._computed[s])
+        with torch.cuda.stream(self.d2h_stream):
+            self.idx_host[s].copy_(self.steps[s].idx, non_blocking=True)
+        self._out_ready[s].record(self.d2h_stream)
+        self._used[s] = True
+        return s
+
+    def results(self, slot: int) -> torch.Tensor:
+        self._out_ready[slot].synchronize()
+        return self.idx_host[slot]
+
+    def synchronize(self) -> None:
+        for s in (self.h2d_stream, self.compute_stream, self.d2h_stream):
+            s.synchronize()

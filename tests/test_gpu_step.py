@@ -133,3 +133,38 @@ def test_full_step_full_size_sampled_rows():
         o, l = oracle.sparse_mla(case.q_mla[r:r + 1].cpu(), case.softmax_scale, oracle.FMT_FP8,
                                  cache, idx[r:r + 1], case.d_v, seq_of_row=[j])
         parity.check_mla(st.out[r:r + 1], st.lse[r:r + 1], o, l)
+
+
+def test_host_pipeline_matches_the_step_and_the_oracle():
+    """HostStepPipeline (inputs from pinned host memory, copies overlapping the
+    neighbouring steps' computation): slot 1 is given other context lengths
+    than slot 0, several steps run back to back, and every step's top-k indices
+    on the host equal those of the plain step on the same inputs; sampled rows
+    of the shorter-length slot also match the oracle."""
+    import dataclasses
+    from deepseek_sparse_attention_mqa_gb300.step import HostStepPipeline
+    case = inputs.make_case("decode", device="cuda")
+    orig = case.context_lens.cpu().numpy().copy()
+    shrunk = orig // 3
+    shrunk[:4] = [0, 1, 2047, 2048]
+    refs = []
+    for lens in (orig, shrunk):
+        c = dataclasses.replace(case, context_lens=torch.from_numpy(np.ascontiguousarray(lens, np.int32)).cuda())
+        st = SparseAttentionStep(c, with_mla=False)
+        st.run()
+        torch.cuda.synchronize()
+        refs.append((st.idx.cpu().numpy(), st))
+    pipe = HostStepPipeline(case)
+    pipe.inputs[1].host["context_lens"].copy_(torch.from_numpy(np.ascontiguousarray(shrunk, np.int32)))
+    for it in range(6):
+        slot = pipe.submit()
+        if it >= 1:
+            prev = slot ^ 1
+            got = pipe.results(prev).numpy()
+            assert np.array_equal(np.sort(got, axis=1), np.sort(refs[prev][0], axis=1)), "slot %d" % prev
+    pipe.synchronize()
+    for s in (0, 1):
+        assert np.array_equal(np.sort(pipe.results(s).numpy(), axis=1), np.sort(refs[s][0], axis=1))
+        assert pipe.steps[s].device_status() == 0
+    check_indexer_rows(dataclasses.replace(case, context_lens=refs[1][1].case.context_lens), refs[1][1],
+                       [0, 1, 2, 3, 17], shrunk)
