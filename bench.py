@@ -509,6 +509,22 @@ def measure_e2e(st, case, args, pairs, dev):
            "serial": {"value": round(pairs / (ms_serial * 1e-3) / 1e3, 1), "ms_per_step": round(ms_serial, 5),
                       "steps": n_serial}}
     del pipe
+    # the same loop with the two slots computing on their own streams, as for two
+    # independent batches (consecutive steps of one batch depend on each other)
+    pipe = HostStepPipeline(case, with_mla=False, fused=st.fused, overlap_steps=True)
+    for _ in range(4):
+        pipe.submit()
+    pipe.synchronize()
+    torch.cuda.synchronize()
+    e0.record(pipe.h2d_stream)
+    for _ in range(steps):
+        pipe.submit()
+    e1.record(pipe.d2h_stream)
+    e1.synchronize()
+    ms_ov = e0.elapsed_time(e1) / steps
+    res["independent_batches_overlapped"] = {"value": round(pairs / (ms_ov * 1e-3) / 1e3, 1),
+                                             "ms_per_step": round(ms_ov, 5), "steps": steps}
+    del pipe
     return res
 
 

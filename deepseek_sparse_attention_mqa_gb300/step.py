@@ -189,14 +189,22 @@ class HostStepPipeline:
     before submitting it to that slot.  With ``graphs`` (the default) each
     slot's computation is captured once in a CUDA graph and replayed, so a
     submission costs the host two copies, four event operations and one replay
-    instead of one library call per kernel."""
+    instead of one library call per kernel.  With ``overlap_steps`` the two
+    slots compute on streams of their own, so step i + 1 may start while step i
+    finishes: for independent batches (two decode steps of the same sequences
+    depend on each other and must not overlap)."""
 
-    def __init__(self, case: Case, with_mla: bool = False, fused: bool = False, graphs: bool = True):
+    def __init__(self, case: Case, with_mla: bool = False, fused: bool = False, graphs: bool = True,
+                 overlap_steps: bool = False):
         self.inputs = [StepInputs(case, with_mla=with_mla) for _ in range(2)]
         self.steps = [SparseAttentionStep(ins.case(), with_mla=with_mla, fused=fused) for ins in self.inputs]
         self.idx_host = [torch.empty(st.idx.shape, dtype=torch.int32).pin_memory() for st in self.steps]
         self.h2d_stream = torch.cuda.Stream()
         self.compute_stream = torch.cuda.Stream()
+        # with overlap_steps each slot computes on its own stream, so step i + 1 may
+        # start while step i finishes (the slots share no buffers)
+        self.compute_streams = ([self.compute_stream, torch.cuda.Stream()] if overlap_steps
+                                else [self.compute_stream, self.compute_stream])
         self.d2h_stream = torch.cuda.Stream()
         self._in_ready = [torch.cuda.Event() for _ in range(2)]
         self._computed = [torch.cuda.Event() for _ in range(2)]
@@ -204,7 +212,7 @@ class HostStepPipeline:
         self._used = [False, False]
         self._next = 0
         # the arenas were filled on the current stream at construction
-        for s in (self.h2d_stream, self.compute_stream, self.d2h_stream):
+        for s in (self.h2d_stream, self.d2h_stream, *self.compute_streams):
             s.wait_stream(torch.cuda.current_stream())
         self.graphs = None
         if graphs:
@@ -236,13 +244,14 @@ class HostStepPipeline:
             self.h2d_stream.wait_event(self._computed[s])
         self.inputs[s].copy_in(self.h2d_stream)
         self._in_ready[s].record(self.h2d_stream)
-        self.compute_stream.wait_event(self._in_ready[s])
+        cs = self.compute_streams[s]
+        cs.wait_event(self._in_ready[s])
         if self.graphs is not None:
-            with torch.cuda.stream(self.compute_stream):
+            with torch.cuda.stream(cs):
                 self.graphs[s].replay()
         else:
-            self.steps[s].run(self.compute_stream)
-        self._computed[s].record(self.compute_stream)
+            self.steps[s].run(cs)
+        self._computed[s].record(cs)
         self.d2h_stream.wait_event(self._computed[s])
         with torch.cuda.stream(self.d2h_stream):
             self.idx_host[s].copy_(self.steps[s].idx, non_blocking=True)
@@ -255,5 +264,5 @@ class HostStepPipeline:
         return self.idx_host[slot]
 
     def synchronize(self) -> None:
-        for s in (self.h2d_stream, self.compute_stream, self.d2h_stream):
+        for s in (self.h2d_stream, self.d2h_stream, *self.compute_streams):
             s.synchronize()

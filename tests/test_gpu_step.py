@@ -135,9 +135,11 @@ def test_full_step_full_size_sampled_rows():
         parity.check_mla(st.out[r:r + 1], st.lse[r:r + 1], o, l)
 
 
-def test_host_pipeline_matches_the_step_and_the_oracle():
+@pytest.mark.parametrize("overlap", [False, True])
+def test_host_pipeline_matches_the_step_and_the_oracle(overlap):
     """HostStepPipeline (inputs from pinned host memory, copies overlapping the
-    neighbouring steps' computation): slot 1 is given other context lengths
+    neighbouring steps' computation; with overlap, the two slots' computations
+    overlap too): slot 1 is given other context lengths
     than slot 0, several steps run back to back, and every step's top-k indices
     on the host equal those of the plain step on the same inputs; sampled rows
     of the shorter-length slot also match the oracle."""
@@ -154,7 +156,7 @@ def test_host_pipeline_matches_the_step_and_the_oracle():
         st.run()
         torch.cuda.synchronize()
         refs.append((st.idx.cpu().numpy(), st))
-    pipe = HostStepPipeline(case)
+    pipe = HostStepPipeline(case, overlap_steps=overlap)
     pipe.inputs[1].host["context_lens"].copy_(torch.from_numpy(np.ascontiguousarray(shrunk, np.int32)))
     for it in range(6):
         slot = pipe.submit()
