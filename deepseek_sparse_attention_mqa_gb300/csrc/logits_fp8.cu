@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "fused_topk.cuh"
@@ -530,8 +531,104 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const int s_base = w.tile_in_unit() * kTileTokens + tok;
             const uint32_t acc_base = tmem_base + static_cast<uint32_t>(acc) * acc_stride +
                                       (static_cast<uint32_t>(quarter * 32) << 16);
+            // Few heads: a unit of 4 columns (4 heads, one row) or 8 (8 heads, one
+            // row) has the columns of up to 8 or 4 of its 128-token blocks loaded
+            // before one wait -- one TMEM round trip per 32 registers instead of one
+            // per block.  Wider units take the per-block path below.
+            int m_first = 0;
+            if constexpr (H <= 8) {
+                const int ucols = ui.nrows * H;
+                auto batched = [&](auto width_tag, int cbase, bool last_window) {
+                    constexpr int W = decltype(width_tag)::value;
+                    constexpr int kBlocks = 32 / W;      // blocks per wait (32 registers)
+                    constexpr int kRows = W / H;         // unit rows in the W columns
+                    const int ib = cbase / H;            // first row of the window
+                    // per row: head weights, visible length and output row (kept in
+                    // registers for windows of at most two rows, else read per block)
+                    constexpr bool kHoist = kRows <= 2;
+                    constexpr int kHr = kHoist ? kRows : 1;
+                    float wr[kHr][H];
+                    int vis[kHr];
+                    float* orow[kHr];
+                    auto row_vis = [&](int i) -> int {
+                        const int row = ib + i;
+                        return row < ui.nrows ? min(visible_entries(L, p.next_n, i0 + row, p.ratio), p.logits_width) : 0;
+                    };
+                    auto row_out = [&](int i) -> float* {
+                        return p.logits + static_cast<int64_t>(ui.first_row + ib + i - p.row_begin) * p.logits_stride;
+                    };
+                    if constexpr (kHoist) {
+#pragma unroll
+                        for (int i = 0; i < kRows; ++i) {
+#pragma unroll
+                            for (int hh = 0; hh < H; ++hh)
+                                wr[i][hh] = wS[cbase + i * H + hh];
+                            vis[i] = row_vis(i);
+                            orow[i] = row_out(i);
+                        }
+                    }
+                    for (int m0 = 0; m0 < nt; m0 += kBlocks) {
+                        uint32_t r[kBlocks][W];
+#pragma unroll
+                        for (int mm = 0; mm < kBlocks; ++mm) {
+                            if (m0 + mm < nt) {
+                                const uint32_t ta = acc_base + (m0 + mm) * p.acc_cols + cbase;
+                                if constexpr (W == 4)
+                                    tmem_ld_32x32b_x4(ta, r[mm]);
+                                else if constexpr (W == 8)
+                                    tmem_ld_32x32b_x8(ta, r[mm]);
+                                else if constexpr (W == 16)
+                                    tmem_ld_32x32b_x16(ta, r[mm]);
+                                else
+                                    tmem_ld_32x32b_x32(ta, r[mm]);
+                            }
+                        }
+                        tmem_ld_wait();
+                        if (last_window && m0 + kBlocks >= nt) {
+                            // the last TMEM reads of this accumulator are in registers
+                            tc_fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(smem_u32(&acce_bar[acc]));
+                        }
+#pragma unroll
+                        for (int mm = 0; mm < kBlocks; ++mm) {
+                            if (m0 + mm >= nt)
+                                break;
+                            const int s = s_base + (m0 + mm) * kTileTokens;
+                            const float ks = myks[(m0 + mm) * 32 + lane];
+#pragma unroll
+                            for (int i = 0; i < kRows; ++i) {
+                                if (!kHoist && ib + i >= ui.nrows)
+                                    break;
+                                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                                for (int hh = 0; hh < H; hh += 2) {
+                                    const float w0 = kHoist ? wr[kHoist ? i : 0][hh] : wS[cbase + i * H + hh];
+                                    const float w1 = kHoist ? wr[kHoist ? i : 0][hh + 1] : wS[cbase + i * H + hh + 1];
+                                    a0 = fmaf(w0, fmaxf(__uint_as_float(r[mm][i * H + hh]), 0.f), a0);
+                                    a1 = fmaf(w1, fmaxf(__uint_as_float(r[mm][i * H + hh + 1]), 0.f), a1);
+                                }
+                                const int v = kHoist ? vis[kHoist ? i : 0] : row_vis(i);
+                                if (s < v)
+                                    (kHoist ? orow[kHoist ? i : 0] : row_out(i))[s] = ks * (a0 + a1);
+                            }
+                        }
+                    }
+                };
+                if constexpr (H <= 4) {
+                    if (ucols <= 4) {
+                        batched(std::integral_constant<int, 4>{}, 0, true);
+                        m_first = nt;                  // every block done
+                    }
+                }
+                if (H == 8 && m_first == 0 && ucols <= 8) {
+                    batched(std::integral_constant<int, 8>{}, 0, true);
+                    m_first = nt;
+                }
+            }
 #pragma unroll 1
-            for (int m = 0; m < nt; ++m) {
+            for (int m = m_first; m < nt; ++m) {
                 const int s = s_base + m * kTileTokens;
                 const float ks = myks[m * 32 + lane];
                 const uint32_t t_acc = acc_base + m * p.acc_cols;
@@ -601,10 +698,10 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         }
                     }
                 };
-                // two 32-column TMEM loads in flight per round, or one where the
-                // block is larger (heads <= 8: four epilogue warpgroups, fewer
-                // registers per thread)
-                constexpr int kPerRound = Fp8Roles<H>::kGroups == 2 ? 2 : 1;
+                // two 32-column TMEM loads in flight per round, one at H <= 8
+                // (units wider than 8 columns; the registers go to the batched
+                // path above)
+                constexpr int kPerRound = H <= 8 ? 1 : 2;
                 for (int c = 0; c < nchunks; c += kPerRound) {
                     uint32_t r[kPerRound][32];
                     tmem_ld_32x32b_x32(t_acc + c * 32, r[0]);
