@@ -334,3 +334,22 @@ def test_mxfp4_full_size_sampled_rows():
         for i in range(n):
             r = b * n + i
             parity.check_logits([g[r]], [o[i]], [parity.visible(case, r)])
+
+
+def test_schedule_of_another_call_sets_status_and_writes_nothing():
+    """A prebuilt schedule that does not describe the call (built for rows
+    [0, 1), passed to a call over rows [0, 2)) is refused on the device:
+    DSA_DEV_SCHEDULE is set and no logit is written."""
+    case = inputs.make_case("decode", device="cuda", lens=[300, 400], num_heads=16, head_dim=64,
+                            width=400, seed=14)
+    st = SparseAttentionStep(case, with_mla=False)
+    dev = torch.device("cuda")
+    n = _abi.schedule_bytes(case.batch, case.next_n, case.num_heads, 0, 2)
+    sched = torch.zeros(((n + 3) // 4,), dtype=torch.int32, device=dev)
+    _abi.build_schedule(case.context_lens, case.batch, case.next_n, case.num_heads, 0, 1, sched, st.status)
+    st.logits.fill_(float("nan"))
+    _abi.mqa_logits(case.q, case.q_scales, case.fmt, case.weights, case.num_heads, st.kcache,
+                    case.context_lens, case.batch, case.next_n, 0, 2, sched, st.logits, st.width, st.status)
+    torch.cuda.synchronize()
+    assert st.device_status() & _abi.DEV_SCHEDULE
+    assert np.all(np.isnan(st.logits[:2].cpu().numpy()))

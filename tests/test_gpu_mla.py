@@ -106,3 +106,36 @@ def test_fp8_latent_repeat_is_deterministic():
     a = run_mla(case, idx)
     b = run_mla(case, idx)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_index_outside_the_block_table_sets_status_and_is_skipped():
+    """A selected index past the sequence's block table, and one in a page the
+    table leaves unused, are reported as DSA_DEV_BAD_INDEX and contribute
+    nothing: the output equals the oracle's with those slots empty."""
+    case = inputs.make_case("full_step", device="cuda", lens=[3000, 2500], seed=35)
+    idx = random_indices(case, 256, 8)
+    P = case.latent.page_kv
+    max_pages = case.block_table.shape[1]
+    bad = idx.copy()
+    bad[0, 5] = max_pages * P + 10                      # beyond the table
+    bad[1, 7] = 2500 + 2 * P                             # row 1 (2500 tokens): a page the table leaves unused
+    assert int(case.block_table[1, (2500 + 2 * P) // P].item()) < 0
+    dev = torch.device("cuda")
+    lat = case.latent
+    cache = _abi.make_cache(lat.fmt, lat.head_dim, lat.page_kv, lat.num_pages, lat.values,
+                            lat.val_page_stride, lat.val_token_stride, lat.scales,
+                            lat.sc_page_stride, lat.sc_token_stride, case.block_table)
+    out = torch.full((case.rows, case.mla_heads, case.d_v), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((case.rows, case.mla_heads), float("nan"), dtype=torch.float32, device=dev)
+    st = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ws_n = _abi.mla_workspace_bytes(case.rows, case.mla_heads, case.d_qk, case.d_v, 256)
+    ws = torch.empty((max(ws_n, 16),), dtype=torch.uint8, device=dev)
+    _abi.sparse_mla(case.q_mla, case.softmax_scale, cache, torch.tensor(bad, device=dev), 256, out, lse,
+                    case.d_v, None, case.next_n, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & _abi.DEV_BAD_INDEX
+    expect = idx.copy()
+    expect[0, 5] = -1
+    expect[1, 7] = -1
+    ro, rl = oracle_mla(case, expect)
+    parity.check_mla(out, lse, ro, rl)
