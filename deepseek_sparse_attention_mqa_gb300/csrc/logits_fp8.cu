@@ -29,7 +29,9 @@
 //               tcgen05.ld of the thread's own lane, then the relu /
 //               head-weighting / k_scale reduction is thread-local (no
 //               shuffles, rows of a unit past its last row skipped), and each
-//               warp stores 32 consecutive logits per row.
+//               warp stores 32 consecutive logits per row.  A unit of only 4 or
+//               8 columns (4 or 8 heads, one row) has those columns of several
+//               blocks loaded before one wait.
 //   Up to eight TMEM accumulators let the epilogues of earlier super-tiles
 //   overlap the MMAs of later ones; the stage ring keeps K bytes in flight.
 //   Without a schedule buffer (at most kInlineUnits units) every CTA first
