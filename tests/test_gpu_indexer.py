@@ -86,7 +86,7 @@ def test_matrix(P, H, next_n, D):
     compare_all(case)
 
 
-@pytest.mark.parametrize("H,next_n", [(4, 1), (4, 3), (8, 2), (128, 1), (128, 3)])
+@pytest.mark.parametrize("H,next_n", [(4, 1), (4, 2), (4, 3), (8, 1), (8, 2), (128, 1), (128, 3)])
 def test_other_head_counts(H, next_n):
     case = inputs.make_case("decode", device="cuda", lens=[5, 130, 257, 1000], next_n=next_n,
                             num_heads=H, head_dim=32 if H <= 8 else 128, width=1024, seed=77 + H)
