@@ -146,9 +146,8 @@ __device__ __forceinline__ float ue8m0_to_float(uint32_t e)
 // Eight packed e2m1 values (element j in nibble j) -> eight e4m3 bytes (element
 // j in byte j).  Every e2m1 value is an e4m3 value: |x| codes 0..7 map to
 // 0x00 0x30 0x38 0x3C 0x40 0x44 0x48 0x4C and the sign moves to bit 7.
-__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w)
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8_tab(uint32_t w, uint32_t lo_tab, uint32_t hi_tab)
 {
-    const uint32_t lo_tab = 0x3C383000u, hi_tab = 0x4C484440u;
     const uint32_t lo16 = w & 0xFFFFu, hi16 = w >> 16;
     const uint32_t m0 = __byte_perm(lo_tab, hi_tab, lo16 & 0x7777u);
     const uint32_t s0 = __byte_perm(0u, 0x80808080u, (lo16 & 0x8888u) >> 1);
@@ -157,8 +156,47 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w)
     return make_uint2(m0 | s0, m1 | s1);
 }
 
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w)
+{
+    return e2m1x8_to_e4m3x8_tab(w, 0x3C383000u, 0x4C484440u);
+}
+
+// The byte-permute tables for e2m1 magnitudes (0, 0.5, 1, 1.5, 2, 3, 4, 6) times
+// 2^-s, 0 <= s <= 8: every such value is exactly an e4m3 value (normal down to
+// 2^-6, then a multiple of 2^-9), codes of magnitudes 0-3 in lo, 4-7 in hi.
+__device__ __forceinline__ void e2m1_shifted_tables(int s, uint32_t& lo, uint32_t& hi)
+{
+    const int kE[8] = {0, -1, 0, 0, 1, 1, 2, 2};      // exponent of each magnitude
+    const int kM[8] = {0, 0, 0, 4, 0, 4, 0, 4};       // its 3-bit e4m3 mantissa
+    uint32_t t[2] = {0u, 0u};
+#pragma unroll
+    for (int m = 1; m < 8; ++m) {
+        const int e = kE[m] - s;
+        const uint32_t code = e >= -6 ? static_cast<uint32_t>(((e + 7) << 3) | kM[m])
+                                      : static_cast<uint32_t>((8 + kM[m]) >> (-6 - e));
+        t[m >> 2] |= code << (8 * (m & 3));
+    }
+    lo = t[0];
+    hi = t[1];
+}
+
 // Widen one packed row (D/2 bytes at src, 16-byte aligned) into row `row` of a
 // swizzled K-major e4m3 tile.
+// The same with each 32-element block's values times 2^-shift[block] (tables from
+// e2m1_shifted_tables).
+template <int D>
+__device__ __forceinline__ void widen_row_tab(const uint8_t* src, uint8_t* tile, int row,
+                                              const uint32_t (&tab)[D / 32][2])
+{
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {                 // chunk c lies in block c / 2
+        const uint2 pk = *reinterpret_cast<const uint2*>(src + 8 * c);
+        const uint2 a = e2m1x8_to_e4m3x8_tab(pk.x, tab[c >> 1][0], tab[c >> 1][1]);
+        const uint2 b = e2m1x8_to_e4m3x8_tab(pk.y, tab[c >> 1][0], tab[c >> 1][1]);
+        *reinterpret_cast<uint4*>(tile + swizzled_offset(row, c, D)) = make_uint4(a.x, a.y, b.x, b.y);
+    }
+}
+
 template <int D>
 __device__ __forceinline__ void widen_row(const uint8_t* src, uint8_t* tile, int row)
 {
@@ -206,6 +244,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(smem + mp.misc);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + mp.misc + 4);
     volatile int* s_u0 = reinterpret_cast<volatile int*>(smem + mp.misc + 8);
+    volatile uint8_t* s_fold = smem + mp.misc + 12;  // [2] per q buffer: its unit's q exponents are folded
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the next kernel (the top-k, launched as a programmatic dependent) may
@@ -479,24 +518,58 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
             }
             const int64_t r0 = static_cast<int64_t>(ui.first_row) * H;
             const int nvalid = ui.nrows * H;
-            // q exponents straight from global memory (tiny), issued before the waits
-            float qs[8][NB];
+            // q exponents (ue8m0 codes) straight from global memory (tiny), issued
+            // before the waits; column c = lane + 32 k
+            uint32_t qc[8][NB];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int c = lane + 32 * k;
 #pragma unroll
                 for (int bk = 0; bk < NB; ++bk)
-                    qs[k][bk] = (c < p.w_cols && c < nvalid) ? ue8m0_to_float(p.q_scales[(r0 + c) * NB + bk]) : 0.f;
+                    qc[k][bk] = (c < p.w_cols && c < nvalid) ? static_cast<uint32_t>(p.q_scales[(r0 + c) * NB + bk])
+                                                             : 127u;
             }
+            // Folding: each column's blocks are widened times 2^(e_blk - e_max) and
+            // its weight times 2^(e_max - 127), so the epilogue drops the per-column
+            // scale.  Powers of two scale every product and sum exactly, so the logits
+            // are bit-identical, provided nothing leaves the normal range: the unit
+            // folds when every code is in [1, 254], a column's codes differ by at most 8
+            // (e4m3 holds e2m1 x 2^-8 exactly) and its largest is within 100 of 127.
+            uint32_t qmax[8];
+            bool fold_ok = true;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                uint32_t mx = qc[k][0], mn = qc[k][0];
+#pragma unroll
+                for (int bk = 1; bk < NB; ++bk) {
+                    mx = max(mx, qc[k][bk]);
+                    mn = min(mn, qc[k][bk]);
+                }
+                qmax[k] = mx;
+                fold_ok = fold_ok && mn >= 1u && mx <= 227u && mx >= 27u && mx - mn <= 8u;
+            }
+            const bool fold = __all_sync(0xffffffffu, fold_ok);
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&qraw_bar[qb]), (ucount >> 1) & 1) &&
                                              mbar_wait(smem_u32(&qe[qb]), ((ucount >> 1) & 1) ^ 1))) {
                 ok = false;
                 break;
             }
             uint8_t* qt = sQ + qb * p.q_buf_bytes;
-            for (int rr = lane; rr < p.n_cols; rr += 32) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int rr = lane + 32 * k;
+                if (rr >= p.n_cols)
+                    break;
                 if (rr < nvalid) {
-                    widen_row<D>(sQraw + qb * qraw_bytes + rr * (D / 2), qt, rr);
+                    if (fold) {
+                        uint32_t tab[NB][2];
+#pragma unroll
+                        for (int bk = 0; bk < NB; ++bk)
+                            e2m1_shifted_tables(static_cast<int>(qmax[k] - qc[k][bk]), tab[bk][0], tab[bk][1]);
+                        widen_row_tab<D>(sQraw + qb * qraw_bytes + rr * (D / 2), qt, rr, tab);
+                    } else {
+                        widen_row<D>(sQraw + qb * qraw_bytes + rr * (D / 2), qt, rr);
+                    }
                 } else {
 #pragma unroll
                     for (int c = 0; c < D / 16; ++c)
@@ -507,12 +580,15 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
             for (int k = 0; k < 8; ++k) {
                 const int c = lane + 32 * k;
                 if (c < p.w_cols) {
-                    sW[qb * p.w_cols + c] = c < nvalid ? sWraw[qb * p.w_cols + c] : 0.f;
+                    const float wv = c < nvalid ? sWraw[qb * p.w_cols + c] : 0.f;
+                    sW[qb * p.w_cols + c] = fold ? wv * ue8m0_to_float(qmax[k]) : wv;
 #pragma unroll
                     for (int bk = 0; bk < NB; ++bk)
-                        sSq[(qb * NB + bk) * p.w_cols + c] = qs[k][bk];
+                        sSq[(qb * NB + bk) * p.w_cols + c] = c < nvalid ? ue8m0_to_float(qc[k][bk]) : 0.f;
                 }
             }
+            if (lane == 0)
+                s_fold[qb] = fold ? 1 : 0;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
@@ -597,6 +673,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
         int L = 0, i0 = 0;
         const float* wS = sW;
         const float* sqS = sSq;
+        bool folded = false;                           // the unit's q exponents are in its q and weights
         for (int j = 0; w.valid() && group < p.n_grp && !__any_sync(0xffffffffu, *s_abort); ++j) {
             const UnitInfo& ui = w.w.ui;
             if (w.w.u != unit) {
@@ -610,6 +687,7 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
                 ++ucount;
                 wS = sW + qb * p.w_cols;
                 sqS = sSq + qb * NB * p.w_cols;
+                folded = s_fold[qb] != 0;
                 L = ui.ctx_len;
                 i0 = ui.first_row - ui.seq * p.next_n;
                 if (e == 0 && lane == 0 && p.status &&
@@ -667,10 +745,16 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
 #pragma unroll
                                 for (int u = 0; u < 2; ++u) {
                                     if (b0 + u < NB) {
-                                        const float* sq = sqS + (b0 + u) * p.w_cols + cb;
+                                        if (folded) {
 #pragma unroll
-                                        for (int q = 0; q < 16; ++q)
-                                            dot[q] = fmaf(sq[q] * sk[b0 + u], __uint_as_float(r[u][q]), dot[q]);
+                                            for (int q = 0; q < 16; ++q)
+                                                dot[q] = fmaf(sk[b0 + u], __uint_as_float(r[u][q]), dot[q]);
+                                        } else {
+                                            const float* sq = sqS + (b0 + u) * p.w_cols + cb;
+#pragma unroll
+                                            for (int q = 0; q < 16; ++q)
+                                                dot[q] = fmaf(sq[q] * sk[b0 + u], __uint_as_float(r[u][q]), dot[q]);
+                                        }
                                     }
                                 }
                             }

@@ -353,3 +353,18 @@ def test_schedule_of_another_call_sets_status_and_writes_nothing():
     torch.cuda.synchronize()
     assert st.device_status() & _abi.DEV_SCHEDULE
     assert np.all(np.isnan(st.logits[:2].cpu().numpy()))
+
+
+def test_mxfp4_q_block_exponents_far_apart():
+    """q whose block exponents within a head differ by more than 8 (block 0 of
+    every even head scaled by 2^12, block 1 of every odd head by 2^-10): the
+    kernel cannot fold them into its widened q and keeps them per block; the
+    logits still match the oracle, as do those of a unit whose codes are close."""
+    case = inputs.make_case("spec_mxfp4", device="cuda", lens=[0, 1, 63, 200, 511, 1000],
+                            width=1024, seed=52)
+    qs = case.q_scales.clone().to(torch.int32)
+    qs[:, 0::2, 0] += 12
+    qs[:, 1::2, 1] -= 10
+    assert int(qs.max()) <= 254 and int(qs.min()) >= 1
+    case.q_scales = qs.to(torch.uint8)
+    compare_all(case)
