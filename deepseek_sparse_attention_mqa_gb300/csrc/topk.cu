@@ -9,13 +9,15 @@
 // for a 64-row decode batch); CTA c owns a contiguous slice of the row, keeps it
 // in shared memory as order-preserving uint32 keys, and the cluster cooperates
 // through distributed shared memory with CTA 0 as the meeting point:
-//  1. key range [kmin, kmax] of the row: each CTA publishes its own, and after
-//     one cluster barrier every CTA reads all of them;
-//  2. 2048 bins over the range by a right shift -- bins uniform in bit-pattern
-//     space, i.e. log scale, so outliers and wide ranges cost nothing; one
-//     histogram round (local histograms added into CTA 0's) finds the bin of
-//     the k-th largest key, refined inside that bin while it is crowded; CTA 0
-//     pushes each decision into every CTA's shared memory;
+//  1. the slice's keys into shared memory; the barrier that publishes the
+//     zeroed counters to the cluster is split around this load (arrive before,
+//     wait after the first local histogram), so its latency is hidden;
+//  2. 2048 bins by a right shift, the first round over the whole key space (the
+//     key's top 11 bits) -- bins uniform in bit-pattern space, i.e. log scale,
+//     so outliers and wide ranges cost nothing; one histogram round (local
+//     histograms added into CTA 0's) finds the bin of the k-th largest key,
+//     refined inside that bin while it is crowded; CTA 0 pushes each decision
+//     into every CTA's shared memory;
 //  3. every position above that bin is written out directly (cluster-wide
 //     counter); the bin's few elements are appended to CTA 0 as candidates;
 //  4. CTA 0 resolves the candidates exactly by the 64-bit order (key, then lower
@@ -80,10 +82,8 @@ struct TopkShared {
     int cp[kCandCap];
     int ws[32];
     int bin, above, in_bin;       // histogram decision (pushed by CTA 0)
-    uint32_t rlo, rhi;            // the row's key range
     int nout, ncand;
     int res_above, res_cand;      // this CTA's reserved output / candidate ranges
-    uint32_t kmin, kmax;
 };
 
 // two CTAs per SM: a decode batch's clusters (e.g. 64 rows x 4 CTAs) fit in one wave
@@ -141,22 +141,19 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     const uint32_t c0_ck = mapa_shared(smem_u32(&sh.ck[0]), 0);
     const uint32_t c0_cp = mapa_shared(smem_u32(&sh.cp[0]), 0);
 
-    // Everything another CTA touches remotely is initialised before the first
-    // cluster barrier (the range barrier below), so no barrier is needed here:
-    // this CTA's own range and its first-round histogram, and CTA 0's output
-    // and candidate counters.
+    // Everything another CTA touches remotely (CTA 0's first-round histogram,
+    // output and candidate counters) is initialised before the first cluster
+    // barrier: arrived at here, waited on after the first local histogram.
     if (tid == 0) {
-        sh.kmin = 0xFFFFFFFFu;
-        sh.kmax = 0u;
         sh.nout = 0;
         sh.ncand = 0;
     }
     for (int j = tid; j < kBins; j += kThreads)
         sh.hist[j] = 0;
     __syncthreads();
+    cluster_arrive();
 
-    // ---- 1. keys of the slice and the row's key range
-    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    // ---- 1. keys of the slice
     {
         const float* src = row + s_lo;
         const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
@@ -174,8 +171,6 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
                     s_keys[4 * v + 2] = c;
                     s_keys[4 * v + 3] = d;
                 }
-                kmin = min(kmin, min(min(a, bb), min(c, d)));
-                kmax = max(kmax, max(max(a, bb), max(c, d)));
             }
             s0 = nv << 2;
         }
@@ -183,42 +178,13 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             const uint32_t a = float_key(__float_as_uint(__ldg(src + s)));
             if (kCached)
                 s_keys[s] = a;
-            kmin = min(kmin, a);
-            kmax = max(kmax, a);
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-    }
-    if (lane == 0 && n > 0) {
-        atomicMin(&sh.kmin, kmin);
-        atomicMax(&sh.kmax, kmax);
-    }
-    cluster_sync();                                       // every CTA's range and zeroed histogram
-    if (tid < 32) {
-        // lane c reads CTA c's range; the warp reduces them
-        uint32_t a = 0xFFFFFFFFu, z = 0u;
-        if (lane < C) {
-            a = ld_cluster_u32(mapa_shared(smem_u32(&sh.kmin), static_cast<uint32_t>(lane)));
-            z = ld_cluster_u32(mapa_shared(smem_u32(&sh.kmax), static_cast<uint32_t>(lane)));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
-            z = max(z, __shfl_xor_sync(0xffffffffu, z, o));
-        }
-        if (lane == 0) {
-            sh.rlo = a;
-            sh.rhi = z;
-        }
-    }
-    __syncthreads();
+    __syncthreads();                                      // the slice's keys are in shared memory
     auto key_at = [&](int j) -> uint32_t {               // j: index within the slice
         return kCached ? s_keys[j] : float_key(__float_as_uint(__ldg(row + s_lo + j)));
     };
-    uint32_t lo = sh.rlo, hi = sh.rhi;
+    uint32_t lo = 0u, hi = 0xFFFFFFFFu;
 
     // ---- 2. histogram rounds: the bin of the k-th largest key
     int need = k;                 // still to take from keys in [lo, hi]
@@ -226,7 +192,7 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         const uint64_t span = static_cast<uint64_t>(hi) - lo + 1;
         const int shift = max(0, log2_ceil_u64(span) - kBinBits);
         if (round > 0) {
-            // (the first round's histograms were zeroed before the range barrier)
+            // (the first round's histograms were zeroed before the first barrier)
             for (int j = tid; j < kBins; j += kThreads)
                 sh.hist[j] = 0;
             cluster_sync();                               // every histogram (CTA 0's too) zeroed
@@ -237,6 +203,8 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
                 atomicAdd(&sh.hist[(key - lo) >> shift], 1);
         }
         __syncthreads();
+        if (round == 0)
+            cluster_wait();                               // every CTA's counters are zeroed
         if (crank != 0)
             for (int j = tid; j < kBins; j += kThreads)
                 if (sh.hist[j])
