@@ -298,13 +298,20 @@ logits_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int lp_end = min(tiles_here * pages_per_tile, lp_vis);
                 const int cnt = min(kPageCache, max(lp_end - lp_first, npages));
                 __syncwarp();
-                for (int i = lane; i < cnt; i += 32) {
-                    const int lp = lp_first + i;
-                    int pg = -1;
-                    if (lp < lp_vis && lp < p.max_pages)
-                        pg = p.block_table[static_cast<int64_t>(ui.seq) * p.bt_stride + lp];
-                    my_pages[i] = pg;
+                // every load of the refill in flight before any store: one
+                // global-memory latency per refill instead of one per 32 pages
+                int pgv[kPageCache / 32];
+#pragma unroll
+                for (int k = 0; k < kPageCache / 32; ++k) {
+                    const int i = lane + 32 * k, lp = lp_first + i;
+                    pgv[k] = (i < cnt && lp < lp_vis && lp < p.max_pages)
+                                 ? __ldg(p.block_table + static_cast<int64_t>(ui.seq) * p.bt_stride + lp)
+                                 : -1;
                 }
+#pragma unroll
+                for (int k = 0; k < kPageCache / 32; ++k)
+                    if (lane + 32 * k < cnt)
+                        my_pages[lane + 32 * k] = pgv[k];
                 __syncwarp();
                 pc_unit = w.w.u;
                 pc_lp0 = lp_first;

@@ -200,12 +200,18 @@ __device__ __forceinline__ void widen_row_tab(const uint8_t* src, uint8_t* tile,
 template <int D>
 __device__ __forceinline__ void widen_row(const uint8_t* src, uint8_t* tile, int row)
 {
+    uint4 pk[D / 32];                                  // 16-byte loads: half the shared-memory wavefronts
 #pragma unroll
-    for (int c = 0; c < D / 16; ++c) {                 // one 16-element chunk = 8 packed bytes
-        const uint2 pk = *reinterpret_cast<const uint2*>(src + 8 * c);
-        const uint2 a = e2m1x8_to_e4m3x8(pk.x);
-        const uint2 b = e2m1x8_to_e4m3x8(pk.y);
-        *reinterpret_cast<uint4*>(tile + swizzled_offset(row, c, D)) = make_uint4(a.x, a.y, b.x, b.y);
+    for (int c = 0; c < D / 32; ++c)                   // two 16-element chunks = 16 packed bytes
+        pk[c] = *reinterpret_cast<const uint4*>(src + 16 * c);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        const uint2 a = e2m1x8_to_e4m3x8(pk[c].x);
+        const uint2 b = e2m1x8_to_e4m3x8(pk[c].y);
+        const uint2 a2 = e2m1x8_to_e4m3x8(pk[c].z);
+        const uint2 b2 = e2m1x8_to_e4m3x8(pk[c].w);
+        *reinterpret_cast<uint4*>(tile + swizzled_offset(row, 2 * c, D)) = make_uint4(a.x, a.y, b.x, b.y);
+        *reinterpret_cast<uint4*>(tile + swizzled_offset(row, 2 * c + 1, D)) = make_uint4(a2.x, a2.y, b2.x, b2.y);
     }
 }
 
@@ -370,13 +376,20 @@ logits_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_k, const Mx4Params p)
                 const int lp_end = min(tiles_here * ppt, lp_vis);
                 const int cnt = min(kPageCache, max(lp_end - lp_first, npages));
                 __syncwarp();
-                for (int i = lane; i < cnt; i += 32) {
-                    const int lp = lp_first + i;
-                    int pg = -1;
-                    if (lp < lp_vis && lp < p.max_pages)
-                        pg = p.block_table[static_cast<int64_t>(ui.seq) * p.bt_stride + lp];
-                    my_pages[i] = pg;
+                // every load of the refill in flight before any store: one
+                // global-memory latency per refill instead of one per 32 pages
+                int pgv[kPageCache / 32];
+#pragma unroll
+                for (int k = 0; k < kPageCache / 32; ++k) {
+                    const int i = lane + 32 * k, lp = lp_first + i;
+                    pgv[k] = (i < cnt && lp < lp_vis && lp < p.max_pages)
+                                 ? __ldg(p.block_table + static_cast<int64_t>(ui.seq) * p.bt_stride + lp)
+                                 : -1;
                 }
+#pragma unroll
+                for (int k = 0; k < kPageCache / 32; ++k)
+                    if (lane + 32 * k < cnt)
+                        my_pages[lane + 32 * k] = pgv[k];
                 __syncwarp();
                 pc_unit = w.w.u;
                 pc_lp0 = lp_first;
