@@ -14,10 +14,11 @@
 //     wait after the first local histogram), so its latency is hidden;
 //  2. 2048 bins by a right shift, the first round over the whole key space (the
 //     key's top 11 bits) -- bins uniform in bit-pattern space, i.e. log scale,
-//     so outliers and wide ranges cost nothing; one histogram round (local
-//     histograms added into CTA 0's) finds the bin of the k-th largest key,
-//     refined inside that bin while it is crowded; CTA 0 pushes each decision
-//     into every CTA's shared memory;
+//     so outliers and wide ranges cost nothing; one histogram round finds the
+//     bin of the k-th largest key, refined inside that bin while it is
+//     crowded.  Each CTA adds its counts into every CTA's copy of the row
+//     histogram, so after one cluster barrier every CTA scans the same counts
+//     and takes the same decision, with no broadcast and no second barrier;
 //  3. every position above that bin is written out directly (cluster-wide
 //     counter); the bin's few elements are appended to CTA 0 as candidates;
 //  4. CTA 0 resolves the candidates exactly by the 64-bit order (key, then lower
@@ -77,11 +78,11 @@ __device__ __forceinline__ int block_incl_scan(int v, int* ws, int* total)
 }
 
 struct TopkShared {
-    int hist[kBins];
+    int hist[kBins];              // the row's histogram: every CTA adds its counts into every CTA's copy
     uint32_t ck[kCandCap];
-    int cp[kCandCap];
+    int cp[kCandCap];             // also this CTA's own histogram during the rounds
     int ws[32];
-    int bin, above, in_bin;       // histogram decision (pushed by CTA 0)
+    int bin, above, in_bin;       // histogram decision (taken by every CTA alike)
     int nout, ncand;
     int res_above, res_cand;      // this CTA's reserved output / candidate ranges
 };
@@ -135,21 +136,24 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     const int n = s_hi - s_lo;
 
     // CTA 0's copies of the shared reduction state (cluster addresses)
-    const uint32_t c0_hist = mapa_shared(smem_u32(&sh.hist[0]), 0);
     const uint32_t c0_nout = mapa_shared(smem_u32(&sh.nout), 0);
     const uint32_t c0_ncand = mapa_shared(smem_u32(&sh.ncand), 0);
     const uint32_t c0_ck = mapa_shared(smem_u32(&sh.ck[0]), 0);
     const uint32_t c0_cp = mapa_shared(smem_u32(&sh.cp[0]), 0);
 
-    // Everything another CTA touches remotely (CTA 0's first-round histogram,
-    // output and candidate counters) is initialised before the first cluster
-    // barrier: arrived at here, waited on after the first local histogram.
+    // Everything another CTA touches remotely (every CTA's first-round row
+    // histogram, CTA 0's output and candidate counters) is initialised before
+    // the first cluster barrier: arrived at here, waited on after the first
+    // local histogram.
+    int* own = sh.cp;                                     // this CTA's histogram (candidates come later)
     if (tid == 0) {
         sh.nout = 0;
         sh.ncand = 0;
     }
-    for (int j = tid; j < kBins; j += kThreads)
+    for (int j = tid; j < kBins; j += kThreads) {
         sh.hist[j] = 0;
+        own[j] = 0;
+    }
     __syncthreads();
     cluster_arrive();
 
@@ -186,31 +190,40 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     };
     uint32_t lo = 0u, hi = 0xFFFFFFFFu;
 
-    // ---- 2. histogram rounds: the bin of the k-th largest key
+    // ---- 2. histogram rounds: the bin of the k-th largest key.  Each CTA adds
+    // its counts into every CTA's row histogram, so after one cluster barrier
+    // every CTA scans the same histogram and takes the same decision itself.
     int need = k;                 // still to take from keys in [lo, hi]
     for (int round = 0;; ++round) {
         const uint64_t span = static_cast<uint64_t>(hi) - lo + 1;
         const int shift = max(0, log2_ceil_u64(span) - kBinBits);
         if (round > 0) {
-            // (the first round's histograms were zeroed before the first barrier)
-            for (int j = tid; j < kBins; j += kThreads)
+            // (the first round's histograms were zeroed before the first barrier;
+            // each CTA has read its row histogram for the last decision)
+            for (int j = tid; j < kBins; j += kThreads) {
                 sh.hist[j] = 0;
-            cluster_sync();                               // every histogram (CTA 0's too) zeroed
+                own[j] = 0;
+            }
+            cluster_sync();                               // every row histogram zeroed
         }
         for (int j = tid; j < n; j += kThreads) {
             const uint32_t key = key_at(j);
             if (key >= lo && key <= hi)
-                atomicAdd(&sh.hist[(key - lo) >> shift], 1);
+                atomicAdd(&own[(key - lo) >> shift], 1);
         }
         __syncthreads();
         if (round == 0)
             cluster_wait();                               // every CTA's counters are zeroed
-        if (crank != 0)
-            for (int j = tid; j < kBins; j += kThreads)
-                if (sh.hist[j])
-                    red_add_cluster(c0_hist + 4u * j, static_cast<uint32_t>(sh.hist[j]));
-        cluster_sync();                                   // CTA 0 holds the row histogram
-        if (crank == 0) {
+        for (int j = tid; j < kBins; j += kThreads) {
+            const int v = own[j];
+            if (v) {
+                const uint32_t a = smem_u32(&sh.hist[j]);
+                for (int cr = 0; cr < C; ++cr)
+                    red_add_cluster(mapa_shared(a, static_cast<uint32_t>(cr)), static_cast<uint32_t>(v));
+            }
+        }
+        cluster_sync();                                   // every CTA holds the row histogram
+        {
             // suffix counts from the top bin down: thread t owns bins 2047-4t .. 2044-4t
             int c[4], loc = 0;
 #pragma unroll
@@ -225,20 +238,16 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if (before + c[q] >= need) {
-                        // the decision goes to every CTA of the cluster
-                        const int db = kBins - 1 - 4 * tid - q;
-                        for (int cr = 0; cr < C; ++cr) {
-                            st_cluster_u32(mapa_shared(smem_u32(&sh.bin), cr), static_cast<uint32_t>(db));
-                            st_cluster_u32(mapa_shared(smem_u32(&sh.above), cr), static_cast<uint32_t>(before));
-                            st_cluster_u32(mapa_shared(smem_u32(&sh.in_bin), cr), static_cast<uint32_t>(c[q]));
-                        }
+                        sh.bin = kBins - 1 - 4 * tid - q;
+                        sh.above = before;
+                        sh.in_bin = c[q];
                         break;
                     }
                     before += c[q];
                 }
             }
         }
-        cluster_sync();                                   // decision in every CTA
+        __syncthreads();                                  // the decision
         const int bin = sh.bin;
         need -= sh.above;
         const int in_bin = sh.in_bin;
