@@ -126,8 +126,6 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         }
         return;
     }
-    if (crank == 0 && tid == 0 && count)
-        count[rloc] = k;
 
     // this CTA's slice [s_lo, s_hi) of the visible row (slice starts 16-byte aligned)
     const int slice = (((vis + C - 1) / C) + 3) & ~3;
@@ -289,13 +287,14 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         sh.res_cand = tot_cand ? static_cast<int>(atom_add_cluster(c0_ncand, static_cast<uint32_t>(tot_cand))) : 0;
     }
     __syncthreads();
+    // The candidates go to CTA 0 first and the barrier that publishes them is
+    // arrived at before the positions above the bin are written: its release
+    // then waits only for the shared-memory stores, not for the global ones.
     {
-        int oa = sh.res_above + off_above, oc = sh.res_cand + off_cand;
+        int oc = sh.res_cand + off_cand;
         for (int j = tid; j < n; j += kThreads) {
             const uint32_t key = key_at(j);
-            if (key > hi) {
-                out[oa++] = s_lo + j;
-            } else if (key >= lo) {
+            if (key >= lo && key <= hi) {
                 if (oc < kCandCap) {
                     st_cluster_u32(c0_ck + 4u * oc, key);
                     st_cluster_u32(c0_cp + 4u * oc, static_cast<uint32_t>(s_lo + j));
@@ -304,9 +303,18 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             }
         }
     }
-    cluster_sync();                                       // all candidates landed in CTA 0
+    cluster_arrive();
+    {
+        int oa = sh.res_above + off_above;
+        for (int j = tid; j < n; j += kThreads)
+            if (key_at(j) > hi)
+                out[oa++] = s_lo + j;
+    }
+    cluster_wait();                                       // all candidates landed in CTA 0
     if (crank != 0)
         return;
+    if (tid == 0 && count)
+        count[rloc] = k;
 
     // ---- 4. CTA 0: the `need` best candidates by (key desc, position asc).
     // Radix selection on o = (key - lo) << 32 | ~position, 11 bits at a time
