@@ -71,12 +71,16 @@ def topk_cluster_size(rows, width, sm_count):
     (64, 32768, 2048, 4),      # the decode workload's launch: 64 rows x 32768
     (256, 65536, 512, 4),      # the speculative workload's launch: 128 x 2 rows x 65536
     (320, 16384, 2048, 1),     # a prefill chunk's launch shape: >= 304 rows x 16384
+    (64, 131072, 2048, 8),     # the full step's launch: 64 rows x 131072
+    (160, 32768, 2048, 2),     # two CTAs per row
 ])
 def test_workload_launch_shapes_exact(rows, width, k, expect_c):
     """Same logits on both sides at the row counts and widths the real workloads
     launch with, so the cluster sizes they run at (4 CTAs per row for decode and
     speculative decode, 1 for prefill chunks) are compared with the oracle's
-    full sort: identical index sets, ties to the lower position."""
+    full sort: identical index sets, ties to the lower position.  Some rows put
+    every key in one first-round bin (distinct values in [1, 1.25), the top 11
+    key bits), so the histogram is refined in further rounds across the cluster."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if sms == 152:
         assert topk_cluster_size(rows, width, sms) == expect_c
@@ -86,6 +90,7 @@ def test_workload_launch_shapes_exact(rows, width, k, expect_c):
     logits = torch.randn((rows, width), generator=g)
     logits[2::7] = torch.round(logits[2::7] * 4)         # rows full of exact ties
     logits[3::11, ::3] = 2.5                             # a heavy tie at the top
+    logits[4::13] = 1.0 + 0.25 * torch.rand((logits[4::13].shape[0], width), generator=g)
     idx, cnt, st = run_topk(logits, lens, 1, k, width)
     assert st == 0
     ref_idx, ref_cnt = oracle.topk(logits.double().numpy(), lens, 1, k)
