@@ -48,11 +48,6 @@ __device__ __forceinline__ UnitInfo unit_info(const SchedUnit& su)
     return ui;
 }
 
-__device__ __forceinline__ UnitInfo load_unit(const WalkParams&, const SchedUnit* units, int, int u)
-{
-    return unit_info(fetch_unit(units, u));
-}
-
 // Last unit whose tile_begin <= t (units with no tiles are skipped naturally).
 __device__ __forceinline__ int find_unit(const SchedUnit* units, int num_units, int t)
 {

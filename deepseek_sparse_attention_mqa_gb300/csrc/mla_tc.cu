@@ -692,8 +692,9 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const MlaParams p
                 sc2[2 * u + 1] = add_f32x2(sc2[2 * u + 1], x.y);
             }
             // X is consumed (its values are in registers): hand it back to the
-            // peer.  A relaxed arrive: a releasing one would also wait for this
-            // thread's st.async to the peer to complete.
+            // peer.  A relaxed arrive: the peer only learns that the slice was
+            // read, and a releasing one would wait for this warp's earlier
+            // memory operations to complete first.
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_remote_relaxed(peer_free);

@@ -397,22 +397,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-// 16-byte asynchronous store into another CTA's shared memory; its bytes
-// complete the transaction count of that CTA's mbarrier (both cluster addresses).
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t remote_bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
-                 : "memory");
-}
-
 // ------------------------------------------- programmatic dependent launch
 
 // Lets the next kernel in the stream (launched with programmatic stream
@@ -447,13 +431,6 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src,
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
-// prior writes (including remote shared-memory stores) at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Arrive on an mbarrier of another CTA of the cluster without ordering this
@@ -530,26 +507,9 @@ __device__ __forceinline__ uint32_t atom_add_cluster(uint32_t cluster_addr, uint
     return old;
 }
 
-__device__ __forceinline__ void red_min_cluster(uint32_t cluster_addr, uint32_t v)
-{
-    asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_max_cluster(uint32_t cluster_addr, uint32_t v)
-{
-    asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void red_add_cluster(uint32_t cluster_addr, uint32_t v)
 {
     asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v)

@@ -8,7 +8,8 @@
 // A cluster of C CTAs per row (C = 1..8, chosen so that all SMs have work even
 // for a 64-row decode batch); CTA c owns a contiguous slice of the row, keeps it
 // in shared memory as order-preserving uint32 keys, and the cluster cooperates
-// through distributed shared memory with CTA 0 as the meeting point:
+// through distributed shared memory (CTA 0 collects the output counters and
+// the candidates):
 //  1. the slice's keys into shared memory; the barrier that publishes the
 //     zeroed counters to the cluster is split around this load (arrive before,
 //     wait after the first local histogram), so its latency is hidden;
