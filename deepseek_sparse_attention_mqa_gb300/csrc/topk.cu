@@ -99,13 +99,32 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     extern __shared__ uint32_t s_keys[];                 // [slice] when kCached
     __shared__ TopkShared sh;
 
-    // launched as a programmatic dependent of the previous kernel of the stream:
-    // nothing it may have written is read before this wait (the launch latency
-    // is what overlaps); the MLA that follows may then start its blocks
-    pdl_wait();
-    pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t crank = cluster_ctarank();
+
+    // Everything another CTA touches remotely (every CTA's first-round row
+    // histogram, CTA 0's output and candidate counters) is initialised before
+    // the first cluster barrier: arrived at here, waited on after the first
+    // local histogram.  This touches shared memory only, so it runs before the
+    // wait below, while the previous kernel finishes.
+    int* own = sh.cp;                                     // this CTA's histogram (candidates come later)
+    if (tid == 0) {
+        sh.nout = 0;
+        sh.ncand = 0;
+    }
+    for (int j = tid; j < kBins; j += kThreads) {
+        sh.hist[j] = 0;
+        own[j] = 0;
+    }
+    __syncthreads();
+    cluster_arrive();
+
+    // launched as a programmatic dependent of the previous kernel of the stream:
+    // nothing it may have written is read before this wait (the launch latency
+    // and the set-up above are what overlap); the MLA that follows may then
+    // start its blocks
+    pdl_wait();
+    pdl_launch_dependents();
     const int C = static_cast<int>(gridDim.x);           // cluster spans gridDim.x
     const int rloc = blockIdx.y;
     const int r = row_begin + rloc;
@@ -125,6 +144,7 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             for (int s = tid; s < k; s += kThreads)
                 out[s] = s < vis ? s : -1;
         }
+        cluster_wait();                                   // the arrive above is matched before leaving
         return;
     }
 
@@ -139,22 +159,6 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     const uint32_t c0_ncand = mapa_shared(smem_u32(&sh.ncand), 0);
     const uint32_t c0_ck = mapa_shared(smem_u32(&sh.ck[0]), 0);
     const uint32_t c0_cp = mapa_shared(smem_u32(&sh.cp[0]), 0);
-
-    // Everything another CTA touches remotely (every CTA's first-round row
-    // histogram, CTA 0's output and candidate counters) is initialised before
-    // the first cluster barrier: arrived at here, waited on after the first
-    // local histogram.
-    int* own = sh.cp;                                     // this CTA's histogram (candidates come later)
-    if (tid == 0) {
-        sh.nout = 0;
-        sh.ncand = 0;
-    }
-    for (int j = tid; j < kBins; j += kThreads) {
-        sh.hist[j] = 0;
-        own[j] = 0;
-    }
-    __syncthreads();
-    cluster_arrive();
 
     // ---- 1. keys of the slice
     {
