@@ -160,7 +160,9 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     const uint32_t c0_ck = mapa_shared(smem_u32(&sh.ck[0]), 0);
     const uint32_t c0_cp = mapa_shared(smem_u32(&sh.cp[0]), 0);
 
-    // ---- 1. keys of the slice
+    // ---- 1. keys of the slice, counted into the first round's local histogram
+    // as they are loaded (that round's bins are the key's top 11 bits)
+    constexpr int kFirstShift = 32 - kBinBits;
     {
         const float* src = row + s_lo;
         const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0);
@@ -178,6 +180,10 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
                     s_keys[4 * v + 2] = c;
                     s_keys[4 * v + 3] = d;
                 }
+                atomicAdd(&own[a >> kFirstShift], 1);
+                atomicAdd(&own[bb >> kFirstShift], 1);
+                atomicAdd(&own[c >> kFirstShift], 1);
+                atomicAdd(&own[d >> kFirstShift], 1);
             }
             s0 = nv << 2;
         }
@@ -185,9 +191,10 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             const uint32_t a = float_key(__float_as_uint(__ldg(src + s)));
             if (kCached)
                 s_keys[s] = a;
+            atomicAdd(&own[a >> kFirstShift], 1);
         }
     }
-    __syncthreads();                                      // the slice's keys are in shared memory
+    __syncthreads();                                      // keys and first-round counts are in place
     auto key_at = [&](int j) -> uint32_t {               // j: index within the slice
         return kCached ? s_keys[j] : float_key(__float_as_uint(__ldg(row + s_lo + j)));
     };
@@ -208,15 +215,16 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
                 own[j] = 0;
             }
             cluster_sync();                               // every row histogram zeroed
-        }
-        for (int j = tid; j < n; j += kThreads) {
-            const uint32_t key = key_at(j);
-            if (key >= lo && key <= hi)
-                atomicAdd(&own[(key - lo) >> shift], 1);
-        }
-        __syncthreads();
-        if (round == 0)
+            for (int j = tid; j < n; j += kThreads) {
+                const uint32_t key = key_at(j);
+                if (key >= lo && key <= hi)
+                    atomicAdd(&own[(key - lo) >> shift], 1);
+            }
+            __syncthreads();
+        } else {
+            // (this CTA's first-round counts were taken as its keys were loaded)
             cluster_wait();                               // every CTA's counters are zeroed
+        }
         for (int j = tid; j < kBins; j += kThreads) {
             const int v = own[j];
             if (v) {
