@@ -89,7 +89,7 @@ struct TopkShared {
 };
 
 // two CTAs per SM: a decode batch's clusters (e.g. 64 rows x 4 CTAs) fit in one wave
-template <bool kCached>
+template <bool kCached, bool kSolo>
 __global__ void __launch_bounds__(kThreads, 2)
 topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             const int32_t* __restrict__ context_lens, int next_n, int ratio, int row_begin, int k,
@@ -101,6 +101,10 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
 
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t crank = cluster_ctarank();
+    const int C = static_cast<int>(gridDim.x);           // cluster spans gridDim.x
+    // kSolo (launched with C = 1): a row handled by one CTA, with block
+    // barriers and local shared memory instead of the cluster's
+    constexpr bool solo = kSolo;
 
     // Everything another CTA touches remotely (every CTA's first-round row
     // histogram, CTA 0's output and candidate counters) is initialised before
@@ -117,7 +121,8 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         own[j] = 0;
     }
     __syncthreads();
-    cluster_arrive();
+    if (!solo)
+        cluster_arrive();
 
     // launched as a programmatic dependent of the previous kernel of the stream:
     // nothing it may have written is read before this wait (the launch latency
@@ -125,7 +130,6 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
     // start its blocks
     pdl_wait();
     pdl_launch_dependents();
-    const int C = static_cast<int>(gridDim.x);           // cluster spans gridDim.x
     const int rloc = blockIdx.y;
     const int r = row_begin + rloc;
     const int b = r / next_n, i = r % next_n;
@@ -144,7 +148,8 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             for (int s = tid; s < k; s += kThreads)
                 out[s] = s < vis ? s : -1;
         }
-        cluster_wait();                                   // the arrive above is matched before leaving
+        if (!solo)
+            cluster_wait();                               // the arrive above is matched before leaving
         return;
     }
 
@@ -214,7 +219,10 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
                 sh.hist[j] = 0;
                 own[j] = 0;
             }
-            cluster_sync();                               // every row histogram zeroed
+            if (solo)
+                __syncthreads();
+            else
+                cluster_sync();                           // every row histogram zeroed
             for (int j = tid; j < n; j += kThreads) {
                 const uint32_t key = key_at(j);
                 if (key >= lo && key <= hi)
@@ -223,17 +231,23 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             __syncthreads();
         } else {
             // (this CTA's first-round counts were taken as its keys were loaded)
-            cluster_wait();                               // every CTA's counters are zeroed
+            if (!solo)
+                cluster_wait();                           // every CTA's counters are zeroed
         }
         for (int j = tid; j < kBins; j += kThreads) {
             const int v = own[j];
-            if (v) {
+            if (v && solo) {
+                sh.hist[j] = v;
+            } else if (v) {
                 const uint32_t a = smem_u32(&sh.hist[j]);
                 for (int cr = 0; cr < C; ++cr)
                     red_add_cluster(mapa_shared(a, static_cast<uint32_t>(cr)), static_cast<uint32_t>(v));
             }
         }
-        cluster_sync();                                   // every CTA holds the row histogram
+        if (solo)
+            __syncthreads();
+        else
+            cluster_sync();                               // every CTA holds the row histogram
         {
             // suffix counts from the top bin down: thread t owns bins 2047-4t .. 2044-4t
             int c[4], loc = 0;
@@ -295,7 +309,12 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         off_above = block_incl_scan(n_above, sh.ws, &tot_above) - n_above;
         off_cand = block_incl_scan(n_cand, sh.ws, &tot_cand) - n_cand;
     }
-    if (tid == 0) {
+    if (tid == 0 && solo) {
+        sh.res_above = 0;
+        sh.res_cand = 0;
+        sh.nout = tot_above;
+        sh.ncand = tot_cand;
+    } else if (tid == 0) {
         sh.res_above = tot_above ? static_cast<int>(atom_add_cluster(c0_nout, static_cast<uint32_t>(tot_above))) : 0;
         sh.res_cand = tot_cand ? static_cast<int>(atom_add_cluster(c0_ncand, static_cast<uint32_t>(tot_cand))) : 0;
     }
@@ -308,7 +327,10 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
         for (int j = tid; j < n; j += kThreads) {
             const uint32_t key = key_at(j);
             if (key >= lo && key <= hi) {
-                if (oc < kCandCap) {
+                if (oc < kCandCap && solo) {
+                    sh.ck[oc] = key;
+                    sh.cp[oc] = s_lo + j;
+                } else if (oc < kCandCap) {
                     st_cluster_u32(c0_ck + 4u * oc, key);
                     st_cluster_u32(c0_cp + 4u * oc, static_cast<uint32_t>(s_lo + j));
                 }
@@ -316,14 +338,18 @@ topk_kernel(const float* __restrict__ logits, int64_t stride, int width,
             }
         }
     }
-    cluster_arrive();
+    if (!solo)
+        cluster_arrive();
     {
         int oa = sh.res_above + off_above;
         for (int j = tid; j < n; j += kThreads)
             if (key_at(j) > hi)
                 out[oa++] = s_lo + j;
     }
-    cluster_wait();                                       // all candidates landed in CTA 0
+    if (solo)
+        __syncthreads();
+    else
+        cluster_wait();                                   // all candidates landed in CTA 0
     if (crank != 0)
         return;
     if (tid == 0 && count)
@@ -469,14 +495,17 @@ dsa_status launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t st
     cfg.numAttrs = 2;
     cudaError_t e;
     if (cached) {
-        e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // one CTA per row (C = 1) gets its own instantiation without cluster operations
+        auto kern = C == 1 ? topk_kernel<true, true> : topk_kernel<true, false>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return cuda_fail(e);
-        e = cudaLaunchKernelEx(&cfg, topk_kernel<true>, a.logits, a.logits_row_stride, a.logits_width,
+        e = cudaLaunchKernelEx(&cfg, kern, a.logits, a.logits_row_stride, a.logits_width,
                                a.context_lens, a.next_n, a.ratio, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
                                a.status);
     } else {
-        e = cudaLaunchKernelEx(&cfg, topk_kernel<false>, a.logits, a.logits_row_stride, a.logits_width,
+        // (a slice above the shared-memory cap happens only at the largest cluster)
+        e = cudaLaunchKernelEx(&cfg, topk_kernel<false, false>, a.logits, a.logits_row_stride, a.logits_width,
                                a.context_lens, a.next_n, a.ratio, a.row_begin, a.k, a.idx, a.idx_row_stride, a.count,
                                a.status);
     }
