@@ -26,6 +26,9 @@
 //     position), the same order as a full sort with ties broken by position:
 //     by ranking each candidate against the others when there are at most 256,
 //     else with a parallel radix selection (11-bit digits, block-wide scans).
+// A launch with one CTA per row (C = 1, prefill chunks) runs its own
+// instantiation, with block barriers and local shared memory in place of the
+// cluster's barriers and distributed shared memory.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
